@@ -1,0 +1,250 @@
+"""Checks that pin the CPU oracle to facts outside itself.
+
+Each ``pin_*`` takes the implementation(s) under test as arguments and raises
+AssertionError when a fact fails.  ``test_oracle_pins.py`` runs them on the
+oracle; ``test_oracle_mutants.py`` runs them on copies of the oracle with one
+planted mistake each and expects a failure, which shows that the pins can see
+those mistakes.
+
+Facts used (none of them is the oracle's own code):
+* closed forms of softmax attention (q = 0, constant V, first causal row,
+  one dominant key);
+* a pure-Python brute force over tiny inputs;
+* ``torch.nn.functional.scaled_dot_product_attention`` and
+  ``torch.logsumexp`` in float64, library routines the oracle does not call;
+* the identity the pages state: the ring's online-softmax result equals the
+  full-row result ("Ring Attention and Ulysses shard a sequence two different
+  ways...", the worked example printing True; "Interrogating parallelism,
+  part 5", "How does attention survive being split?");
+* the zigzag pairing and the per-rank work counts printed in "Interrogating
+  parallelism, part 5", "What breaks the load balance?" (fixtures in
+  ``tests/golden/``).
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def read_golden(name: str) -> list[list[str]]:
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+def rand(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+# --------------------------------------------------------------------------- full attention
+
+def brute_force(q, k, v, causal):
+    """Pure-Python loops, math.exp only; tiny inputs."""
+    Hq, S, d = q.shape
+    g = Hq // k.shape[0]
+    out = [[[0.0] * d for _ in range(S)] for _ in range(Hq)]
+    lse = [[0.0] * S for _ in range(Hq)]
+    for h in range(Hq):
+        kh = h // g
+        for i in range(S):
+            keys = [j for j in range(S) if (not causal or j <= i)]
+            sc = [sum(float(q[h][i][t]) * float(k[kh][j][t]) for t in range(d)) for j in keys]
+            M = max(sc)
+            w = [math.exp(s - M) for s in sc]
+            L = sum(w)
+            for t in range(d):
+                out[h][i][t] = sum(w[n] * float(v[kh][j][t]) for n, j in enumerate(keys)) / L
+            lse[h][i] = M + math.log(L)
+    return np.array(out), np.array(lse)
+
+
+def pin_full_brute(full_fn):
+    for causal in (False, True):
+        for (Hq, Hkv, S, d, seed) in ((1, 1, 5, 3, 10), (4, 2, 7, 4, 11), (2, 1, 9, 2, 12)):
+            q, k, v = rand((Hq, S, d), seed), rand((Hkv, S, d), seed + 100), rand((Hkv, S, d), seed + 200)
+            o, l = full_fn(q, k, v, causal)
+            ob, lb = brute_force(q, k, v, causal)
+            assert np.abs(o - ob).max() < 1e-12, "out differs from brute force"
+            assert np.abs(l - lb).max() < 1e-12, "lse differs from brute force"
+
+
+def pin_full_vs_torch(full_fn):
+    for causal in (False, True):
+        for (Hq, Hkv, S, d, seed) in ((2, 2, 33, 8, 1), (8, 2, 40, 16, 2), (4, 1, 17, 5, 3)):
+            q, k, v = rand((Hq, S, d), seed), rand((Hkv, S, d), seed + 1), rand((Hkv, S, d), seed + 2)
+            o, l = full_fn(q, k, v, causal)
+            g = Hq // Hkv
+            tq = torch.from_numpy(q)
+            tk = torch.from_numpy(k).repeat_interleave(g, dim=0)
+            tv = torch.from_numpy(v).repeat_interleave(g, dim=0)
+            to = torch.nn.functional.scaled_dot_product_attention(
+                tq[None], tk[None], tv[None], is_causal=causal, scale=1.0)[0]
+            sc = tq @ tk.transpose(-1, -2)
+            if causal:
+                sc = sc.masked_fill(torch.ones(S, S, dtype=torch.bool).triu(1), float("-inf"))
+            tl = torch.logsumexp(sc, dim=-1)
+            assert np.abs(o - to.numpy()).max() < 1e-10, "out differs from torch SDPA"
+            assert np.abs(l - tl.numpy()).max() < 1e-10, "lse differs from torch.logsumexp"
+
+
+def pin_full_closed_forms(full_fn):
+    S, d = 11, 6
+    k, v = rand((1, S, d), 21), rand((1, S, d), 22)
+    # q = 0: uniform weights over the visible keys
+    for causal in (False, True):
+        o, l = full_fn(np.zeros((1, S, d)), k, v, causal)
+        for i in range(S):
+            n = i + 1 if causal else S
+            assert np.abs(o[0, i] - v[0, :n].mean(axis=0)).max() < 1e-12, "q=0 is not the mean of V"
+            assert abs(l[0, i] - math.log(n)) < 1e-12, "q=0 lse is not ln|A(i)|"
+    # constant V: output is that constant whatever the scores
+    q = rand((1, S, d), 23)
+    for causal in (False, True):
+        o, _ = full_fn(q, k, np.full((1, S, d), 0.375), causal)
+        assert np.abs(o - 0.375).max() < 1e-12, "constant V not reproduced"
+    # first causal row sees only key 0
+    o, l = full_fn(q, k, v, True)
+    assert np.abs(o[0, 0] - v[0, 0]).max() < 1e-12, "causal row 0 is not v_0"
+    assert abs(l[0, 0] - float(q[0, 0] @ k[0, 0])) < 1e-12, "causal row 0 lse is not q0.k0"
+    # one dominant key: q along k_j with a score 60 above every other
+    kk = np.zeros((1, S, d)); kk[0, :, 0] = 1.0; kk[0, 7, 0] = 61.0
+    qq = np.zeros((1, S, d)); qq[0, :, 0] = 1.0
+    o, l = full_fn(qq, kk, v, False)
+    assert np.abs(o[0] - v[0, 7][None, :]).max() < 2 * S * math.exp(-60) * np.abs(v).max() + 1e-15, \
+        "dominant key does not dominate"
+
+
+# --------------------------------------------------------------------------- ring simulation
+
+def pin_ring_identity(ring_fn, full_fn):
+    cases = [
+        # (Hq, Hkv, S, d, c, layout, causal, kv_block)
+        (1, 1, 12, 8, 3, 0, False, 4),
+        (2, 1, 24, 5, 3, 1, True, 2),
+        (4, 2, 32, 4, 4, 1, True, 4),
+        (2, 2, 32, 4, 4, 0, True, 8),
+        (3, 3, 16, 3, 2, 1, False, 1),
+        (2, 1, 40, 6, 5, 0, True, 8),
+        (1, 1, 20, 3, 1, 0, True, 5),
+    ]
+    for (Hq, Hkv, S, d, c, layout, causal, kvb) in cases:
+        q, k, v = rand((Hq, S, d), S + c), rand((Hkv, S, d), S + c + 1), rand((Hkv, S, d), S + c + 2)
+        o, l = ring_fn(q, k, v, c, layout, causal, kvb)
+        of, lf = full_fn(q, k, v, causal)
+        assert np.abs(o - of).max() < 1e-12, f"ring out != full out for {(c, layout, causal, kvb)}"
+        assert np.abs(l - lf).max() < 1e-12, f"ring lse != full lse for {(c, layout, causal, kvb)}"
+
+
+def pin_worked_example(ring_fn, full_fn):
+    g = {r[0]: r[1] for r in read_golden("ring_worked_example.txt")}
+    n_q, d, n_kv, blocks = int(g["q_rows"]), int(g["d"]), int(g["kv_rows"]), int(g["blocks"])
+    atol = float(g["atol"])
+    expected = g["allclose"] == "True"
+    # the page's 4x8 q is rank 0's query chunk of a 12-row sequence cut into 3 ring blocks
+    q = rand((1, n_kv, d), 5)
+    k, v = rand((1, n_kv, d), 6), rand((1, n_kv, d), 7)
+    o, _ = ring_fn(q, k, v, blocks, 0, False, n_kv // blocks)
+    of, _ = full_fn(q, k, v, False)
+    assert np.allclose(of[0, :n_q], o[0, :n_q], atol=atol) == expected
+
+
+def pin_hop_partials(hop_fn, merge_fn, full_fn):
+    """Merging every ring message's partial, in ring order, gives the full result."""
+    for (Hq, Hkv, S, d, c, layout, causal, kvb) in ((2, 1, 24, 4, 3, 1, True, 2),
+                                                   (1, 1, 16, 3, 4, 0, True, 4),
+                                                   (2, 2, 16, 5, 2, 1, False, 4)):
+        q, k, v = rand((Hq, S, d), 41), rand((Hkv, S, d), 42), rand((Hkv, S, d), 43)
+        o = np.zeros((Hq, S, d)); l = np.full((Hq, S), -np.inf)
+        per_hop = (S // c) // kvb
+        for hop in range(c):
+            for sub in range(per_hop):
+                op, lp = hop_fn(q, k, v, c, layout, causal, kvb, hop, sub)
+                o, l = merge_fn(o, l, op, lp)
+        of, lf = full_fn(q, k, v, causal)
+        assert np.abs(o - of).max() < 1e-12 and np.abs(l - lf).max() < 1e-12, "hop partials do not merge to full"
+
+
+# --------------------------------------------------------------------------- layout and work
+
+def pin_zigzag_golden(rank_chunks_fn):
+    rows = read_golden("zigzag_pairing_c8.txt")
+    for r, a, b in rows:
+        assert list(rank_chunks_fn(8, 1, int(r))) == [int(a), int(b)], f"rank {r} pairing"
+    for r in range(8):
+        assert list(rank_chunks_fn(8, 0, r)) == [r]
+
+
+def pin_layout_bijection(order_fn):
+    for (S, c, layout) in ((16, 2, 1), (24, 3, 1), (12, 3, 0), (64, 4, 1), (10, 5, 0)):
+        perm = np.asarray(order_fn(S, c, layout))
+        assert sorted(perm.tolist()) == list(range(S)), "not a permutation of the positions"
+        if layout == 0:
+            assert perm.tolist() == list(range(S)), "contiguous must be the identity"
+
+
+def pin_work_golden(work_fn):
+    rows = read_golden("causal_work_units_c8.txt")
+    S = 16 * 64
+    uc, _, _ = work_fn(S, 8, True, 0, 32)
+    uz, _, _ = work_fn(S, 8, True, 1, 32)
+    for r, cu, zu in rows:
+        assert uc[int(r)] == int(cu) and uz[int(r)] == int(zu), f"rank {r} units"
+    assert uc[-1] == 8 * uc[0], "contiguous spread is not c-fold"
+
+
+def pin_work_closed_forms(work_fn):
+    for (S, c) in ((1024, 8), (4096, 4), (96, 3)):
+        n, m = S // c, S // (2 * c)
+        _, pc, _ = work_fn(S, c, True, 0, 32)
+        _, pz, _ = work_fn(S, c, True, 1, 32)
+        for i in range(c):
+            assert pc[i] == i * n * n + n * (n + 1) // 2, "contiguous pairs closed form"
+            assert pz[i] == (2 * c - 1) * m * m + m * (m + 1), "zigzag pairs closed form"
+        assert pc.sum() == S * (S + 1) // 2 and pz.sum() == S * (S + 1) // 2
+    # tiles by brute force over (query, key) pairs on a small case
+    S, c, tile = 48, 3, 4
+    for layout in (0, 1):
+        _, _, t = work_fn(S, c, True, layout, tile)
+        from oracle.layout import rank_positions  # positions only, to enumerate pairs
+        nch = c * (2 if layout else 1)
+        m = S // nch
+        for r in range(c):
+            pos = rank_positions(S, c, layout, r)
+            cnt = 0
+            for t0 in range(0, len(pos), tile):
+                qs = pos[t0:t0 + tile]
+                for kc in range(nch):
+                    for k0 in range(kc * m, kc * m + m, tile):
+                        ks = range(k0, min(k0 + tile, kc * m + m))
+                        cnt += any(kk <= qq for qq in qs for kk in ks)
+            assert t[r] == cnt, "tile count"
+
+
+# --------------------------------------------------------------------------- merge
+
+def pin_merge(merge_fn, full_fn):
+    S, d = 14, 5
+    q, k, v = rand((1, S, d), 31), rand((1, S, d), 32), rand((1, S, d), 33)
+    split = np.array([0, 3, 4, 8, 11, 12])
+    rest = np.setdiff1d(np.arange(S), split)
+    oa, la = full_fn(q, k[:, split], v[:, split], False)
+    ob, lb = full_fn(q, k[:, rest], v[:, rest], False)
+    om, lm = merge_fn(oa, la, ob, lb)
+    of, lf = full_fn(q, k, v, False)
+    assert np.abs(om - of).max() < 1e-12 and np.abs(lm - lf).max() < 1e-12, "merge is not exact"
+    om2, lm2 = merge_fn(ob, lb, oa, la)
+    assert np.abs(om2 - om).max() < 1e-12 and np.abs(lm2 - lm).max() < 1e-12, "merge not symmetric"
+    ninf = np.full_like(la, -np.inf)
+    oe, le = merge_fn(oa, la, np.zeros_like(oa), ninf)
+    assert np.abs(oe - oa).max() == 0.0 and np.abs(le - la).max() == 0.0, "-inf partial not neutral"
+    oz, lz = merge_fn(np.zeros_like(oa), ninf, np.zeros_like(oa), ninf)
+    assert np.all(oz == 0.0) and np.all(np.isneginf(lz)), "two empty partials"

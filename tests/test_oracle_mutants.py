@@ -1,0 +1,152 @@
+"""Plant one plausible mistake at a time in a copy of the oracle and check
+that the pins reject it (CPU only).  The oracle itself is not modified."""
+import numpy as np
+import pytest
+
+from oracle import attention, layout, merge, ring, work
+from tests import pins
+
+
+# ---------------------------------------------------------------- full attention mutants
+
+def _full(q, k, v, causal, *, off=0, lse_no_max=False, gqa_mod=False, no_norm=False, rev_k=False):
+    q = np.asarray(q, float); k = np.asarray(k, float); v = np.asarray(v, float)
+    Hq, S, d = q.shape
+    Hkv = k.shape[0]
+    g = Hq // Hkv
+    out = np.empty((Hq, S, v.shape[2])); lse = np.empty((Hq, S))
+    for h in range(Hq):
+        kh = h % Hkv if gqa_mod else h // g
+        kk = k[kh][:, ::-1] if rev_k else k[kh]
+        s = q[h] @ kk.T
+        if causal:
+            s = np.where(np.arange(S)[None, :] > np.arange(S)[:, None] + off, -np.inf, s)
+        M = s.max(1)
+        e = np.exp(s - M[:, None])
+        L = e.sum(1)
+        out[h] = (e @ v[kh]) / (1.0 if no_norm else L[:, None])
+        lse[h] = (0.0 if lse_no_max else M) + np.log(L)
+    return out, lse
+
+
+FULL_MUTANTS = {
+    "mask_off_by_one": dict(off=1),
+    "lse_drops_max": dict(lse_no_max=True),
+    "gqa_head_map_mod": dict(gqa_mod=True),
+    "no_normalisation": dict(no_norm=True),
+    "key_features_reversed": dict(rev_k=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FULL_MUTANTS))
+def test_full_mutant_caught(name):
+    kw = FULL_MUTANTS[name]
+    fn = lambda q, k, v, causal: _full(q, k, v, causal, **kw)  # noqa: E731
+    failures = 0
+    for pin in (pins.pin_full_brute, pins.pin_full_vs_torch, pins.pin_full_closed_forms):
+        try:
+            pin(fn)
+        except AssertionError:
+            failures += 1
+    assert failures > 0, f"mutant {name} passed every pin"
+
+
+def test_unmutated_copy_passes():
+    # the mutant harness with no mutation is a faithful copy: all pins pass
+    fn = lambda q, k, v, causal: _full(q, k, v, causal)  # noqa: E731
+    pins.pin_full_brute(fn)
+    pins.pin_full_vs_torch(fn)
+    pins.pin_full_closed_forms(fn)
+
+
+# ---------------------------------------------------------------- ring mutants
+
+def _ring_rank(q_rows, q_pos, k, v, blocks, causal, *, no_out_corr=False, no_sum_corr=False, flip=False):
+    n = q_rows.shape[0]
+    m = np.full(n, -np.inf); l = np.zeros(n); o = np.zeros((n, v.shape[1]))
+    with np.errstate(invalid="ignore", over="ignore"):
+        for pk in blocks:
+            s = q_rows @ k[pk].T
+            if causal:
+                s = np.where(pk[None, :] > q_pos[:, None], -np.inf, s)
+            nm = np.maximum(m, s.max(1))
+            seen = np.isfinite(nm)
+            corr = np.where(seen, np.exp((nm - m) if flip else (m - nm)), 1.0)
+            corr = np.where(np.isfinite(corr), corr, 0.0)
+            p = np.where(seen[:, None], np.exp(s - nm[:, None]), 0.0)
+            l = (l if no_sum_corr else l * corr) + p.sum(1)
+            o = (o if no_out_corr else o * corr[:, None]) + p @ v[pk]
+            m = nm
+    return o / l[:, None], m + np.log(l)
+
+
+def _ring(q, k, v, c, lay, causal, kvb, **kw):
+    q = np.asarray(q, float); k = np.asarray(k, float); v = np.asarray(v, float)
+    Hq, S, d = q.shape
+    g = Hq // k.shape[0]
+    out = np.zeros((Hq, S, v.shape[2])); lse = np.zeros((Hq, S))
+    for h in range(Hq):
+        for r in range(c):
+            pos = layout.rank_positions(S, c, lay, r)
+            o, l = _ring_rank(q[h, pos], pos, k[h // g], v[h // g],
+                              ring.ring_schedule(S, c, lay, r, kvb), causal, **kw)
+            out[h, pos] = o; lse[h, pos] = l
+    return out, lse
+
+
+RING_MUTANTS = {
+    "output_not_rescaled": dict(no_out_corr=True),
+    "sum_not_rescaled": dict(no_sum_corr=True),
+    "correction_sign_flipped": dict(flip=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(RING_MUTANTS))
+def test_ring_mutant_caught(name):
+    kw = RING_MUTANTS[name]
+    fn = lambda *a: _ring(*a, **kw)  # noqa: E731
+    with pytest.raises(AssertionError):
+        pins.pin_ring_identity(fn, attention.full_attention)
+
+
+def test_ring_copy_passes():
+    pins.pin_ring_identity(lambda *a: _ring(*a), attention.full_attention)
+
+
+# ---------------------------------------------------------------- layout / work / merge mutants
+
+def test_zigzag_pairing_mutant_caught():
+    bad = lambda c, lay, r: [r, 2 * c - 2 - r] if lay == 1 else [r]  # noqa: E731
+    with pytest.raises(AssertionError):
+        pins.pin_zigzag_golden(bad)
+
+
+def test_work_mutants_caught():
+    def shifted(S, c, causal, lay, tile):
+        u, p, t = work.rank_work(S, c, causal, lay, tile)
+        return (u[::-1] if lay == 0 else u - 1), p, t
+
+    with pytest.raises(AssertionError):
+        pins.pin_work_golden(shifted)
+
+    def half_diag(S, c, causal, lay, tile):
+        u, p, t = work.rank_work(S, c, causal, lay, tile)
+        m = S // (c * (2 if lay else 1))
+        return u, p - m // 2, t
+
+    with pytest.raises(AssertionError):
+        pins.pin_work_closed_forms(half_diag)
+
+
+def test_merge_mutants_caught():
+    def unnormalised(oa, la, ob, lb):
+        o, l = merge.merge(oa, la, ob, lb)
+        return o * 1.0001, l
+
+    def lse_sum(oa, la, ob, lb):
+        o, _ = merge.merge(oa, la, ob, lb)
+        return o, np.maximum(la, lb)
+
+    for fn in (unnormalised, lse_sum):
+        with pytest.raises(AssertionError):
+            pins.pin_merge(fn, attention.full_attention)

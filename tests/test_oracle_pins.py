@@ -1,0 +1,82 @@
+"""The oracle against facts outside itself (CPU only)."""
+import numpy as np
+import pytest
+
+from oracle import attention, layout, merge, ring, work
+from tests import pins
+
+
+def test_full_vs_brute_force():
+    pins.pin_full_brute(attention.full_attention)
+
+
+def test_full_vs_torch_library():
+    pins.pin_full_vs_torch(attention.full_attention)
+
+
+def test_full_closed_forms():
+    pins.pin_full_closed_forms(attention.full_attention)
+
+
+def test_full_rows_matches_library():
+    # the row-subset form against torch's SDPA on selected rows
+    import torch
+    rng = np.random.default_rng(3)
+    Hq, Hkv, S, d = 4, 2, 300, 8
+    q, k, v = rng.standard_normal((Hq, S, d)), rng.standard_normal((Hkv, S, d)), rng.standard_normal((Hkv, S, d))
+    heads = np.array([0, 0, 1, 3, 3, 2])
+    posn = np.array([0, 299, 17, 150, 151, 64])
+    for causal in (False, True):
+        o, l = attention.full_attention_rows(q, k, v, heads, posn, causal, batch_rows=2)
+        tk = torch.from_numpy(k).repeat_interleave(2, 0)
+        tv = torch.from_numpy(v).repeat_interleave(2, 0)
+        to = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q)[None], tk[None], tv[None], is_causal=causal, scale=1.0)[0]
+        assert np.abs(o - to.numpy()[heads, posn]).max() < 1e-10
+
+
+def test_ring_equals_full():
+    pins.pin_ring_identity(ring.ring_attention, attention.full_attention)
+
+
+def test_worked_example():
+    pins.pin_worked_example(ring.ring_attention, attention.full_attention)
+
+
+def test_hop_partials_merge_to_full():
+    pins.pin_hop_partials(ring.ring_hop_partial, merge.merge, attention.full_attention)
+
+
+def test_merge_exact():
+    pins.pin_merge(merge.merge, attention.full_attention)
+
+
+def test_zigzag_pairing_golden():
+    pins.pin_zigzag_golden(layout.rank_chunks)
+
+
+def test_layout_bijection_and_inverse():
+    pins.pin_layout_bijection(layout.rank_major_order)
+    x = np.arange(2 * 48 * 3).reshape(2, 48, 3)
+    for (c, lay) in ((3, 0), (3, 1), (4, 1), (1, 1)):
+        y = layout.to_rank_major(x, 48, c, lay)
+        assert np.array_equal(layout.from_rank_major(y, 48, c, lay), x)
+
+
+def test_work_golden():
+    pins.pin_work_golden(work.rank_work)
+
+
+def test_work_closed_forms():
+    pins.pin_work_closed_forms(work.rank_work)
+
+
+def test_ring_schedule_covers_each_key_once():
+    for (S, c, lay, kvb) in ((32, 4, 1, 2), (24, 3, 0, 4), (16, 1, 1, 8)):
+        for r in range(c):
+            msgs = ring.ring_schedule(S, c, lay, r, kvb)
+            allk = np.sort(np.concatenate(msgs))
+            assert np.array_equal(allk, np.arange(S))
+            # hop 0 is the rank's own block (no communication on the first round)
+            own = layout.rank_positions(S, c, lay, r)
+            assert np.array_equal(np.concatenate(msgs[: len(own) // kvb]), own)
