@@ -1,0 +1,369 @@
+#!/usr/bin/env python3
+"""Benchmark of the ring-attention hot path on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one pass of the whole path over one batch of synthetic input resident in
+HBM: natural -> rank-major permutation of Q, K and V, the fused ring-attention
+kernel (every virtual rank's queries against the KV blocks in ring order), and the
+inverse permutation of the output and its log-sum-exp.  The metric is
+causal-adjusted attention TFLOP/s: 4*B*Hq*d*S^2 per step, halved when causal.
+
+Several GPUs run independent replicas of the same workload (the c virtual ranks of
+the ring all live on one GPU; there is no data-path collective).  --impl reference
+times the float64 CPU oracle on the host cores on a bounded sample of the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from online_softmax_attention_zigzag_gb300.configs import WORKLOADS, CAUSAL_GQA_S32K  # noqa: E402
+from online_softmax_attention_zigzag_gb300.inputs import make_qkv, sample_rows  # noqa: E402
+
+METRIC = "causal-adjusted attention TFLOP/s and % of GB300 bf16 tensor peak, 1 GPU"
+UNIT = "TFLOP/s"
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+ATTN_SRC = os.path.join(ROOT, "online_softmax_attention_zigzag_gb300", "csrc", "attn_bf16.cu")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=CAUSAL_GQA_S32K.name, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return j.get("bf16_tflops"), j.get("bf16_tflops_sustained"), j.get("hbm_gbs"), "measured"
+    return FALLBACK_BF16_TFLOPS, None, FALLBACK_HBM_GBS, "fallback"
+
+
+def src_hash() -> str:
+    with open(ATTN_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_for(workload: str):
+    """DRAM bytes per launch of the attention kernel from the committed ncu summary, or
+    None when there is none for this workload or the kernel changed since."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        j = json.load(f)
+    e = j.get(workload)
+    if not e or e.get("attn_bf16_sha256_16") != src_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            ident = str(device_index)
+        self.cmd = ["nvidia-smi", "-i", ident, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", "200"]
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(self.cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+def cpu_oracle_sample(w, budget_s: float, seed: int = 7):
+    """Time the float64 oracle on sampled query rows of workload ``w``; returns
+    (TFLOP/s, rows, seconds, threads)."""
+    from oracle.attention import full_attention_rows
+    q, k, v = make_qkv(w)
+    hs, ps = sample_rows(w.bhq, w.seq, 1 << 20, seed=seed)
+    perm = np.random.default_rng(seed).permutation(len(hs))
+    hs, ps = hs.numpy()[perm], ps.numpy()[perm]
+
+    def flop(pos):
+        keys = (pos + 1) if w.causal else np.full_like(pos, w.seq)
+        return float(np.sum(4.0 * w.d * keys))
+
+    n, done_rows, done_flop, t_used = 32, 0, 0.0, 0.0
+    while t_used < budget_s and done_rows < len(hs):
+        sel = slice(done_rows, min(done_rows + n, len(hs)))
+        t0 = time.perf_counter()
+        full_attention_rows(q, k, v, hs[sel], ps[sel], bool(w.causal))
+        t_used += time.perf_counter() - t0
+        done_flop += flop(ps[sel])
+        done_rows = sel.stop
+        n = min(4 * n, 4096)
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max(i.get("num_threads", 1) for i in threadpool_info()) if threadpool_info() else 1
+    except Exception:
+        threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return done_flop / t_used / 1e12, done_rows, t_used, threads
+
+
+def run_reference(args, w, rank):
+    if rank != 0:
+        return
+    per_step = []
+    rows_total = 0
+    threads = 1
+    budget = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    for i in range(args.warmup + args.steps):
+        tf, rows, secs, threads = cpu_oracle_sample(w, budget, seed=100 + i)
+        if i >= args.warmup:
+            per_step.append((tf, rows, secs))
+            rows_total += rows
+    value = float(np.mean([x[0] for x in per_step]))
+    secs = sum(x[2] for x in per_step)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1))",
+        "config": {"workload": w.name, "S": w.seq, "Hq": w.hq, "Hkv": w.hkv, "d": w.d, "c": w.c,
+                   "causal": w.causal, "layout": "zigzag" if w.layout else "contiguous", "batch": w.batch},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{rows_total} sampled query rows over {args.steps} steps, float64 numpy"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def main():
+    args = parse()
+    w = WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        return
+    if w.dtype != "bf16":
+        raise SystemExit("the bench times the bf16 tensor-core path; pick a bf16 workload")
+
+    from online_softmax_attention_zigzag_gb300 import ringattn as ra
+    ra.lib()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    S, c, L = w.seq, w.c, w.layout
+    q_h, k_h, v_h = make_qkv(w)
+    q_h, k_h, v_h = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    qr, kr, vr = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    o_r = torch.empty((w.bhq, S, w.d), dtype=torch.float32, device=dev)
+    l_r = torch.empty((w.bhq, S), dtype=torch.float32, device=dev)
+    out = torch.empty_like(o_r)
+    lse = torch.empty_like(l_r)
+    out_h = torch.empty(out.shape, dtype=torch.float32, pin_memory=True)
+    lse_h = torch.empty(lse.shape, dtype=torch.float32, pin_memory=True)
+    kw = dict(c=c, causal=w.causal, layout=L, kv_block=w.kv_block)
+    attn_ev = []
+
+    def step(record=False):
+        ra.permute(q, qr, c=c, layout=L, inverse=0)
+        ra.permute(k, kr, c=c, layout=L, inverse=0)
+        ra.permute(v, vr, c=c, layout=L, inverse=0)
+        if record:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        ra.fwd(qr, kr, vr, o_r, l_r, **kw)
+        if record:
+            e1.record(stream)
+            attn_ev.append((e0, e1))
+        ra.permute(o_r, out, c=c, layout=L, inverse=1)
+        ra.permute(l_r, lse, c=c, layout=L, inverse=1)
+
+    launches_per_step = 6
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if ra.sync_status() != ra.RA_OK:
+        raise SystemExit("device wait timed out during warm-up")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    if ra.sync_status() != ra.RA_OK:
+        raise SystemExit("device wait timed out in the timed region")
+    attn_ms = float(np.mean([a.elapsed_time(b) for a, b in attn_ev]))
+
+    # end to end through the public call with host buffers: H2D of Q/K/V from pinned
+    # memory, the whole path, D2H of out and lse, every step inside the timed region
+    e2e_steps = max(1, min(args.steps, 5))
+    torch.cuda.synchronize()
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(e2e_steps):
+        qd, kd, vd = (x.to(dev, non_blocking=True) for x in (q_h, k_h, v_h))
+        o_d, l_d = ra.attention(qd, kd, vd, **kw)
+        out_h.copy_(o_d, non_blocking=True)
+        lse_h.copy_(l_d, non_blocking=True)
+    s1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = s0.elapsed_time(s1) / e2e_steps
+    if ra.sync_status() != ra.RA_OK:
+        raise SystemExit("device wait timed out in the end-to-end region")
+
+    # secondary HBM-bound kernels: the merge (per-hop path) and one permutation
+    def time_ms(fn, reps=5):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    rows = w.bhq * S
+    merge_ms = time_ms(lambda: ra.merge(o_r, l_r, out, lse))
+    merge_bytes = rows * (12 * w.d + 12)
+    perm_ms = time_ms(lambda: ra.permute(q, qr, c=c, layout=L, inverse=0))
+    perm_bytes = 2 * q.numel() * q.element_size()
+    torch.cuda.synchronize()
+
+    ms_step = ms_total / args.steps
+    if dist is not None:
+        t = torch.tensor([ms_step, e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, e2e_ms = t.tolist()
+    flop = w.flops()
+    value = world * flop / (ms_step * 1e-3) / 1e12
+    e2e_value = world * flop / (e2e_ms * 1e-3) / 1e12
+    bf16_peak, bf16_sust, hbm_peak, peak_src = peaks()
+    achieved = flop / (attn_ms * 1e-3) / 1e12
+    traffic = traffic_for(w.name)
+    h2d = sum(x.numel() * x.element_size() for x in (q_h, k_h, v_h))
+    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        tf, rows_s, secs, threads = cpu_oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": tf, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{rows_s} sampled query rows ({secs:.1f} s), float64 numpy, same inputs"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1), see inputs.py)",
+            "config": {"workload": w.name, "S": S, "Hq": w.hq, "Hkv": w.hkv, "d": w.d, "c": c,
+                       "causal": w.causal, "layout": "zigzag" if L else "contiguous", "kv_block": w.kv_block,
+                       "batch": w.batch, "step": "permute QKV + fused ring attention + inverse permute O, LSE",
+                       "l2": "inputs larger than L2 (Q+K+V %.2f GiB per step)" % (h2d / 2**30),
+                       "replicas": "one independent replica per GPU"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": achieved / bf16_peak, "traffic": traffic,
+                         "kernel": "attn_bf16_kernel<%d>" % w.d, "kernel_ms": attn_ms,
+                         "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
+                         "frac_of_sustained": (achieved / bf16_sust) if bf16_sust else None},
+            "secondary": {
+                "merge": {"bound": "hbm", "achieved": merge_bytes / (merge_ms * 1e-3) / 1e9, "peak": hbm_peak,
+                          "unit": "GB/s", "frac": merge_bytes / (merge_ms * 1e-3) / 1e9 / hbm_peak,
+                          "kernel_ms": merge_ms, "bytes": merge_bytes},
+                "permute_q": {"bound": "hbm", "achieved": perm_bytes / (perm_ms * 1e-3) / 1e9, "peak": hbm_peak,
+                              "unit": "GB/s", "frac": perm_bytes / (perm_ms * 1e-3) / 1e9 / hbm_peak,
+                              "kernel_ms": perm_ms, "bytes": perm_bytes},
+            },
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms, "steps": e2e_steps},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,171 @@
+/*
+ * ringattn.h -- C ABI of libringattn.so: the per-rank hot path of ring attention
+ * (context parallelism) with contiguous or zigzag chunking, all c virtual ranks on
+ * one GB300 (sm_103a) GPU.
+ *
+ * The operation (sources are the pages' titles and sections):
+ *  - "Ring Attention and Ulysses shard a sequence two different ways...", section
+ *    "Ring Attention: point-to-point rotation, and an online softmax that never sees
+ *    the whole row at once": each rank keeps its queries fixed and attends to KV
+ *    blocks one hop at a time, merging with a running max, a running sum and a
+ *    correction factor exp(old max - new max).
+ *  - "Interrogating parallelism, part 5", section "How does attention survive being
+ *    split?": rank i sends its KV block to rank i+1, so at hop h rank r holds the
+ *    block of rank (r - h) mod c; the merged result is exact.
+ *  - same page, section "What breaks the load balance?": contiguous chunking gives
+ *    rank i chunk i of c; zigzag chunking gives rank i chunks i and 2c-1-i of 2c.
+ *  - "Context & Expert Parallelism", section "Context parallelism: splitting the
+ *    sequence": under the causal mask token i attends to every token j <= i.
+ *
+ * Per (query head h, query position i) every entry point computes, up to rounding,
+ *     out[h,i,:] = sum_j softmax_j(q_i . k_j) v_j,   lse[h,i] = ln sum_j exp(q_i . k_j)
+ * over the visible keys j (all keys, or j <= i when causal), with kv head h / (Hq/Hkv).
+ * No 1/sqrt(d) scale is applied (the pages' rule uses q @ k.T as is); callers that
+ * want one scale q before the call.
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers are DEVICE pointers unless stated otherwise; the caller allocates and
+ *    owns every buffer.  Inputs are read-only; outputs are fully overwritten.
+ *  - Tensors are head-major, [H, S, row] with H = batch * heads (batch folds into
+ *    heads: kv head of query head b*Hq+h is b*Hkv + h/g).
+ *  - "Rank-major" order stores rank 0's local rows, then rank 1's, ...; a zigzag rank
+ *    holds chunk r then chunk 2c-1-r.  ringattn_permute converts from/to natural order.
+ *  - layout: 0 = contiguous (c chunks), 1 = zigzag (2c chunks).  causal: 0 or 1.
+ *  - kv_block: rows of one simulated ring message; it must divide a chunk
+ *    (S/c contiguous, S/(2c) zigzag).  A rank's KV block is split into messages of
+ *    kv_block rows, visited in ring order.
+ *  - stream: a cudaStream_t (0 = legacy default stream).  Calls are asynchronous:
+ *    they validate, enqueue kernels on `stream` and return.
+ *  - Errors: every argument is validated on the host before any launch; on a bad
+ *    argument the call returns a negative ra_status and touches no device memory.
+ *    RA_ERR_ARCH: the current device is not compute capability 10.3.  RA_ERR_CUDA: a
+ *    CUDA runtime call or launch failed.  Device-side waits are bounded; one that
+ *    runs out records RA_ERR_TIMEOUT, read with ringattn_sync_status.  No exception
+ *    crosses the ABI and there is no CPU fallback.
+ *  - The library allocates no device memory per call.
+ */
+#ifndef RINGATTN_H
+#define RINGATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ra_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    RA_OK = 0,
+    RA_ERR_INVALID_ARG = -1,
+    RA_ERR_UNSUPPORTED = -2,
+    RA_ERR_ARCH = -3,
+    RA_ERR_CUDA = -4,
+    RA_ERR_TIMEOUT = -5
+} ra_status;
+
+/*
+ * ringattn_fwd -- fused ring attention, bf16 in, fp32 out (tcgen05 tensor cores).
+ * q:   [Hq,  S, d] bf16, rank-major.      k, v: [Hkv, S, d] bf16, rank-major.
+ * out: [Hq,  S, d] fp32, rank-major.      lse:  [Hq, S] fp32 natural log, rank-major.
+ * Every rank's query tiles visit the KV blocks in ring order (hop 0 = own block);
+ * each 128-row key tile is one exact online-softmax update (finer than kv_block,
+ * which only has to be valid here), and key tiles that the causal mask hides
+ * entirely are skipped.
+ * Requires d in {64, 128}; S/(c*(layout?2:1)) and kv_block multiples of 128;
+ * Hq % Hkv == 0; 16-byte aligned pointers.
+ */
+int ringattn_fwd(const void* q, const void* k, const void* v, float* out, float* lse,
+                 int S, int Hq, int Hkv, int d, int c, int causal, int layout, int kv_block,
+                 ra_stream_t stream);
+
+/*
+ * ringattn_fwd_natural -- as ringattn_fwd, but q, k, v, out and lse are in NATURAL
+ * sequence order: the zigzag/contiguous chunk map is applied in the kernel's tile
+ * addressing, so no permutation pass is needed.  Same result, same requirements.
+ */
+int ringattn_fwd_natural(const void* q, const void* k, const void* v, float* out, float* lse,
+                         int S, int Hq, int Hkv, int d, int c, int causal, int layout,
+                         int kv_block, ra_stream_t stream);
+
+/*
+ * ringattn_fwd_f32 -- the same computation in fp32 with FFMA (no tensor cores), one
+ * online update per kv_block message exactly as the pages' rule.  Any 1 <= d <= 128;
+ * S divisible by the chunk count; kv_block divides a chunk.  Rank-major layout.
+ */
+int ringattn_fwd_f32(const float* q, const float* k, const float* v, float* out, float* lse,
+                     int S, int Hq, int Hkv, int d, int c, int causal, int layout, int kv_block,
+                     ra_stream_t stream);
+
+/*
+ * ringattn_fwd_hop / ringattn_fwd_hop_f32 -- one ring message: every rank attends
+ * to message `sub` (0 <= sub < (S/c)/kv_block) of the KV block it holds at hop `hop`
+ * (0 <= hop < c) and writes the normalised partial o_part [Hq,S,d] fp32 and its
+ * log-sum-exp lse_part [Hq,S] fp32 (rank-major).  Rows that see no key in that
+ * message get o_part = 0 and lse_part = -inf.  Folding every message's partial
+ * into a running (out, lse) with ringattn_merge, in ring order, gives ringattn_fwd's
+ * result.  Requirements as ringattn_fwd (bf16) or ringattn_fwd_f32.
+ */
+int ringattn_fwd_hop(const void* q, const void* k, const void* v, float* o_part, float* lse_part,
+                     int S, int Hq, int Hkv, int d, int c, int causal, int layout, int kv_block,
+                     int hop, int sub, ra_stream_t stream);
+int ringattn_fwd_hop_f32(const float* q, const float* k, const float* v, float* o_part,
+                         float* lse_part, int S, int Hq, int Hkv, int d, int c, int causal,
+                         int layout, int kv_block, int hop, int sub, ra_stream_t stream);
+
+/*
+ * ringattn_merge -- exact merge of a partial into a running result, in place:
+ *   lse' = ln(exp(lse_run) + exp(lse_part))
+ *   o'   = o_run * exp(lse_run - lse') + o_part * exp(lse_part - lse')
+ * ("Interrogating parallelism, part 5", "How does attention survive being split?":
+ * partials over disjoint key sets combine exactly).  A partial with lse = -inf has
+ * weight 0; two -inf partials give o = 0, lse = -inf.  rows >= 0 rows of d fp32
+ * (any 1 <= d <= 4096); o_run/lse_run are read and overwritten.  To start a ring,
+ * fill o_run with 0 and lse_run with -inf (or copy the first partial).
+ */
+int ringattn_merge(float* o_run, float* lse_run, const float* o_part, const float* lse_part,
+                   long long rows, int d, ra_stream_t stream);
+
+/*
+ * ringattn_permute -- move rows between natural and rank-major order.
+ * src, dst: [H, S, row_bytes] bytes, distinct buffers.  inverse = 0: natural ->
+ * rank-major; 1: rank-major -> natural.  row_bytes >= 1 (2*d for bf16 Q/K/V, 4*d
+ * for fp32 out, 4 for lse).  Bit-exact copy ("What breaks the load balance?": the
+ * zigzag assignment is index bookkeeping only).
+ */
+int ringattn_permute(const void* src, void* dst, int S, int H, int row_bytes, int c, int layout,
+                     int inverse, ra_stream_t stream);
+
+/*
+ * ringattn_rank_work -- host only, no device use.  Per rank r < c (each output array
+ * has c entries; any may be NULL), for one head:
+ *   units[r] -- (query chunk, key chunk) pairs with a visible key, the pages' count
+ *               (contiguous causal: r+1; zigzag causal: 2c+1);
+ *   pairs[r] -- visible (query, key) pairs;
+ *   tiles[r] -- (query tile, key tile) pairs of `tile` rows with a visible pair, the
+ *               tiles the fused kernel computes when tile = 128.
+ */
+int ringattn_rank_work(int S, int c, int causal, int layout, int tile, long long* units,
+                       long long* pairs, long long* tiles);
+
+/*
+ * ringattn_sync_status -- synchronise `stream`, then return RA_ERR_TIMEOUT if a
+ * bounded device wait of any earlier call on the current device ran out (the record
+ * is cleared), RA_ERR_CUDA if the synchronisation failed, else RA_OK.
+ */
+int ringattn_sync_status(ra_stream_t stream);
+
+/*
+ * ringattn_selftest_timeout -- launch one tiny kernel whose single wait is on a
+ * barrier that nothing signals, bounded by timeout_ns (1e3 .. 1e10).  The kernel gives
+ * up, records RA_ERR_TIMEOUT and exits, leaving the context usable; the caller reads
+ * the record with ringattn_sync_status.  Exists to test the failure path.
+ */
+int ringattn_selftest_timeout(long long timeout_ns, ra_stream_t stream);
+
+/* ringattn_strerror -- static description of a status code. */
+const char* ringattn_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RINGATTN_H */

@@ -63,8 +63,14 @@ NONCAUSAL_MHA_B2_S64K = Workload("noncausal_mha_B2_S65536_h16_d128_c8_contig", s
                                  outlier_frac=0.01, outlier_factor=8.0,
                                  kv_sweep=(512, 1024, 2048, 4096, 8192))
 
+# Half-length version of the 32k workload (same heads, d, c and chunking; Q 256 MiB, still
+# larger than L2) for detailed counter captures, which replay each launch many times.
+PROFILE_GQA_S16K = Workload("causal_gqa_S16384_h64x8_d128_c8_zigzag", seq=16384, hq=64, hkv=8,
+                            d=128, c=8, causal=1, layout=1, kv_block=1024,
+                            q_scale=1.0 / math.sqrt(128.0))
+
 WORKLOADS = {w.name: w for w in (TINY_F32, CAUSAL_MHA_S4K, CAUSAL_GQA_S32K, CAUSAL_GQA_S128K,
-                                 NONCAUSAL_MHA_B2_S64K)}
+                                 NONCAUSAL_MHA_B2_S64K, PROFILE_GQA_S16K)}
 
 
 def with_layout(w: Workload, layout: int) -> Workload:

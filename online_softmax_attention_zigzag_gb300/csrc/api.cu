@@ -1,0 +1,347 @@
+// api.cu -- the C ABI of libringattn.so (declared in include/ringattn.h): argument
+// validation, device checks, TMA descriptors, work geometry and kernel launches.
+// Host code only; the compute is in attn_bf16.cu, attn_f32.cu and permute_merge.cu.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "ringattn.h"
+#include "internal.h"
+
+namespace {
+
+// Device error word: bounded waits that run out write RA_ERR_TIMEOUT here.  It is a
+// static device variable, so the library allocates nothing; host code reaches it
+// through the address cudaGetSymbolAddress returns for the current device.
+__device__ int g_err_word;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    int status = RA_OK;  // RA_ERR_ARCH when the device is not sm_103
+    int sms = 0;
+    int* err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Current device's info; performs the one-time set-up for that device.
+int device_info(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return RA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return RA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return RA_ERR_CUDA;
+        if (major != 10 || minor != 3) {
+            d.status = RA_ERR_ARCH;
+        } else {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return RA_ERR_CUDA;
+            d.err = static_cast<int*>(p);
+            d.status = RA_OK;
+        }
+        d.ready = true;
+    }
+    if (d.status != RA_OK) return d.status;
+    *out = &d;
+    return RA_OK;
+}
+
+int get_encoder() {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_encode) return RA_OK;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return RA_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return RA_OK;
+}
+
+// [rows, d] bf16 tensor, boxes of 128 rows x 64 columns, 128-byte swizzle.
+int encode_bf16_map(CUtensorMap* map, const void* base, long long rows, int d) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? RA_OK : RA_ERR_CUDA;
+}
+
+unsigned long long wait_timeout_ns() {
+    static unsigned long long ns = [] {
+        const char* e = std::getenv("RINGATTN_WAIT_TIMEOUT_MS");
+        long long ms = e ? std::atoll(e) : 2000;
+        if (ms < 1) ms = 1;
+        if (ms > 600000) ms = 600000;
+        return static_cast<unsigned long long>(ms) * 1000000ull;
+    }();
+    return ns;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Geometry checks shared by every attention entry point.
+int make_ring(int S, int Hq, int Hkv, int d, int c, int causal, int layout, int kv_block, ra::Ring* R) {
+    if (S < 1 || Hq < 1 || Hkv < 1 || d < 1 || c < 1 || kv_block < 1) return RA_ERR_INVALID_ARG;
+    if ((causal != 0 && causal != 1) || (layout != 0 && layout != 1)) return RA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return RA_ERR_INVALID_ARG;
+    const int nch = c * (layout == 1 ? 2 : 1);
+    if (S % nch != 0) return RA_ERR_INVALID_ARG;
+    const int m = S / nch;
+    if (m % kv_block != 0) return RA_ERR_INVALID_ARG;
+    if (static_cast<long long>(Hq) * S > INT_MAX || static_cast<long long>(Hq) * S * d > (1LL << 40))
+        return RA_ERR_UNSUPPORTED;
+    R->S = S;
+    R->Hq = Hq;
+    R->Hkv = Hkv;
+    R->g = Hq / Hkv;
+    R->d = d;
+    R->c = c;
+    R->causal = causal;
+    R->layout = layout;
+    R->n_r = S / c;
+    R->m = m;
+    R->nslot = layout == 1 ? 2 : 1;
+    R->hop_lo = 0;
+    R->hop_hi = c;
+    R->kv_lo = 0;
+    R->kv_hi = S / c;
+    return RA_OK;
+}
+
+int select_hop(ra::Ring* R, int kv_block, int hop, int sub) {
+    if (hop < 0 || hop >= R->c) return RA_ERR_INVALID_ARG;
+    if (sub < 0 || sub >= R->n_r / kv_block) return RA_ERR_INVALID_ARG;
+    R->hop_lo = hop;
+    R->hop_hi = hop + 1;
+    R->kv_lo = sub * kv_block;
+    R->kv_hi = (sub + 1) * kv_block;
+    return RA_OK;
+}
+
+int fwd_bf16(const void* q, const void* k, const void* v, float* out, float* lse, int S, int Hq, int Hkv, int d,
+             int c, int causal, int layout, int kv_block, int natural, int hop, int sub, cudaStream_t stream) {
+    if (!q || !k || !v || !out || !lse) return RA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+        return RA_ERR_INVALID_ARG;
+    ra::Ring R;
+    int st = make_ring(S, Hq, Hkv, d, c, causal, layout, kv_block, &R);
+    if (st != RA_OK) return st;
+    if (d != 64 && d != 128) return RA_ERR_UNSUPPORTED;
+    if (R.m % 128 != 0 || kv_block % 128 != 0) return RA_ERR_UNSUPPORTED;
+    if (hop >= 0 && (st = select_hop(&R, kv_block, hop, sub)) != RA_OK) return st;
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != RA_OK) return st;
+    if ((st = get_encoder()) != RA_OK) return st;
+
+    ra::AttnBf16Params p;
+    p.ring = R;
+    p.natural = natural;
+    p.n_tiles = S / 128;
+    const int tiles_per_chunk = R.m / 128;
+    if (R.g % 2 == 0) {
+        p.pair_mode = ra::kPairHeads;
+        p.n_items = p.n_tiles * (Hq / 2);
+    } else if (R.g == 1 && tiles_per_chunk % 2 == 0) {
+        p.pair_mode = ra::kPairPositions;
+        p.n_items = (p.n_tiles / 2) * Hq;
+    } else {
+        p.pair_mode = ra::kSingles;
+        p.n_items = p.n_tiles * Hq;
+    }
+    p.out = out;
+    p.lse = lse;
+    p.err = dev->err;
+    p.timeout_ns = wait_timeout_ns();
+
+    CUtensorMap tq, tk, tv;
+    if (encode_bf16_map(&tq, q, static_cast<long long>(Hq) * S, d) != RA_OK ||
+        encode_bf16_map(&tk, k, static_cast<long long>(Hkv) * S, d) != RA_OK ||
+        encode_bf16_map(&tv, v, static_cast<long long>(Hkv) * S, d) != RA_OK)
+        return RA_ERR_CUDA;
+    const int grid = p.n_items < dev->sms ? p.n_items : dev->sms;
+    return ra::launch_attn_bf16(p, tq, tk, tv, grid, stream);
+}
+
+int fwd_f32(const float* q, const float* k, const float* v, float* out, float* lse, int S, int Hq, int Hkv, int d,
+            int c, int causal, int layout, int kv_block, int hop, int sub, cudaStream_t stream) {
+    if (!q || !k || !v || !out || !lse) return RA_ERR_INVALID_ARG;
+    ra::Ring R;
+    int st = make_ring(S, Hq, Hkv, d, c, causal, layout, kv_block, &R);
+    if (st != RA_OK) return st;
+    if (d > 128) return RA_ERR_UNSUPPORTED;
+    if (R.c > 65535 || Hq > 65535) return RA_ERR_UNSUPPORTED;
+    if (hop >= 0 && (st = select_hop(&R, kv_block, hop, sub)) != RA_OK) return st;
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != RA_OK) return st;
+    ra::AttnF32Params p;
+    p.ring = R;
+    p.kv_block = kv_block;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.out = out;
+    p.lse = lse;
+    return ra::launch_attn_f32(p, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int ringattn_fwd(const void* q, const void* k, const void* v, float* out, float* lse, int S, int Hq, int Hkv, int d,
+                 int c, int causal, int layout, int kv_block, ra_stream_t stream) {
+    return fwd_bf16(q, k, v, out, lse, S, Hq, Hkv, d, c, causal, layout, kv_block, 0, -1, 0,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ringattn_fwd_natural(const void* q, const void* k, const void* v, float* out, float* lse, int S, int Hq,
+                         int Hkv, int d, int c, int causal, int layout, int kv_block, ra_stream_t stream) {
+    return fwd_bf16(q, k, v, out, lse, S, Hq, Hkv, d, c, causal, layout, kv_block, 1, -1, 0,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ringattn_fwd_hop(const void* q, const void* k, const void* v, float* o_part, float* lse_part, int S, int Hq,
+                     int Hkv, int d, int c, int causal, int layout, int kv_block, int hop, int sub,
+                     ra_stream_t stream) {
+    if (hop < 0) return RA_ERR_INVALID_ARG;
+    return fwd_bf16(q, k, v, o_part, lse_part, S, Hq, Hkv, d, c, causal, layout, kv_block, 0, hop, sub,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ringattn_fwd_f32(const float* q, const float* k, const float* v, float* out, float* lse, int S, int Hq,
+                     int Hkv, int d, int c, int causal, int layout, int kv_block, ra_stream_t stream) {
+    return fwd_f32(q, k, v, out, lse, S, Hq, Hkv, d, c, causal, layout, kv_block, -1, 0,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ringattn_fwd_hop_f32(const float* q, const float* k, const float* v, float* o_part, float* lse_part, int S,
+                         int Hq, int Hkv, int d, int c, int causal, int layout, int kv_block, int hop, int sub,
+                         ra_stream_t stream) {
+    if (hop < 0) return RA_ERR_INVALID_ARG;
+    return fwd_f32(q, k, v, o_part, lse_part, S, Hq, Hkv, d, c, causal, layout, kv_block, hop, sub,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ringattn_merge(float* o_run, float* lse_run, const float* o_part, const float* lse_part, long long rows, int d,
+                   ra_stream_t stream) {
+    if (rows < 0 || d < 1 || d > 4096) return RA_ERR_INVALID_ARG;
+    if (rows > 0 && (!o_run || !lse_run || !o_part || !lse_part)) return RA_ERR_INVALID_ARG;
+    if (rows == 0) return RA_OK;
+    DeviceInfo* dev = nullptr;
+    int st = device_info(&dev);
+    if (st != RA_OK) return st;
+    return ra::launch_merge(o_run, lse_run, o_part, lse_part, rows, d, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ringattn_permute(const void* src, void* dst, int S, int H, int row_bytes, int c, int layout, int inverse,
+                     ra_stream_t stream) {
+    if (!src || !dst || src == dst) return RA_ERR_INVALID_ARG;
+    if (S < 1 || H < 1 || row_bytes < 1 || c < 1) return RA_ERR_INVALID_ARG;
+    if ((layout != 0 && layout != 1) || (inverse != 0 && inverse != 1)) return RA_ERR_INVALID_ARG;
+    if (S % (c * (layout == 1 ? 2 : 1)) != 0) return RA_ERR_INVALID_ARG;
+    const long long bytes = static_cast<long long>(H) * S * row_bytes;
+    const char* a = static_cast<const char*>(src);
+    const char* b = static_cast<const char*>(dst);
+    if (a < b + bytes && b < a + bytes) return RA_ERR_INVALID_ARG;  // overlapping buffers
+    DeviceInfo* dev = nullptr;
+    int st = device_info(&dev);
+    if (st != RA_OK) return st;
+    return ra::launch_permute(src, dst, S, H, row_bytes, c, layout, inverse, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ringattn_rank_work(int S, int c, int causal, int layout, int tile, long long* units, long long* pairs,
+                       long long* tiles) {
+    if (S < 1 || c < 1 || tile < 1 || (causal != 0 && causal != 1) || (layout != 0 && layout != 1))
+        return RA_ERR_INVALID_ARG;
+    const int nch = c * (layout == 1 ? 2 : 1);
+    if (S % nch != 0) return RA_ERR_INVALID_ARG;
+    const long long m = S / nch, n_r = S / c;
+    const long long kv_tiles_per_chunk = (m + tile - 1) / tile;
+    for (int r = 0; r < c; ++r) {
+        const int nslot = layout == 1 ? 2 : 1;
+        long long u = 0, pr = 0, t = 0;
+        for (int slot = 0; slot < nslot; ++slot) {
+            const long long qc = slot == 0 ? r : 2LL * c - 1 - r;  // natural chunk
+            const long long a = qc * m;                            // its first position
+            u += causal ? qc + 1 : nch;
+            pr += causal ? m * a + m * (m + 1) / 2 : m * S;
+        }
+        // query tiles over the rank's local rows; positions grow with the local row
+        for (long long t0 = 0; t0 < n_r; t0 += tile) {
+            const long long last = (t0 + tile < n_r ? t0 + tile : n_r) - 1;
+            const long long slot = last / m;
+            const long long qc = slot == 0 ? r : 2LL * c - 1 - r;
+            const long long qmax = qc * m + (last - slot * m);
+            for (long long kc = 0; kc < nch; ++kc) {
+                if (!causal) {
+                    t += kv_tiles_per_chunk;
+                } else if (qmax >= kc * m) {
+                    const long long n = (qmax - kc * m) / tile + 1;
+                    t += n < kv_tiles_per_chunk ? n : kv_tiles_per_chunk;
+                }
+            }
+        }
+        if (units) units[r] = u;
+        if (pairs) pairs[r] = pr;
+        if (tiles) tiles[r] = t;
+    }
+    return RA_OK;
+}
+
+int ringattn_sync_status(ra_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return RA_ERR_CUDA;
+    DeviceInfo* dev = nullptr;
+    int st = device_info(&dev);
+    if (st != RA_OK) return st;
+    int word = 0;
+    if (cudaMemcpy(&word, dev->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return RA_ERR_CUDA;
+    if (word != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(dev->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return RA_ERR_CUDA;
+        return RA_ERR_TIMEOUT;
+    }
+    return RA_OK;
+}
+
+int ringattn_selftest_timeout(long long timeout_ns, ra_stream_t stream) {
+    if (timeout_ns < 1000 || timeout_ns > 10000000000LL) return RA_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    int st = device_info(&dev);
+    if (st != RA_OK) return st;
+    return ra::launch_selftest_timeout(dev->err, static_cast<unsigned long long>(timeout_ns),
+                                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char* ringattn_strerror(int status) {
+    switch (status) {
+        case RA_OK: return "ok";
+        case RA_ERR_INVALID_ARG: return "invalid argument";
+        case RA_ERR_UNSUPPORTED: return "unsupported shape or size";
+        case RA_ERR_ARCH: return "current device is not compute capability 10.3 (sm_103)";
+        case RA_ERR_CUDA: return "CUDA runtime error";
+        case RA_ERR_TIMEOUT: return "a bounded device wait ran out";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

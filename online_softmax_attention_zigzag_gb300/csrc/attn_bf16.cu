@@ -1,0 +1,582 @@
+// attn_bf16.cu -- fused ring attention on the tcgen05 tensor cores of sm_103a.
+//
+// What it computes ("Ring Attention and Ulysses shard a sequence two different
+// ways...", section "Ring Attention: point-to-point rotation, and an online softmax
+// that never sees the whole row at once"): every virtual rank keeps its query rows
+// fixed and visits the KV blocks in ring order -- hop h brings the block rank
+// (r - h) mod c started with ("Interrogating parallelism, part 5", "How does
+// attention survive being split?") -- folding each block into a running max, a
+// running sum and a rescaled output.  Chunks are contiguous or zigzag (rank i holds
+// chunks i and 2c-1-i, "What breaks the load balance?").  Under the causal mask,
+// key tiles that lie wholly after a query tile are never visited.
+//
+// Design (one CTA per SM, persistent):
+//   * a work item is two 128-row query tiles that share every K/V tile: two query
+//     heads of one KV group at the same positions, or two adjacent tiles of one head;
+//   * warp 9 (one thread) streams Q tiles and, in ring order, K and V tiles into
+//     shared memory with TMA (128-byte swizzle), through a ring of stages guarded by
+//     mbarriers;
+//   * warp 8 (one thread) issues tcgen05.mma: S_x = Q_x K^T into TMEM, and after
+//     softmax O_x += P_x V with P_x read from TMEM;
+//   * warpgroups 0 and 1 each own one query tile (thread = row): they read S from
+//     TMEM, apply the causal mask on diagonal tiles, update the running max and sum
+//     with exp2, write P (bf16) back to TMEM, rescale O in TMEM when the running max
+//     rose by more than 2^8, and at the end write out = O / (sum of the bf16 P) and
+//     lse = m + ln(sum of the exact p).
+//   The two warpgroups alternate, so one's softmax overlaps the other's MMAs.
+//
+// TMEM (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256) -- P_x is stored
+// as packed bf16 pairs in the upper half of S_x's columns -- O_0 [256, 256+D),
+// O_1 [256+D, 256+2D).
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ra {
+namespace {
+
+constexpr int kTile = 128;
+constexpr int kThreads = 384;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994531f;
+// The running max used for P is only moved when the true max exceeds it by more
+// than this (log2 units): P then stays below 2^8 and O needs no rescale otherwise.
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D>
+struct Cfg {
+    static constexpr int kTileBytes = kTile * D * 2;   // one 128 x D bf16 tile
+    static constexpr int kBoxBytes = kTile * 64 * 2;   // one 128 x 64 TMA box (16 KB)
+    static constexpr int kBoxes = D / 64;
+    static constexpr int kStages = (D == 128) ? 4 : 8;  // K/V tiles in flight (128 KB)
+    static constexpr int kQOff = 0;
+    static constexpr int kKVOff = 2 * kTileBytes;
+    static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+    static constexpr int kNumBars = 13 + 2 * kStages;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1 KB
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kOCol = 256;
+};
+
+struct Bars {
+    uint64_t* q_full;    // [2] loader -> mma (TMA bytes)
+    uint64_t* q_empty;   // [2] mma -> loader (last S MMA of an item done)
+    uint64_t* s_full;    // [2] mma -> softmax
+    uint64_t* p_full;    // [2] softmax (128 threads) -> mma
+    uint64_t* o_done;    // [2] mma -> softmax (last PV of an item done)
+    uint64_t* o_free;    // [2] softmax (128 threads) -> mma (O read out)
+    uint64_t* drain;     // [1] mma, on abort only
+    uint64_t* kv_full;   // [stages]
+    uint64_t* kv_empty;  // [stages]
+};
+
+// A work item: up to two query tiles (units) of one rank that share a KV head.
+struct Item {
+    int hq[2];    // query head of each unit; hq[1] < 0 when the item has one unit
+    int hk;       // KV head
+    int pos[2];   // natural position of each unit's first row
+    int r;        // virtual rank holding the units
+    int qrow[2];  // row of each unit's first query in q / out / lse
+    int pmax;     // last natural query position in the item
+};
+
+__device__ __forceinline__ void decode_item(const AttnBf16Params& p, int item, Item& it) {
+    const Ring& R = p.ring;
+    int t0, t1;
+    if (p.pair_mode == kPairHeads) {
+        const int per = R.Hq / 2, gh = R.g / 2;
+        const int pi = item / per, rem = item - pi * per;
+        t0 = t1 = p.n_tiles - 1 - pi;
+        it.hk = rem / gh;
+        it.hq[0] = it.hk * R.g + 2 * (rem - it.hk * gh);
+        it.hq[1] = it.hq[0] + 1;
+    } else if (p.pair_mode == kPairPositions) {
+        const int pi = item / R.Hq, h = item - pi * R.Hq;
+        t1 = p.n_tiles - 1 - 2 * pi;
+        t0 = t1 - 1;
+        it.hk = h / R.g;
+        it.hq[0] = it.hq[1] = h;
+    } else {
+        const int pi = item / R.Hq, h = item - pi * R.Hq;
+        t0 = t1 = p.n_tiles - 1 - pi;
+        it.hk = h / R.g;
+        it.hq[0] = h;
+        it.hq[1] = -1;
+    }
+    it.pos[0] = t0 * kTile;
+    it.pos[1] = t1 * kTile;
+    // rank and local row of a natural position (both units share chunk and rank)
+    int local0;
+    if (R.layout == 1) {
+        const int k = it.pos[0] / R.m;
+        it.r = (k < R.c) ? k : 2 * R.c - 1 - k;
+        local0 = ((k < R.c) ? 0 : R.m) + (it.pos[0] - k * R.m);
+    } else {
+        it.r = it.pos[0] / R.n_r;
+        local0 = it.pos[0] - it.r * R.n_r;
+    }
+    const int local1 = local0 + (it.pos[1] - it.pos[0]);
+    const int rbase = it.r * R.n_r;
+    it.qrow[0] = it.hq[0] * R.S + (p.natural ? it.pos[0] : rbase + local0);
+    it.qrow[1] = (it.hq[1] < 0) ? -1 : it.hq[1] * R.S + (p.natural ? it.pos[1] : rbase + local1);
+    it.pmax = max(it.pos[0], it.pos[1]) + kTile - 1;
+}
+
+// Visit the item's key tiles in ring order: f(kv_row, key_pos).  kv_row is the row of
+// the tile's first key in k / v; key_pos its natural position.
+template <class F>
+__device__ __forceinline__ void for_each_kv_tile(const AttnBf16Params& p, const Item& it, F&& f) {
+    const Ring& R = p.ring;
+    for (int hop = R.hop_lo; hop < R.hop_hi; ++hop) {
+        int s = it.r - hop;
+        if (s < 0) s += R.c;
+        for (int slot = 0; slot < R.nslot; ++slot) {
+            const int k = (slot == 0) ? s : 2 * R.c - 1 - s;  // natural chunk
+            const int base = slot * R.m;                      // its first local row in the block
+            const int lo = max(R.kv_lo, base);
+            int hi = min(R.kv_hi, base + R.m);
+            if (R.causal) hi = min(hi, base + max(0, it.pmax - k * R.m + 1));
+            for (int x = lo; x < hi; x += kTile) {
+                const int pos = k * R.m + (x - base);
+                const int row = it.hk * R.S + (p.natural ? pos : s * R.n_r + x);
+                if (!f(row, pos)) return;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ int count_kv_tiles(const AttnBf16Params& p, const Item& it) {
+    const Ring& R = p.ring;
+    int n = 0;
+    for (int hop = R.hop_lo; hop < R.hop_hi; ++hop) {
+        int s = it.r - hop;
+        if (s < 0) s += R.c;
+        for (int slot = 0; slot < R.nslot; ++slot) {
+            const int k = (slot == 0) ? s : 2 * R.c - 1 - s;
+            const int base = slot * R.m;
+            const int lo = max(R.kv_lo, base);
+            int hi = min(R.kv_hi, base + R.m);
+            if (R.causal) hi = min(hi, base + max(0, it.pmax - k * R.m + 1));
+            if (hi > lo) n += (hi - lo + kTile - 1) / kTile;
+        }
+    }
+    return n;
+}
+
+// Snake order over persistent CTAs: items are sorted by decreasing work, so
+// alternating the direction each round evens out the totals.
+__device__ __forceinline__ int item_of_round(int round) {
+    const int b = (round & 1) ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;
+    return round * gridDim.x + b;
+}
+
+// Bounded wait that ignores the abort flag (used to drain in-flight work on abort).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > timeout_ns) return;
+    }
+}
+
+// ------------------------------------------------------------------ TMA producer
+template <int D>
+__device__ void load_role(const AttnBf16Params& p, const CUtensorMap* tq, const CUtensorMap* tk,
+                          const CUtensorMap* tv, uint8_t* sQ, uint8_t* sKV, const Bars& b, const WaitCtl& wc) {
+    using C = Cfg<D>;
+    uint32_t kv_idx = 0, qit[2] = {0, 0};
+    bool ok = true;
+    for (int round = 0; ok; ++round) {
+        if (round * (int)gridDim.x >= p.n_items) break;
+        const int item = item_of_round(round);
+        if (item >= p.n_items) continue;
+        Item it;
+        decode_item(p, item, it);
+        if (count_kv_tiles(p, it) == 0) continue;
+        const int nx = (it.hq[1] >= 0) ? 2 : 1;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            if (x >= nx || !ok) break;
+            if (!mbar_wait(&b.q_empty[x], (qit[x] & 1u) ^ 1u, wc)) { ok = false; break; }
+            ++qit[x];
+            mbar_arrive_expect_tx(&b.q_full[x], C::kTileBytes);
+            const int qrow = x ? it.qrow[1] : it.qrow[0];
+#pragma unroll
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+                tma_load_2d(sQ + x * C::kTileBytes + bx * C::kBoxBytes, tq, &b.q_full[x], bx * 64, qrow);
+        }
+        if (!ok) break;
+        for_each_kv_tile(p, it, [&](int row, int) -> bool {
+            for (int kv = 0; kv < 2; ++kv) {
+                const uint32_t s = kv_idx % C::kStages;
+                if (!mbar_wait(&b.kv_empty[s], ((kv_idx / C::kStages) & 1u) ^ 1u, wc)) { ok = false; return false; }
+                mbar_arrive_expect_tx(&b.kv_full[s], C::kTileBytes);
+                const CUtensorMap* map = kv ? tv : tk;
+                for (int bx = 0; bx < C::kBoxes; ++bx)
+                    tma_load_2d(sKV + s * C::kTileBytes + bx * C::kBoxBytes, map, &b.kv_full[s], bx * 64, row);
+                ++kv_idx;
+            }
+            return true;
+        });
+    }
+    if (!ok) {
+        // let every copy already issued land before the CTA's shared memory goes away
+        for (uint32_t s = 0; s < (uint32_t)C::kStages && s < kv_idx; ++s) {
+            const uint32_t last = kv_idx - 1 - ((kv_idx - 1 - s) % C::kStages);
+            drain_wait(&b.kv_full[s], (last / C::kStages) & 1u, wc.timeout_ns);
+        }
+        for (int x = 0; x < 2; ++x)
+            if (qit[x] > 0) drain_wait(&b.q_full[x], (qit[x] - 1) & 1u, wc.timeout_ns);
+    }
+}
+
+// ------------------------------------------------------------------ MMA issuer
+template <int D>
+__device__ __forceinline__ void issue_s(uint32_t tmem, int x, uint32_t q_base, uint32_t k_base) {
+    using C = Cfg<D>;
+    constexpr uint32_t idesc = idesc_bf16(kTile, kTile, 0);
+    const uint32_t d_tmem = tmem + x * kTile;
+    // the start-address field holds (address >> 4): step it in place per K slice
+    const uint64_t qd = sdesc_sw128(q_base, 16, 1024);
+    const uint64_t kd = sdesc_sw128(k_base, 16, 1024);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4;
+        mma_ss(d_tmem, qd + off, kd + off, idesc, kk > 0 ? 1u : 0u);
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tmem, int x, uint32_t v_base, bool accumulate) {
+    using C = Cfg<D>;
+    constexpr uint32_t idesc = idesc_bf16(kTile, D, 1);
+    const uint32_t d_tmem = tmem + C::kOCol + x * D;
+    const uint32_t a_tmem = tmem + x * kTile + 64;
+    const uint64_t vd = sdesc_sw128(v_base, C::kBoxBytes, 1024);
+#pragma unroll
+    for (int kk = 0; kk < kTile / 16; ++kk) {
+        mma_ts(d_tmem, a_tmem + kk * 8, vd + ((kk * 16 * 128) >> 4), idesc, (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
+template <int D>
+__device__ void mma_role(const AttnBf16Params& p, uint8_t* sQ, uint8_t* sKV, const Bars& b, uint32_t tmem,
+                         const WaitCtl& wc) {
+    using C = Cfg<D>;
+    const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
+    uint32_t kv_idx = 0, qit[2] = {0, 0}, pit[2] = {0, 0};
+    bool ok = true;
+    for (int round = 0; ok; ++round) {
+        if (round * (int)gridDim.x >= p.n_items) break;
+        const int item = item_of_round(round);
+        if (item >= p.n_items) continue;
+        Item it;
+        decode_item(p, item, it);
+        const int nj = count_kv_tiles(p, it);
+        if (nj == 0) continue;
+        const int nx = (it.hq[1] >= 0) ? 2 : 1;
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+            if (x < nx && ok && !mbar_wait(&b.q_full[x], qit[x] & 1u, wc)) ok = false;
+        if (!ok) break;
+        // S(0)
+        uint32_t ks = kv_idx % C::kStages;
+        if (!mbar_wait(&b.kv_full[ks], (kv_idx / C::kStages) & 1u, wc)) { ok = false; break; }
+        ++kv_idx;
+        tc_fence_after();
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            if (x >= nx) break;
+            issue_s<D>(tmem, x, sQa + x * C::kTileBytes, sKVa + ks * C::kTileBytes);
+            mma_commit(&b.s_full[x]);
+        }
+        mma_commit(&b.kv_empty[ks]);
+        if (nj == 1)
+#pragma unroll
+            for (int x = 0; x < 2; ++x)
+                if (x < nx) mma_commit(&b.q_empty[x]);
+        for (int j = 0; j < nj && ok; ++j) {
+            const uint32_t vs = kv_idx % C::kStages;
+            if (!mbar_wait(&b.kv_full[vs], (kv_idx / C::kStages) & 1u, wc)) { ok = false; break; }
+            ++kv_idx;
+            const bool more = (j + 1 < nj);
+            const uint32_t ks2 = kv_idx % C::kStages;
+            const uint32_t ks2_par = (kv_idx / C::kStages) & 1u;
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                if (x >= nx) break;
+                if (!mbar_wait(&b.p_full[x], pit[x] & 1u, wc)) { ok = false; break; }
+                ++pit[x];
+                if (j == 0 && !mbar_wait(&b.o_free[x], (qit[x] & 1u) ^ 1u, wc)) { ok = false; break; }
+                tc_fence_after();
+                issue_pv<D>(tmem, x, sKVa + vs * C::kTileBytes, j > 0);
+                if (!more) mma_commit(&b.o_done[x]);
+                if (more) {
+                    if (x == 0) {
+                        if (!mbar_wait(&b.kv_full[ks2], ks2_par, wc)) { ok = false; break; }
+                        tc_fence_after();
+                    }
+                    issue_s<D>(tmem, x, sQa + x * C::kTileBytes, sKVa + ks2 * C::kTileBytes);
+                    mma_commit(&b.s_full[x]);
+                }
+            }
+            if (!ok) break;
+            mma_commit(&b.kv_empty[vs]);
+            if (more) {
+                ++kv_idx;
+                mma_commit(&b.kv_empty[ks2]);
+                if (j + 2 == nj)
+#pragma unroll
+                    for (int x = 0; x < 2; ++x)
+                        if (x < nx) mma_commit(&b.q_empty[x]);
+            }
+        }
+        qit[0] += 1;
+        qit[1] += (nx > 1) ? 1u : 0u;
+    }
+    if (!ok) {
+        // every MMA issued so far must finish before TMEM is released
+        mma_commit(b.drain);
+        drain_wait(b.drain, 0, wc.timeout_ns);
+    }
+}
+
+// ------------------------------------------------------------------ softmax warpgroups
+template <int D>
+__device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint32_t tmem, const WaitCtl& wc) {
+    using C = Cfg<D>;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;                  // this thread's row of the query tile
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t s_tmem = tmem + lane_off + x * kTile;
+    const uint32_t p_tmem = s_tmem + 64;
+    const uint32_t o_tmem = tmem + lane_off + C::kOCol + x * D;
+    const bool causal = p.ring.causal != 0;
+    uint32_t sit = 0, iit = 0;
+    bool ok = true;
+    for (int round = 0; ok; ++round) {
+        if (round * (int)gridDim.x >= p.n_items) break;
+        const int item = item_of_round(round);
+        if (item >= p.n_items) continue;
+        Item it;
+        decode_item(p, item, it);
+        const int my_hq = x ? it.hq[1] : it.hq[0];
+        if (my_hq < 0) continue;
+        const int nj = count_kv_tiles(p, it);
+        const size_t grow = static_cast<size_t>((x ? it.qrow[1] : it.qrow[0]) + row);
+        float* orow = p.out + grow * D;
+        if (nj == 0) {  // a message with no visible key for this tile
+            float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < D / 4; ++i) reinterpret_cast<float4*>(orow)[i] = z;
+            p.lse[grow] = -INFINITY;
+            continue;
+        }
+        const int tpos = x ? it.pos[1] : it.pos[0];
+        const int qpos = tpos + row;
+        // l: sum of the exact p (for lse); lr: sum of p as rounded to bf16 for the P V
+        // product, so that out = O / lr weighs every key consistently (a key that
+        // dominates the row then comes out exactly, whatever its rounding)
+        float m = -INFINITY, l = 0.f, lr = 0.f;
+        int j = 0;
+        for_each_kv_tile(p, it, [&](int, int kpos) -> bool {
+            // the warp leaves together: tcgen05.ld/st below are warp-collective
+            if (!__all_sync(0xffffffffu, mbar_wait(&b.s_full[x], sit & 1u, wc))) { ok = false; return false; }
+            ++sit;
+            tc_fence_after();
+            float s[kTile];
+            {
+                uint32_t r[32];
+#pragma unroll
+                for (int cchunk = 0; cchunk < 4; ++cchunk) {
+                    tmem_ld32(s_tmem + cchunk * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[cchunk * 32 + i] = __uint_as_float(r[i]);
+                }
+            }
+            if (causal && kpos + kTile - 1 > tpos) {  // tile crosses the diagonal
+                const int lim = qpos - kpos;          // keys [0, lim] of the tile are visible
+#pragma unroll
+                for (int i = 0; i < kTile; ++i) s[i] = (i > lim) ? -INFINITY : s[i];
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int i = 1; i < kTile; ++i) mx = fmaxf(mx, s[i]);
+            const float m_new = fmaxf(m, mx * kLog2e);
+            // Decide the reference max first; the O rescale itself waits until S is
+            // dead (after P is formed) to keep register pressure down.
+            float f = 1.f;
+            bool need = false;
+            if (j == 0) {
+                m = m_new;
+            } else if (m_new > m + kRescaleLog2) {
+                need = true;
+                f = ex2(m - m_new);
+                l *= f;
+                lr *= f;
+                m = m_new;
+            }
+            const float mu = (m == -INFINITY) ? 0.f : m;
+            float rs = 0.f, rr = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float a = ex2(fmaf(s[h * 64 + 2 * i], kLog2e, -mu));
+                    const float c2 = ex2(fmaf(s[h * 64 + 2 * i + 1], kLog2e, -mu));
+                    rs += a + c2;
+                    pk[i] = pack_bf16x2(a, c2);
+                    rr += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
+                }
+                tmem_st32(p_tmem + h * 32, pk);
+            }
+            // O is stable here: the commit that signalled this S also covered the
+            // previous P V, and the next P V waits for this warpgroup's arrival.
+            if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t o[32];
+                    tmem_ld32(o_tmem + cc * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+                    tmem_st32(o_tmem + cc * 32, o);
+                }
+            }
+            l += rs;
+            lr += rr;
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&b.p_full[x]);
+            ++j;
+            return true;
+        });
+        if (!ok) break;
+        if (!__all_sync(0xffffffffu, mbar_wait(&b.o_done[x], iit & 1u, wc))) { ok = false; break; }
+        ++iit;
+        tc_fence_after();
+        const float inv = (lr > 0.f) ? 1.f / lr : 0.f;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(o_tmem + cc * 32, o);
+            tmem_wait_ld();
+            float4* dst = reinterpret_cast<float4*>(orow + cc * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                     __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+        }
+        tc_fence_before();
+        mbar_arrive(&b.o_free[x]);
+        p.lse[grow] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bf16_kernel(const __grid_constant__ AttnBf16Params p, const __grid_constant__ CUtensorMap tq,
+                     const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sQ = smem + C::kQOff;
+    uint8_t* sKV = smem + C::kKVOff;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+    Bars b;
+    b.q_full = bars + 0;
+    b.q_empty = bars + 2;
+    b.s_full = bars + 4;
+    b.p_full = bars + 6;
+    b.o_done = bars + 8;
+    b.o_free = bars + 10;
+    b.drain = bars + 12;
+    b.kv_full = bars + 13;
+    b.kv_empty = bars + 13 + C::kStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&b.q_full[x], 1);
+            mbar_init(&b.q_empty[x], 1);
+            mbar_init(&b.s_full[x], 1);
+            mbar_init(&b.p_full[x], 128);
+            mbar_init(&b.o_done[x], 1);
+            mbar_init(&b.o_free[x], 128);
+        }
+        mbar_init(b.drain, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&b.kv_full[s], 1);
+            mbar_init(&b.kv_empty[s], 1);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 8) {
+        tmem_alloc(tmem_slot, C::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 9 && lane == 0) {
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtl wc{abort_flag, p.err, p.timeout_ns};
+
+    // Register split: the launch gives 384 threads x 168 registers.  The producer
+    // warpgroup (loader + MMA issuer) drops to 72 and the two softmax warpgroups
+    // rise to 216 each: 128 x (216 + 216 + 72) = 64512 = 384 x 168.
+    if (warp < 8) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 216;\n" ::: "memory");
+        softmax_role<D>(p, warp / 4, b, tmem, wc);
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n" ::: "memory");
+    }
+    if (warp < 8) {
+    } else if (warp == 8) {
+        if (lane == 0) mma_role<D>(p, sQ, sKV, b, tmem, wc);
+    } else if (warp == 9) {
+        if (lane == 0) load_role<D>(p, &tq, &tk, &tv, sQ, sKV, b, wc);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 8) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+template <int D>
+int launch_d(const AttnBf16Params& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+             int grid, cudaStream_t stream) {
+    using C = Cfg<D>;
+    auto kern = attn_bf16_kernel<D>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+        return -4;
+    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(p, tq, tk, tv);
+    return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+}  // namespace
+
+size_t attn_bf16_smem_bytes(int d) {
+    return d == 128 ? Cfg<128>::kSmemBytes : Cfg<64>::kSmemBytes;
+}
+
+int launch_attn_bf16(const AttnBf16Params& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                     const CUtensorMap& tv, int grid, cudaStream_t stream) {
+    if (p.ring.d == 128) return launch_d<128>(p, tq, tk, tv, grid, stream);
+    if (p.ring.d == 64) return launch_d<64>(p, tq, tk, tv, grid, stream);
+    return -2;
+}
+
+}  // namespace ra

@@ -1,0 +1,63 @@
+// internal.h -- parameter blocks and launchers shared by the translation units of
+// libringattn.so.  Not part of the public ABI (that is include/ringattn.h).
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace ra {
+
+// Ring geometry, fixed per call.
+//   n_r  rows per rank (S / c);  m  rows per chunk (n_r, or n_r / 2 for zigzag);
+//   nslot chunks per rank (1 or 2).  A rank's local row x lies in chunk slot x / m;
+//   slot 0 holds natural chunk r, slot 1 (zigzag) natural chunk 2c-1-r.
+struct Ring {
+    int S, Hq, Hkv, g, d, c, causal, layout;
+    int n_r, m, nslot;
+    // messages visited: hops [hop_lo, hop_hi) and, inside each held block, local
+    // key rows [kv_lo, kv_hi) (the whole block for the fused path)
+    int hop_lo, hop_hi, kv_lo, kv_hi;
+};
+
+// How query tiles are grouped two by two onto the two softmax warpgroups of a CTA.
+enum PairMode : int {
+    kPairHeads = 0,      // two query heads of one KV group at the same position
+    kPairPositions = 1,  // two adjacent 128-row tiles of one head, same chunk
+    kSingles = 2         // one tile per work item
+};
+
+struct AttnBf16Params {
+    Ring ring;
+    int natural;    // 1: tensors in natural order (chunk map folded into addressing)
+    int pair_mode;
+    int n_tiles;    // 128-row query tiles per head (S / 128)
+    int n_items;
+    float* out;
+    float* lse;
+    int* err;
+    unsigned long long timeout_ns;
+};
+
+struct AttnF32Params {
+    Ring ring;
+    int kv_block;
+    const float* q;
+    const float* k;
+    const float* v;
+    float* out;
+    float* lse;
+};
+
+int launch_attn_bf16(const AttnBf16Params& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                     const CUtensorMap& tv, int grid, cudaStream_t stream);
+int launch_attn_f32(const AttnF32Params& p, cudaStream_t stream);
+int launch_permute(const void* src, void* dst, int S, int H, int row_bytes, int c, int layout, int inverse,
+                   cudaStream_t stream);
+int launch_merge(float* o_run, float* lse_run, const float* o_part, const float* lse_part, long long rows,
+                 int d, cudaStream_t stream);
+int launch_selftest_timeout(int* err, unsigned long long timeout_ns, cudaStream_t stream);
+
+// Shared-memory footprint of the bf16 kernel for head dimension d.
+size_t attn_bf16_smem_bytes(int d);
+
+}  // namespace ra

@@ -1,0 +1,186 @@
+// permute_merge.cu -- the HBM-bound kernels of the path:
+//   * chunk permutation between natural and rank-major order (contiguous: identity
+//     map of c chunks; zigzag: natural chunk k of 2c goes to rank k if k < c, else to
+//     rank 2c-1-k as its second chunk -- "Interrogating parallelism, part 5", "What
+//     breaks the load balance?");
+//   * the exact (O, LSE) merge of a ring message's partial into a running result
+//     (same page, "How does attention survive being split?");
+//   * a self-test kernel whose only wait is never satisfied and runs out.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ra {
+namespace {
+
+// ------------------------------------------------------------------ permutation
+// The tensor is H * nchunks slabs of `slab` bytes.  Work item = one vector of width
+// sizeof(V) inside one destination slab; four independent vectors per thread per
+// iteration keep enough loads in flight to approach the copy bandwidth.
+template <typename V>
+__global__ void __launch_bounds__(256) permute_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                                      long long slab_vecs, int nchunks, int c, int layout,
+                                                      int inverse, long long total_vecs) {
+    constexpr int kUnroll = 4;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long base = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; base < total_vecs;
+         base += stride * kUnroll) {
+        V vals[kUnroll];
+        long long dsto[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const long long i = base + u * stride;  // vector index in the destination
+            dsto[u] = -1;
+            if (i < total_vecs) {
+                const long long slab = i / slab_vecs;
+                const long long off = i - slab * slab_vecs;
+                const long long h = slab / nchunks;
+                const int dslab = static_cast<int>(slab - h * nchunks);
+                // natural chunk <-> rank-major chunk
+                int sslab;
+                if (layout == 1) {
+                    if (!inverse) {  // dst is rank-major: rank-major chunk j = 2r + slot
+                        const int r = dslab >> 1, slot = dslab & 1;
+                        sslab = slot ? 2 * c - 1 - r : r;
+                    } else {         // dst is natural chunk k
+                        const int k = dslab;
+                        sslab = (k < c) ? 2 * k : 2 * (2 * c - 1 - k) + 1;
+                    }
+                } else {
+                    sslab = dslab;
+                }
+                vals[u] = reinterpret_cast<const V*>(src)[(h * nchunks + sslab) * slab_vecs + off];
+                dsto[u] = i;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            if (dsto[u] >= 0) reinterpret_cast<V*>(dst)[dsto[u]] = vals[u];
+    }
+}
+
+template <typename V>
+int launch_permute_v(const void* src, void* dst, long long slab_bytes, int H, int nchunks, int c, int layout,
+                     int inverse, cudaStream_t stream) {
+    const long long slab_vecs = slab_bytes / static_cast<long long>(sizeof(V));
+    const long long total = slab_vecs * H * nchunks;
+    if (total == 0) return 0;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long per_block = 256LL * 4;
+    long long blocks = (total + per_block - 1) / per_block;
+    const long long cap = static_cast<long long>(sms) * 8;  // 8 CTAs of 256 threads per SM
+    if (blocks > cap) blocks = cap;
+    permute_kernel<V><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), slab_vecs, nchunks, c, layout, inverse,
+        total);
+    return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+// ------------------------------------------------------------------ merge
+__device__ __forceinline__ float mix(float x, float wa, bool use_a, float y, float wb, bool use_b) {
+    return (use_a ? x * wa : 0.f) + (use_b ? y * wb : 0.f);
+}
+
+// One warp per row at a time; the lanes stride over the row.  Every lane reads
+// lse_run before the warp synchronises and lane 0 overwrites it, so the in-place
+// update never races.
+template <bool kVec4>
+__global__ void __launch_bounds__(256) merge_kernel(float* __restrict__ o_run, float* __restrict__ lse_run,
+                                                    const float* __restrict__ o_part,
+                                                    const float* __restrict__ lse_part, long long rows, int d) {
+    const int lane = threadIdx.x & 31;
+    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
+    for (long long row = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; row < rows;
+         row += warps) {
+        const float a = lse_run[row];
+        const float b = lse_part[row];
+        const float M = fmaxf(a, b);
+        float wa, wb, lse;
+        if (M == -INFINITY) {  // neither partial saw a key
+            wa = 0.f;
+            wb = 0.f;
+            lse = -INFINITY;
+        } else {
+            const float ea = expf(a - M), eb = expf(b - M);  // exp(-inf) = 0: weight 0
+            const float tot = ea + eb;
+            wa = ea / tot;
+            wb = eb / tot;
+            lse = M + logf(tot);
+        }
+        // a side with no key contributes exactly nothing, whatever its o holds
+        const bool use_a = a != -INFINITY, use_b = b != -INFINITY;
+        const size_t base = static_cast<size_t>(row) * d;
+        if (kVec4) {
+            float4* orun = reinterpret_cast<float4*>(o_run + base);
+            const float4* opart = reinterpret_cast<const float4*>(o_part + base);
+            for (int i = lane; i < d / 4; i += 32) {
+                const float4 x = orun[i], y = opart[i];
+                orun[i] = make_float4(mix(x.x, wa, use_a, y.x, wb, use_b), mix(x.y, wa, use_a, y.y, wb, use_b),
+                                      mix(x.z, wa, use_a, y.z, wb, use_b), mix(x.w, wa, use_a, y.w, wb, use_b));
+            }
+        } else {
+            for (int i = lane; i < d; i += 32)
+                o_run[base + i] = mix(o_run[base + i], wa, use_a, o_part[base + i], wb, use_b);
+        }
+        __syncwarp();
+        if (lane == 0) lse_run[row] = lse;
+    }
+}
+
+// ------------------------------------------------------------------ bounded-wait self test
+__global__ void selftest_timeout_kernel(int* err, unsigned long long timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const WaitCtl wc{&abort_flag, err, timeout_ns};
+        // nothing ever arrives on `bar`: the wait must give up and record the error
+        (void)mbar_wait(&bar, 0, wc);
+    }
+}
+
+}  // namespace
+
+int launch_permute(const void* src, void* dst, int S, int H, int row_bytes, int c, int layout, int inverse,
+                   cudaStream_t stream) {
+    const int nchunks = c * (layout == 1 ? 2 : 1);
+    const long long slab = static_cast<long long>(S / nchunks) * row_bytes;
+    const uintptr_t align = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst) |
+                            static_cast<uintptr_t>(slab);
+    if ((align & 15) == 0) return launch_permute_v<uint4>(src, dst, slab, H, nchunks, c, layout, inverse, stream);
+    if ((align & 7) == 0) return launch_permute_v<uint2>(src, dst, slab, H, nchunks, c, layout, inverse, stream);
+    if ((align & 3) == 0) return launch_permute_v<uint32_t>(src, dst, slab, H, nchunks, c, layout, inverse, stream);
+    if ((align & 1) == 0) return launch_permute_v<uint16_t>(src, dst, slab, H, nchunks, c, layout, inverse, stream);
+    return launch_permute_v<uint8_t>(src, dst, slab, H, nchunks, c, layout, inverse, stream);
+}
+
+int launch_merge(float* o_run, float* lse_run, const float* o_part, const float* lse_part, long long rows, int d,
+                 cudaStream_t stream) {
+    if (rows == 0) return 0;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long warps_needed = rows;
+    long long blocks = (warps_needed + 7) / 8;
+    const long long cap = static_cast<long long>(sms) * 8;
+    if (blocks > cap) blocks = cap;
+    const bool vec = (d % 4 == 0) && ((reinterpret_cast<uintptr_t>(o_run) | reinterpret_cast<uintptr_t>(o_part)) & 15) == 0;
+    if (vec)
+        merge_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o_run, lse_run, o_part, lse_part, rows, d);
+    else
+        merge_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o_run, lse_run, o_part, lse_part, rows, d);
+    return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+int launch_selftest_timeout(int* err, unsigned long long timeout_ns, cudaStream_t stream) {
+    selftest_timeout_kernel<<<1, 32, 0, stream>>>(err, timeout_ns);
+    return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+}  // namespace ra

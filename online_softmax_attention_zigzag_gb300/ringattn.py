@@ -1,0 +1,217 @@
+"""Thin Python binding of libringattn.so (C ABI in include/ringattn.h).
+
+Argument marshalling only: every function checks shapes/dtypes/devices of the
+torch tensors it is given, passes their device pointers and sizes to the C
+entry point of the same name, and raises :class:`RingAttnError` on a non-zero
+status.  PyTorch provides device memory and streams; all computation happens in
+the library's CUDA kernels.  There is no fallback: if the library is missing
+or the device is not sm_103, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libringattn.so")
+
+RA_OK = 0
+RA_ERR_INVALID_ARG = -1
+RA_ERR_UNSUPPORTED = -2
+RA_ERR_ARCH = -3
+RA_ERR_CUDA = -4
+RA_ERR_TIMEOUT = -5
+
+EXPORTS = (
+    "ringattn_fwd", "ringattn_fwd_natural", "ringattn_fwd_f32", "ringattn_fwd_hop",
+    "ringattn_fwd_hop_f32", "ringattn_merge", "ringattn_permute", "ringattn_rank_work",
+    "ringattn_sync_status", "ringattn_selftest_timeout", "ringattn_strerror",
+)
+
+
+class RingAttnError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} failed: {code} ({strerror(code)})")
+
+
+_lib = None
+
+_P, _I, _LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
+_ATTN = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I]
+
+
+def lib() -> ctypes.CDLL:
+    """Load the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                "or python -m online_softmax_attention_zigzag_gb300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        sig = {
+            "ringattn_fwd": _ATTN + [_P],
+            "ringattn_fwd_natural": _ATTN + [_P],
+            "ringattn_fwd_f32": _ATTN + [_P],
+            "ringattn_fwd_hop": _ATTN + [_I, _I, _P],
+            "ringattn_fwd_hop_f32": _ATTN + [_I, _I, _P],
+            "ringattn_merge": [_P, _P, _P, _P, _LL, _I, _P],
+            "ringattn_permute": [_P, _P, _I, _I, _I, _I, _I, _I, _P],
+            "ringattn_rank_work": [_I, _I, _I, _I, _I, _P, _P, _P],
+            "ringattn_sync_status": [_P],
+            "ringattn_selftest_timeout": [_LL, _P],
+        }
+        for name, args in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = _I
+        L.ringattn_strerror.argtypes = [_I]
+        L.ringattn_strerror.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    try:
+        return lib().ringattn_strerror(int(code)).decode()
+    except Exception:  # the library itself may be missing
+        return "unknown"
+
+
+def _check(fn: str, code: int) -> None:
+    if code != RA_OK:
+        raise RingAttnError(fn, code)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _attn_args(q, k, v, out, lse, in_dtype):
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise ValueError("q, k, v must be [H, S, d]")
+    Hq, S, d = q.shape
+    Hkv = k.shape[0]
+    if tuple(k.shape) != (Hkv, S, d) or tuple(v.shape) != (Hkv, S, d):
+        raise ValueError("k and v must be [Hkv, S, d] with q's S and d")
+    if tuple(out.shape) != (Hq, S, d) or tuple(lse.shape) != (Hq, S):
+        raise ValueError("out must be [Hq, S, d] and lse [Hq, S]")
+    ptrs = [_dev(q, "q", in_dtype), _dev(k, "k", in_dtype), _dev(v, "v", in_dtype),
+            _dev(out, "out", torch.float32), _dev(lse, "lse", torch.float32)]
+    return ptrs, S, Hq, Hkv, d
+
+
+def fwd(q, k, v, out, lse, *, c, causal, layout, kv_block, stream=None) -> None:
+    """ringattn_fwd: bf16 rank-major q [Hq,S,d], k/v [Hkv,S,d] -> fp32 out, lse."""
+    ptrs, S, Hq, Hkv, d = _attn_args(q, k, v, out, lse, torch.bfloat16)
+    _check("ringattn_fwd", lib().ringattn_fwd(*ptrs, S, Hq, Hkv, d, c, int(causal), layout, kv_block,
+                                              ctypes.c_void_p(_stream(stream))))
+
+
+def fwd_natural(q, k, v, out, lse, *, c, causal, layout, kv_block, stream=None) -> None:
+    """ringattn_fwd_natural: as :func:`fwd` with every tensor in natural order."""
+    ptrs, S, Hq, Hkv, d = _attn_args(q, k, v, out, lse, torch.bfloat16)
+    _check("ringattn_fwd_natural", lib().ringattn_fwd_natural(
+        *ptrs, S, Hq, Hkv, d, c, int(causal), layout, kv_block, ctypes.c_void_p(_stream(stream))))
+
+
+def fwd_f32(q, k, v, out, lse, *, c, causal, layout, kv_block, stream=None) -> None:
+    """ringattn_fwd_f32: fp32 rank-major inputs."""
+    ptrs, S, Hq, Hkv, d = _attn_args(q, k, v, out, lse, torch.float32)
+    _check("ringattn_fwd_f32", lib().ringattn_fwd_f32(*ptrs, S, Hq, Hkv, d, c, int(causal), layout,
+                                                      kv_block, ctypes.c_void_p(_stream(stream))))
+
+
+def fwd_hop(q, k, v, o_part, lse_part, *, c, causal, layout, kv_block, hop, sub, stream=None) -> None:
+    """ringattn_fwd_hop: the partial of one ring message (bf16 inputs)."""
+    ptrs, S, Hq, Hkv, d = _attn_args(q, k, v, o_part, lse_part, torch.bfloat16)
+    _check("ringattn_fwd_hop", lib().ringattn_fwd_hop(*ptrs, S, Hq, Hkv, d, c, int(causal), layout,
+                                                      kv_block, hop, sub, ctypes.c_void_p(_stream(stream))))
+
+
+def fwd_hop_f32(q, k, v, o_part, lse_part, *, c, causal, layout, kv_block, hop, sub, stream=None) -> None:
+    """ringattn_fwd_hop_f32: the partial of one ring message (fp32 inputs)."""
+    ptrs, S, Hq, Hkv, d = _attn_args(q, k, v, o_part, lse_part, torch.float32)
+    _check("ringattn_fwd_hop_f32", lib().ringattn_fwd_hop_f32(
+        *ptrs, S, Hq, Hkv, d, c, int(causal), layout, kv_block, hop, sub, ctypes.c_void_p(_stream(stream))))
+
+
+def merge(o_run, lse_run, o_part, lse_part, stream=None) -> None:
+    """ringattn_merge: fold (o_part, lse_part) into (o_run, lse_run) in place."""
+    d = o_run.shape[-1]
+    rows = lse_run.numel()
+    if o_run.numel() != rows * d or o_part.shape != o_run.shape or lse_part.shape != lse_run.shape:
+        raise ValueError("o_* must be [..., d] with one lse per row")
+    _check("ringattn_merge", lib().ringattn_merge(
+        _dev(o_run, "o_run", torch.float32), _dev(lse_run, "lse_run", torch.float32),
+        _dev(o_part, "o_part", torch.float32), _dev(lse_part, "lse_part", torch.float32),
+        rows, d, ctypes.c_void_p(_stream(stream))))
+
+
+def permute(src, dst, *, c, layout, inverse, stream=None) -> None:
+    """ringattn_permute: src/dst [H, S, ...] contiguous, same shape and dtype."""
+    if src.shape != dst.shape or src.dtype != dst.dtype:
+        raise ValueError("src and dst must have the same shape and dtype")
+    H, S = src.shape[0], src.shape[1]
+    row_bytes = src.element_size() * (src.numel() // max(1, H * S))
+    _check("ringattn_permute", lib().ringattn_permute(
+        _dev(src, "src"), _dev(dst, "dst"), S, H, row_bytes, c, layout, int(inverse),
+        ctypes.c_void_p(_stream(stream))))
+
+
+def rank_work(S: int, c: int, causal: int, layout: int, tile: int = 128):
+    """ringattn_rank_work (host only): per-rank (units, pairs, tiles) as int64 arrays."""
+    u = np.zeros(c, dtype=np.int64)
+    p = np.zeros(c, dtype=np.int64)
+    t = np.zeros(c, dtype=np.int64)
+    _check("ringattn_rank_work", lib().ringattn_rank_work(
+        S, c, int(causal), layout, tile, u.ctypes.data_as(ctypes.c_void_p),
+        p.ctypes.data_as(ctypes.c_void_p), t.ctypes.data_as(ctypes.c_void_p)))
+    return u, p, t
+
+
+def sync_status(stream=None) -> int:
+    """ringattn_sync_status: synchronise, return RA_OK or RA_ERR_TIMEOUT / RA_ERR_CUDA."""
+    return lib().ringattn_sync_status(ctypes.c_void_p(_stream(stream)))
+
+
+def selftest_timeout(timeout_ns: int, stream=None) -> None:
+    _check("ringattn_selftest_timeout", lib().ringattn_selftest_timeout(
+        int(timeout_ns), ctypes.c_void_p(_stream(stream))))
+
+
+def attention(q, k, v, *, c, causal, layout, kv_block, stream=None):
+    """Natural-order convenience call: permute q/k/v to rank-major, run the fused
+    kernel, permute out/lse back.  Returns (out fp32 [Hq,S,d], lse fp32 [Hq,S])."""
+    Hq, S, d = q.shape
+    dev = q.device
+    qr, kr, vr = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    permute(q, qr, c=c, layout=layout, inverse=0, stream=stream)
+    permute(k, kr, c=c, layout=layout, inverse=0, stream=stream)
+    permute(v, vr, c=c, layout=layout, inverse=0, stream=stream)
+    o_r = torch.empty((Hq, S, d), dtype=torch.float32, device=dev)
+    l_r = torch.empty((Hq, S), dtype=torch.float32, device=dev)
+    fwd(qr, kr, vr, o_r, l_r, c=c, causal=causal, layout=layout, kv_block=kv_block, stream=stream)
+    out = torch.empty_like(o_r)
+    lse = torch.empty_like(l_r)
+    permute(o_r, out, c=c, layout=layout, inverse=1, stream=stream)
+    permute(l_r, lse, c=c, layout=layout, inverse=1, stream=stream)
+    return out, lse
