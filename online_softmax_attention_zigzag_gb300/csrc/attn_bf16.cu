@@ -386,15 +386,21 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
             if (!__all_sync(0xffffffffu, mbar_wait(&b.s_full[x], sit & 1u, wc))) { ok = false; return false; }
             ++sit;
             tc_fence_after();
+            // S row: four 32-column loads in flight, one wait
             float s[kTile];
             {
-                uint32_t r[32];
+                uint32_t r0[32], r1[32], r2[32], r3[32];
+                tmem_ld32(s_tmem + 0, r0);
+                tmem_ld32(s_tmem + 32, r1);
+                tmem_ld32(s_tmem + 64, r2);
+                tmem_ld32(s_tmem + 96, r3);
+                tmem_wait_ld();
 #pragma unroll
-                for (int cchunk = 0; cchunk < 4; ++cchunk) {
-                    tmem_ld32(s_tmem + cchunk * 32, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[cchunk * 32 + i] = __uint_as_float(r[i]);
+                for (int i = 0; i < 32; ++i) {
+                    s[i] = __uint_as_float(r0[i]);
+                    s[32 + i] = __uint_as_float(r1[i]);
+                    s[64 + i] = __uint_as_float(r2[i]);
+                    s[96 + i] = __uint_as_float(r3[i]);
                 }
             }
             if (causal && kpos + kTile - 1 > tpos) {  // tile crosses the diagonal
@@ -402,9 +408,18 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
 #pragma unroll
                 for (int i = 0; i < kTile; ++i) s[i] = (i > lim) ? -INFINITY : s[i];
             }
-            float mx = s[0];
+            // row max: eight independent chains of 3-input max, then a small tree
+            float mx;
+            {
+                float c[8];
 #pragma unroll
-            for (int i = 1; i < kTile; ++i) mx = fmaxf(mx, s[i]);
+                for (int a = 0; a < 8; ++a) c[a] = fmaxf(s[2 * a], s[2 * a + 1]);
+#pragma unroll
+                for (int i = 16; i < kTile; i += 16)
+#pragma unroll
+                    for (int a = 0; a < 8; ++a) c[a] = fmax3(c[a], s[i + 2 * a], s[i + 2 * a + 1]);
+                mx = fmax3(fmax3(c[0], c[1], c[2]), fmax3(c[3], c[4], c[5]), fmaxf(c[6], c[7]));
+            }
             const float m_new = fmaxf(m, mx * kLog2e);
             // Decide the reference max first; the O rescale itself waits until S is
             // dead (after P is formed) to keep register pressure down.
@@ -419,32 +434,49 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
                 lr *= f;
                 m = m_new;
             }
-            const float mu = (m == -INFINITY) ? 0.f : m;
-            float rs = 0.f, rr = 0.f;
+            const float nmu = (m == -INFINITY) ? 0.f : -m;
+            // p = 2^(s*log2e - m) two lanes per instruction; exact and bf16-rounded row
+            // sums in four packed accumulators each
+            float se[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            float sr[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float a = ex2(fmaf(s[h * 64 + 2 * i], kLog2e, -mu));
-                    const float c2 = ex2(fmaf(s[h * 64 + 2 * i + 1], kLog2e, -mu));
-                    rs += a + c2;
+                    float t0, t1;
+                    ffma2(t0, t1, s[h * 64 + 2 * i], s[h * 64 + 2 * i + 1], kLog2e, kLog2e, nmu, nmu);
+                    const float a = ex2(t0), c2 = ex2(t1);
+                    const int q4 = 2 * (i & 3);
+                    fadd2(se[q4], se[q4 + 1], se[q4], se[q4 + 1], a, c2);
                     pk[i] = pack_bf16x2(a, c2);
-                    rr += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
+                    fadd2(sr[q4], sr[q4 + 1], sr[q4], sr[q4 + 1], __uint_as_float(pk[i] << 16),
+                          __uint_as_float(pk[i] & 0xffff0000u));
                 }
                 tmem_st32(p_tmem + h * 32, pk);
             }
+            fadd2(se[0], se[1], se[0], se[1], se[2], se[3]);
+            fadd2(se[4], se[5], se[4], se[5], se[6], se[7]);
+            fadd2(sr[0], sr[1], sr[0], sr[1], sr[2], sr[3]);
+            fadd2(sr[4], sr[5], sr[4], sr[5], sr[6], sr[7]);
+            const float rs = (se[0] + se[1]) + (se[4] + se[5]);
+            const float rr = (sr[0] + sr[1]) + (sr[4] + sr[5]);
             // O is stable here: the commit that signalled this S also covered the
             // previous P V, and the next P V waits for this warpgroup's arrival.
             if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t o[32];
-                    tmem_ld32(o_tmem + cc * 32, o);
+                for (int cc = 0; cc < D / 32; cc += 2) {
+                    uint32_t o0[32], o1[32];
+                    tmem_ld32(o_tmem + cc * 32, o0);
+                    tmem_ld32(o_tmem + cc * 32 + 32, o1);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-                    tmem_st32(o_tmem + cc * 32, o);
+                    for (int i = 0; i < 32; ++i) {
+                        o0[i] = __float_as_uint(__uint_as_float(o0[i]) * f);
+                        o1[i] = __float_as_uint(__uint_as_float(o1[i]) * f);
+                    }
+                    tmem_st32(o_tmem + cc * 32, o0);
+                    tmem_st32(o_tmem + cc * 32 + 32, o1);
                 }
             }
             l += rs;
@@ -461,15 +493,19 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
         tc_fence_after();
         const float inv = (lr > 0.f) ? 1.f / lr : 0.f;
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t o[32];
-            tmem_ld32(o_tmem + cc * 32, o);
+        for (int cc = 0; cc < D / 32; cc += 2) {
+            uint32_t o0[32], o1[32];
+            tmem_ld32(o_tmem + cc * 32, o0);
+            tmem_ld32(o_tmem + cc * 32 + 32, o1);
             tmem_wait_ld();
             float4* dst = reinterpret_cast<float4*>(orow + cc * 32);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
-                                     __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+            for (int i = 0; i < 8; ++i) {
+                dst[i] = make_float4(__uint_as_float(o0[4 * i]) * inv, __uint_as_float(o0[4 * i + 1]) * inv,
+                                     __uint_as_float(o0[4 * i + 2]) * inv, __uint_as_float(o0[4 * i + 3]) * inv);
+                dst[8 + i] = make_float4(__uint_as_float(o1[4 * i]) * inv, __uint_as_float(o1[4 * i + 1]) * inv,
+                                         __uint_as_float(o1[4 * i + 2]) * inv, __uint_as_float(o1[4 * i + 3]) * inv);
+            }
         }
         tc_fence_before();
         mbar_arrive(&b.o_free[x]);
@@ -534,13 +570,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const WaitCtl wc{abort_flag, p.err, p.timeout_ns};
 
     // Register split: the launch gives 384 threads x 168 registers.  The producer
-    // warpgroup (loader + MMA issuer) drops to 72 and the two softmax warpgroups
-    // rise to 216 each: 128 x (216 + 216 + 72) = 64512 = 384 x 168.
+    // warpgroup (loader + MMA issuer) drops to 136 and the two softmax warpgroups
+    // rise to 184 each: 128 x (184 + 184 + 136) = 64512 = 384 x 168.
     if (warp < 8) {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 216;\n" ::: "memory");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 184;\n" ::: "memory");
         softmax_role<D>(p, warp / 4, b, tmem, wc);
     } else {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n" ::: "memory");
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 136;\n" ::: "memory");
     }
     if (warp < 8) {
     } else if (warp == 8) {
