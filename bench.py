@@ -51,6 +51,10 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the 128k workload and the natural-order step measured beside the headline")
+    ap.add_argument("--per-hop-sweep", action="store_true",
+                    help="instead of the headline: fused vs per-hop + merge over the workload's kv_block sweep")
     return ap.parse_args()
 
 
@@ -136,11 +140,11 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle baseline
-def cpu_oracle_sample(w, budget_s: float, seed: int = 7):
+def cpu_oracle_sample(w, budget_s: float, seed: int = 7, qkv=None):
     """Time the float64 oracle on sampled query rows of workload ``w``; returns
-    (TFLOP/s, rows, seconds, threads)."""
+    (TFLOP/s, rows, seconds, threads).  Input generation is not timed."""
     from oracle.attention import full_attention_rows
-    q, k, v = make_qkv(w)
+    q, k, v = qkv if qkv is not None else make_qkv(w)
     hs, ps = sample_rows(w.bhq, w.seq, 1 << 20, seed=seed)
     perm = np.random.default_rng(seed).permutation(len(hs))
     hs, ps = hs.numpy()[perm], ps.numpy()[perm]
@@ -173,8 +177,9 @@ def run_reference(args, w, rank):
     rows_total = 0
     threads = 1
     budget = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    qkv = make_qkv(w)
     for i in range(args.warmup + args.steps):
-        tf, rows, secs, threads = cpu_oracle_sample(w, budget, seed=100 + i)
+        tf, rows, secs, threads = cpu_oracle_sample(w, budget, seed=100 + i, qkv=qkv)
         if i >= args.warmup:
             per_step.append((tf, rows, secs))
             rows_total += rows
@@ -195,6 +200,76 @@ def run_reference(args, w, rank):
 
 
 # ------------------------------------------------------------------ GPU arm
+def time_events(fn, reps, stream):
+    """Mean device time (ms) of fn() over reps calls, CUDA events on `stream`."""
+    fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def attention_only(ra, w, dev, stream, reps, peak):
+    """Fused kernel on rank-major device inputs of workload w: TFLOP/s and fraction of peak."""
+    q_h, k_h, v_h = make_qkv(w)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    del q_h, k_h, v_h
+    qr, kr, vr = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    for src, dst in ((q, qr), (k, kr), (v, vr)):
+        ra.permute(src, dst, c=w.c, layout=w.layout, inverse=0)
+    del q, k, v
+    o = torch.empty((w.bhq, w.seq, w.d), dtype=torch.float32, device=dev)
+    l = torch.empty((w.bhq, w.seq), dtype=torch.float32, device=dev)
+    kw = dict(c=w.c, causal=w.causal, layout=w.layout, kv_block=w.kv_block)
+    ms = time_events(lambda: ra.fwd(qr, kr, vr, o, l, **kw), reps, stream)
+    if ra.sync_status() != ra.RA_OK:
+        raise SystemExit("device wait timed out")
+    tf = w.flops() / (ms * 1e-3) / 1e12
+    return {"workload": w.name, "kernel_ms": ms, "achieved": tf, "unit": "TFLOP/s", "peak": peak,
+            "frac": tf / peak, "launches": reps + 1}
+
+
+def per_hop_sweep(ra, w, dev, stream):
+    """Fused kernel vs the ring-faithful per-hop path (one partial per message, folded in
+    with the merge kernel) for each kv_block of the workload's sweep."""
+    q_h, k_h, v_h = make_qkv(w)
+    qr, kr, vr = (torch.empty(x.shape, dtype=x.dtype, device=dev) for x in (q_h, k_h, v_h))
+    for src, dst in ((q_h, qr), (k_h, kr), (v_h, vr)):
+        ra.permute(src.to(dev), dst, c=w.c, layout=w.layout, inverse=0)
+    o = torch.empty((w.bhq, w.seq, w.d), dtype=torch.float32, device=dev)
+    l = torch.empty((w.bhq, w.seq), dtype=torch.float32, device=dev)
+    op, lp = torch.empty_like(o), torch.empty_like(l)
+    rows = w.bhq * w.seq
+    out = []
+    for kvb in (w.kv_sweep or (w.kv_block,)):
+        kw = dict(c=w.c, causal=w.causal, layout=w.layout, kv_block=kvb)
+        fused_ms = time_events(lambda: ra.fwd(qr, kr, vr, o, l, **kw), 3, stream)
+        n_msg = (w.seq // w.c) // kvb
+
+        def ring():
+            o.zero_()
+            l.fill_(-float("inf"))
+            for hop in range(w.c):
+                for sub in range(n_msg):
+                    ra.fwd_hop(qr, kr, vr, op, lp, hop=hop, sub=sub, **kw)
+                    ra.merge(o, l, op, lp)
+        ring_ms = time_events(ring, 1, stream)
+        merge_ms = time_events(lambda: ra.merge(o, l, op, lp), 3, stream)
+        mbytes = rows * (12 * w.d + 12)
+        out.append({"kv_block": kvb, "messages": w.c * n_msg, "fused_ms": fused_ms,
+                    "fused_tflops": w.flops() / (fused_ms * 1e-3) / 1e12, "per_hop_ms": ring_ms,
+                    "per_hop_tflops": w.flops() / (ring_ms * 1e-3) / 1e12, "merge_ms": merge_ms,
+                    "merge_gbs": mbytes / (merge_ms * 1e-3) / 1e9,
+                    "merge_traffic_gib": w.c * n_msg * mbytes / 2**30})
+    if ra.sync_status() != ra.RA_OK:
+        raise SystemExit("device wait timed out")
+    return out
+
+
 def main():
     args = parse()
     w = WORKLOADS[args.workload]
@@ -210,6 +285,13 @@ def main():
     from online_softmax_attention_zigzag_gb300 import ringattn as ra
     ra.lib()
     torch.cuda.set_device(local)
+    if args.per_hop_sweep:
+        dev = torch.device("cuda", local)
+        res = per_hop_sweep(ra, w, dev, torch.cuda.current_stream(dev))
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "unit": UNIT, "mode": "per-hop sweep", "workload": w.name,
+                              "sweep": res}), flush=True)
+        return
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -304,6 +386,9 @@ def main():
         torch.cuda.synchronize()
         return a.elapsed_time(b) / reps
 
+    # the same path with the chunk map folded into the kernel's tile addressing: no
+    # permutation passes (natural-order inputs and outputs)
+    nat_ms = time_ms(lambda: ra.fwd_natural(q, k, v, out, lse, **kw))
     rows = w.bhq * S
     merge_ms = time_ms(lambda: ra.merge(o_r, l_r, out, lse))
     merge_bytes = rows * (12 * w.d + 12)
@@ -325,9 +410,16 @@ def main():
     h2d = sum(x.numel() * x.element_size() for x in (q_h, k_h, v_h))
     d2h = out_h.numel() * 4 + lse_h.numel() * 4
 
+    extra = None
+    if not args.no_extra and w.name == CAUSAL_GQA_S32K.name:
+        del qr, kr, vr, o_r, l_r
+        torch.cuda.empty_cache()
+        extra = attention_only(ra, WORKLOADS["causal_gqa_S131072_h32x8_d128_c16_zigzag"], dev, stream, 5,
+                               peaks()[0])
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        tf, rows_s, secs, threads = cpu_oracle_sample(w, args.cpu_seconds)
+        tf, rows_s, secs, threads = cpu_oracle_sample(w, args.cpu_seconds, qkv=(q_h, k_h, v_h))
         cpu = {"value": tf, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{rows_s} sampled query rows ({secs:.1f} s), float64 numpy, same inputs"}
 
@@ -346,6 +438,9 @@ def main():
                          "kernel": "attn_bf16_kernel<%d>" % w.d, "kernel_ms": attn_ms,
                          "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
                          "frac_of_sustained": (achieved / bf16_sust) if bf16_sust else None},
+            "natural_step": {"ms_per_step": nat_ms, "value": flop / (nat_ms * 1e-3) / 1e12, "unit": UNIT,
+                             "what": "ringattn_fwd_natural: chunk map in TMA addressing, no permutation passes"},
+            "also_measured": extra,
             "secondary": {
                 "merge": {"bound": "hbm", "achieved": merge_bytes / (merge_ms * 1e-3) / 1e9, "peak": hbm_peak,
                           "unit": "GB/s", "frac": merge_bytes / (merge_ms * 1e-3) / 1e9 / hbm_peak,

@@ -37,7 +37,8 @@ namespace ra {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kThreads = 384;
+constexpr int kThreads = 576;  // 4 softmax warpgroups + MMA warp + TMA warp
+constexpr int kMmaWarp = 16, kLoadWarp = 17;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
 // The running max used for P is only moved when the true max exceeds it by more
@@ -53,9 +54,10 @@ struct Cfg {
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = 2 * kTileBytes;
     static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
-    static constexpr int kNumBars = 13 + 2 * kStages;
+    static constexpr int kNumBars = 15 + 2 * kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base to 1 KB
+    static constexpr int kXchgOff = kMiscOff + 16;              // softmax exchange: 2 x 8 x 128 floats
+    static constexpr int kSmemBytes = kXchgOff + 2 * 8 * kTile * 4 + 1024;  // + slack to align the base
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kOCol = 256;
 };
@@ -68,6 +70,7 @@ struct Bars {
     uint64_t* o_done;    // [2] mma -> softmax (last PV of an item done)
     uint64_t* o_free;    // [2] softmax (128 threads) -> mma (O read out)
     uint64_t* drain;     // [1] mma, on abort only
+    uint64_t* tok;       // [2] softmax turn: tok[x] completes when the other tile's softmax is done
     uint64_t* kv_full;   // [stages]
     uint64_t* kv_empty;  // [stages]
 };
@@ -198,7 +201,7 @@ __device__ void load_role(const AttnBf16Params& p, const CUtensorMap* tq, const 
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
             if (x >= nx || !ok) break;
-            if (!mbar_wait(&b.q_empty[x], (qit[x] & 1u) ^ 1u, wc)) { ok = false; break; }
+            if (!mbar_wait(&b.q_empty[x], (qit[x] & 1u) ^ 1u, wc, 32)) { ok = false; break; }
             ++qit[x];
             mbar_arrive_expect_tx(&b.q_full[x], C::kTileBytes);
             const int qrow = x ? it.qrow[1] : it.qrow[0];
@@ -210,7 +213,7 @@ __device__ void load_role(const AttnBf16Params& p, const CUtensorMap* tq, const 
         for_each_kv_tile(p, it, [&](int row, int) -> bool {
             for (int kv = 0; kv < 2; ++kv) {
                 const uint32_t s = kv_idx % C::kStages;
-                if (!mbar_wait(&b.kv_empty[s], ((kv_idx / C::kStages) & 1u) ^ 1u, wc)) { ok = false; return false; }
+                if (!mbar_wait(&b.kv_empty[s], ((kv_idx / C::kStages) & 1u) ^ 1u, wc, 32)) { ok = false; return false; }
                 mbar_arrive_expect_tx(&b.kv_full[s], C::kTileBytes);
                 const CUtensorMap* map = kv ? tv : tk;
                 for (int bx = 0; bx < C::kBoxes; ++bx)
@@ -232,6 +235,14 @@ __device__ void load_role(const AttnBf16Params& p, const CUtensorMap* tq, const 
 }
 
 // ------------------------------------------------------------------ MMA issuer
+// desc + off computed where it is used: an opaque add keeps the compiler from hoisting
+// every (descriptor, K-slice) pair out of the loops into registers.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t off16) {
+    uint64_t r;
+    asm volatile("add.s64 %0, %1, %2;" : "=l"(r) : "l"(desc), "l"(static_cast<uint64_t>(off16)));
+    return r;
+}
+
 template <int D>
 __device__ __forceinline__ void issue_s(uint32_t tmem, int x, uint32_t q_base, uint32_t k_base) {
     using C = Cfg<D>;
@@ -243,7 +254,7 @@ __device__ __forceinline__ void issue_s(uint32_t tmem, int x, uint32_t q_base, u
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4;
-        mma_ss(d_tmem, qd + off, kd + off, idesc, kk > 0 ? 1u : 0u);
+        mma_ss(d_tmem, desc_add(qd, off), desc_add(kd, off), idesc, kk > 0 ? 1u : 0u);
     }
 }
 
@@ -256,7 +267,8 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, int x, uint32_t v_base, 
     const uint64_t vd = sdesc_sw128(v_base, C::kBoxBytes, 1024);
 #pragma unroll
     for (int kk = 0; kk < kTile / 16; ++kk) {
-        mma_ts(d_tmem, a_tmem + kk * 8, vd + ((kk * 16 * 128) >> 4), idesc, (accumulate || kk > 0) ? 1u : 0u);
+        mma_ts(d_tmem, a_tmem + kk * 8, desc_add(vd, (kk * 16 * 128) >> 4), idesc,
+               (accumulate || kk > 0) ? 1u : 0u);
     }
 }
 
@@ -343,18 +355,42 @@ __device__ void mma_role(const AttnBf16Params& p, uint8_t* sQ, uint8_t* sKV, con
 }
 
 // ------------------------------------------------------------------ softmax warpgroups
+// Named barrier over the two warpgroups (256 threads) that share query tile x; returns
+// the AND of every thread's `ok`, so that both halves leave together on an abort.
+__device__ __forceinline__ bool unit_bar_and(int x, bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.and.pred po, %2, 256, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(ok ? 1u : 0u), "r"(1 + x)
+        : "memory");
+    return r != 0;
+}
+
+// One warpgroup owns column half h (keys [64h, 64h+64) of every key tile) of query tile
+// x; thread t of the warpgroup owns row t.  The two halves of a tile exchange their
+// partial row maxima through shared memory once per key tile, so both compute P against
+// the same reference max; row sums stay per half until the epilogue.
 template <int D>
-__device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint32_t tmem, const WaitCtl& wc) {
+__device__ void softmax_role(const AttnBf16Params& p, int x, int h, const Bars& b, uint32_t tmem, float* xchg,
+                             const WaitCtl& wc) {
     using C = Cfg<D>;
+    constexpr int kHalf = kTile / 2;   // key columns per warpgroup
+    constexpr int kOHalf = D / 2;      // output columns per warpgroup
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int wq = warp & 3;
-    const int row = wq * 32 + lane;                  // this thread's row of the query tile
+    const int row = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t s_tmem = tmem + lane_off + x * kTile;
-    const uint32_t p_tmem = s_tmem + 64;
-    const uint32_t o_tmem = tmem + lane_off + C::kOCol + x * D;
+    const uint32_t s_tmem = tmem + lane_off + x * kTile + h * kHalf;   // my 64 score columns
+    const uint32_t p_tmem = tmem + lane_off + x * kTile + 64 + h * 32;  // my 32 packed P columns
+    const uint32_t o_tmem = tmem + lane_off + C::kOCol + x * D + h * kOHalf;
+    // exchange slots per tile x: max [tile parity][half][row], sums [half][l | lr][row]
+    float* xm = xchg + x * (8 * kTile);
+    float* xs = xm + 4 * kTile;
     const bool causal = p.ring.causal != 0;
-    uint32_t sit = 0, iit = 0;
+    const bool poller = h == 0 && wq == 0;  // the warp that waits on the tile's barriers
+    uint32_t sit = 0, iit = 0, tit = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
         if (round * (int)gridDim.x >= p.n_items) break;
@@ -364,14 +400,15 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
         decode_item(p, item, it);
         const int my_hq = x ? it.hq[1] : it.hq[0];
         if (my_hq < 0) continue;
+        const bool pair = it.hq[1] >= 0;  // two tiles: their softmax phases alternate
         const int nj = count_kv_tiles(p, it);
         const size_t grow = static_cast<size_t>((x ? it.qrow[1] : it.qrow[0]) + row);
-        float* orow = p.out + grow * D;
+        float* orow = p.out + grow * D + h * kOHalf;
         if (nj == 0) {  // a message with no visible key for this tile
             float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int i = 0; i < D / 4; ++i) reinterpret_cast<float4*>(orow)[i] = z;
-            p.lse[grow] = -INFINITY;
+            for (int i = 0; i < kOHalf / 4; ++i) reinterpret_cast<float4*>(orow)[i] = z;
+            if (h == 0) p.lse[grow] = -INFINITY;
             continue;
         }
         const int tpos = x ? it.pos[1] : it.pos[0];
@@ -382,47 +419,60 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
         float m = -INFINITY, l = 0.f, lr = 0.f;
         int j = 0;
         for_each_kv_tile(p, it, [&](int, int kpos) -> bool {
-            // the warp leaves together: tcgen05.ld/st below are warp-collective
-            if (!__all_sync(0xffffffffu, mbar_wait(&b.s_full[x], sit & 1u, wc))) { ok = false; return false; }
+            // One warp of the tile polls; the other seven wait in the named barrier, which
+            // costs no issue slots (spinning warps would steal them from the ones computing).
+            // Turn-taking: tile 0's softmax and tile 1's alternate (0, 1, 0, 1, ...), so each
+            // runs alone on the SM's schedulers while the tensor core works on the other
+            // tile's MMAs.  Tile 0's first wait passes at once (it waits on the phase before
+            // the first).
+            bool w_ok = true;
+            if (poller) {
+                if (pair) w_ok = mbar_wait(&b.tok[x], (tit & 1u) ^ (x == 0 ? 1u : 0u), wc);
+                w_ok = __all_sync(0xffffffffu, w_ok && mbar_wait(&b.s_full[x], sit & 1u, wc));
+            }
+            if (pair) ++tit;
+            w_ok = unit_bar_and(x, w_ok);
+            const uint32_t par = sit & 1u;
             ++sit;
             tc_fence_after();
-            // S row: four 32-column loads in flight, one wait
-            float s[kTile];
-            {
-                uint32_t r0[32], r1[32], r2[32], r3[32];
+            float s[kHalf];
+            if (w_ok) {
+                uint32_t r0[32], r1[32];
                 tmem_ld32(s_tmem + 0, r0);
                 tmem_ld32(s_tmem + 32, r1);
-                tmem_ld32(s_tmem + 64, r2);
-                tmem_ld32(s_tmem + 96, r3);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     s[i] = __uint_as_float(r0[i]);
                     s[32 + i] = __uint_as_float(r1[i]);
-                    s[64 + i] = __uint_as_float(r2[i]);
-                    s[96 + i] = __uint_as_float(r3[i]);
                 }
-            }
-            if (causal && kpos + kTile - 1 > tpos) {  // tile crosses the diagonal
-                const int lim = qpos - kpos;          // keys [0, lim] of the tile are visible
+            } else {
 #pragma unroll
-                for (int i = 0; i < kTile; ++i) s[i] = (i > lim) ? -INFINITY : s[i];
+                for (int i = 0; i < kHalf; ++i) s[i] = 0.f;
             }
-            // row max: eight independent chains of 3-input max, then a small tree
+            const int kcol = kpos + h * kHalf;  // natural position of my first key column
+            if (causal && kcol + kHalf - 1 > qpos - row) {  // my half may cross the diagonal
+                const int lim = qpos - kcol;                // my keys [0, lim] are visible
+#pragma unroll
+                for (int i = 0; i < kHalf; ++i) s[i] = (i > lim) ? -INFINITY : s[i];
+            }
             float mx;
             {
-                float c[8];
+                float c[4];
 #pragma unroll
-                for (int a = 0; a < 8; ++a) c[a] = fmaxf(s[2 * a], s[2 * a + 1]);
+                for (int a = 0; a < 4; ++a) c[a] = fmaxf(s[2 * a], s[2 * a + 1]);
 #pragma unroll
-                for (int i = 16; i < kTile; i += 16)
+                for (int i = 8; i < kHalf; i += 8)
 #pragma unroll
-                    for (int a = 0; a < 8; ++a) c[a] = fmax3(c[a], s[i + 2 * a], s[i + 2 * a + 1]);
-                mx = fmax3(fmax3(c[0], c[1], c[2]), fmax3(c[3], c[4], c[5]), fmaxf(c[6], c[7]));
+                    for (int a = 0; a < 4; ++a) c[a] = fmax3(c[a], s[i + 2 * a], s[i + 2 * a + 1]);
+                mx = fmaxf(fmax3(c[0], c[1], c[2]), c[3]);
             }
+            // both halves have read their scores (the P stores below overwrite the upper
+            // half of S) and published their partial max
+            xm[(par * 2 + h) * kTile + row] = mx;
+            if (!unit_bar_and(x, w_ok)) { ok = false; return false; }
+            mx = fmaxf(mx, xm[(par * 2 + (h ^ 1)) * kTile + row]);
             const float m_new = fmaxf(m, mx * kLog2e);
-            // Decide the reference max first; the O rescale itself waits until S is
-            // dead (after P is formed) to keep register pressure down.
             float f = 1.f;
             bool need = false;
             if (j == 0) {
@@ -435,81 +485,73 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
                 m = m_new;
             }
             const float nmu = (m == -INFINITY) ? 0.f : -m;
-            // p = 2^(s*log2e - m) two lanes per instruction; exact and bf16-rounded row
-            // sums in four packed accumulators each
-            float se[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            float sr[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            float se[4] = {0.f, 0.f, 0.f, 0.f};
+            float sr[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t pk[32];
+            for (int hh = 0; hh < 4; ++hh) {
+                uint32_t pk[8];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
+                for (int i = 0; i < 8; ++i) {
                     float t0, t1;
-                    ffma2(t0, t1, s[h * 64 + 2 * i], s[h * 64 + 2 * i + 1], kLog2e, kLog2e, nmu, nmu);
+                    ffma2(t0, t1, s[hh * 16 + 2 * i], s[hh * 16 + 2 * i + 1], kLog2e, kLog2e, nmu, nmu);
                     const float a = ex2(t0), c2 = ex2(t1);
-                    const int q4 = 2 * (i & 3);
-                    fadd2(se[q4], se[q4 + 1], se[q4], se[q4 + 1], a, c2);
+                    const int q2 = 2 * (i & 1);
+                    fadd2(se[q2], se[q2 + 1], se[q2], se[q2 + 1], a, c2);
                     pk[i] = pack_bf16x2(a, c2);
-                    fadd2(sr[q4], sr[q4 + 1], sr[q4], sr[q4 + 1], __uint_as_float(pk[i] << 16),
-                          __uint_as_float(pk[i] & 0xffff0000u));
+                    add_bf16x2_f32(sr[q2], sr[q2 + 1], pk[i]);
                 }
-                tmem_st32(p_tmem + h * 32, pk);
+                tmem_st8(p_tmem + hh * 8, pk);
             }
-            fadd2(se[0], se[1], se[0], se[1], se[2], se[3]);
-            fadd2(se[4], se[5], se[4], se[5], se[6], se[7]);
-            fadd2(sr[0], sr[1], sr[0], sr[1], sr[2], sr[3]);
-            fadd2(sr[4], sr[5], sr[4], sr[5], sr[6], sr[7]);
-            const float rs = (se[0] + se[1]) + (se[4] + se[5]);
-            const float rr = (sr[0] + sr[1]) + (sr[4] + sr[5]);
             // O is stable here: the commit that signalled this S also covered the
-            // previous P V, and the next P V waits for this warpgroup's arrival.
+            // previous P V, and the next P V waits for this tile's arrivals.
             if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-                for (int cc = 0; cc < D / 32; cc += 2) {
-                    uint32_t o0[32], o1[32];
-                    tmem_ld32(o_tmem + cc * 32, o0);
-                    tmem_ld32(o_tmem + cc * 32 + 32, o1);
+                for (int cc = 0; cc < kOHalf; cc += 32) {
+                    uint32_t o0[32];
+                    tmem_ld32(o_tmem + cc, o0);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        o0[i] = __float_as_uint(__uint_as_float(o0[i]) * f);
-                        o1[i] = __float_as_uint(__uint_as_float(o1[i]) * f);
-                    }
-                    tmem_st32(o_tmem + cc * 32, o0);
-                    tmem_st32(o_tmem + cc * 32 + 32, o1);
+                    for (int i = 0; i < 32; ++i) o0[i] = __float_as_uint(__uint_as_float(o0[i]) * f);
+                    tmem_st32(o_tmem + cc, o0);
                 }
             }
-            l += rs;
-            lr += rr;
+            l += (se[0] + se[1]) + (se[2] + se[3]);
+            lr += (sr[0] + sr[1]) + (sr[2] + sr[3]);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&b.p_full[x]);
+            if (pair) mbar_arrive(&b.tok[x ^ 1]);  // the other tile's turn
             ++j;
             return true;
         });
         if (!ok) break;
-        if (!__all_sync(0xffffffffu, mbar_wait(&b.o_done[x], iit & 1u, wc))) { ok = false; break; }
+        // epilogue: combine the two halves' sums, then each half writes its output columns
+        xs[(h * 2 + 0) * kTile + row] = l;
+        xs[(h * 2 + 1) * kTile + row] = lr;
+        bool d_ok = true;
+        if (poller) d_ok = __all_sync(0xffffffffu, mbar_wait(&b.o_done[x], iit & 1u, wc));
         ++iit;
+        if (!unit_bar_and(x, d_ok)) { ok = false; break; }
+        const float l_all = l + xs[((h ^ 1) * 2 + 0) * kTile + row];
+        const float lr_all = lr + xs[((h ^ 1) * 2 + 1) * kTile + row];
         tc_fence_after();
-        const float inv = (lr > 0.f) ? 1.f / lr : 0.f;
+        const float inv = (lr_all > 0.f) ? 1.f / lr_all : 0.f;
 #pragma unroll
-        for (int cc = 0; cc < D / 32; cc += 2) {
-            uint32_t o0[32], o1[32];
-            tmem_ld32(o_tmem + cc * 32, o0);
-            tmem_ld32(o_tmem + cc * 32 + 32, o1);
+        for (int cc = 0; cc < kOHalf; cc += 32) {
+            uint32_t o0[32];
+            tmem_ld32(o_tmem + cc, o0);
             tmem_wait_ld();
-            float4* dst = reinterpret_cast<float4*>(orow + cc * 32);
+            float4* dst = reinterpret_cast<float4*>(orow + cc);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < 8; ++i)
                 dst[i] = make_float4(__uint_as_float(o0[4 * i]) * inv, __uint_as_float(o0[4 * i + 1]) * inv,
                                      __uint_as_float(o0[4 * i + 2]) * inv, __uint_as_float(o0[4 * i + 3]) * inv);
-                dst[8 + i] = make_float4(__uint_as_float(o1[4 * i]) * inv, __uint_as_float(o1[4 * i + 1]) * inv,
-                                         __uint_as_float(o1[4 * i + 2]) * inv, __uint_as_float(o1[4 * i + 3]) * inv);
-            }
         }
         tc_fence_before();
         mbar_arrive(&b.o_free[x]);
-        p.lse[grow] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
+        if (h == 0) p.lse[grow] = (l_all > 0.f) ? (m + log2f(l_all)) * kLn2 : -INFINITY;
+        // the sum slots are rewritten only at the next item's epilogue, after both halves
+        // have passed at least one more exchange barrier
     }
 }
 
@@ -531,8 +573,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     b.o_done = bars + 8;
     b.o_free = bars + 10;
     b.drain = bars + 12;
-    b.kv_full = bars + 13;
-    b.kv_empty = bars + 13 + C::kStages;
+    b.tok = bars + 13;
+    b.kv_full = bars + 15;
+    b.kv_empty = bars + 15 + C::kStages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
 
@@ -542,11 +585,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&b.q_full[x], 1);
             mbar_init(&b.q_empty[x], 1);
             mbar_init(&b.s_full[x], 1);
-            mbar_init(&b.p_full[x], 128);
+            mbar_init(&b.p_full[x], 256);
             mbar_init(&b.o_done[x], 1);
-            mbar_init(&b.o_free[x], 128);
+            mbar_init(&b.o_free[x], 256);
         }
         mbar_init(b.drain, 1);
+        mbar_init(&b.tok[0], 256);
+        mbar_init(&b.tok[1], 256);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&b.kv_full[s], 1);
             mbar_init(&b.kv_empty[s], 1);
@@ -554,11 +599,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 8) {
+    if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, C::kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 9 && lane == 0) {
+    if (warp == kLoadWarp && lane == 0) {
         tma_prefetch_desc(&tq);
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
@@ -569,26 +614,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const WaitCtl wc{abort_flag, p.err, p.timeout_ns};
 
-    // Register split: the launch gives 384 threads x 168 registers.  The producer
-    // warpgroup (loader + MMA issuer) drops to 136 and the two softmax warpgroups
-    // rise to 184 each: 128 x (184 + 184 + 136) = 64512 = 384 x 168.
-    if (warp < 8) {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 184;\n" ::: "memory");
-        softmax_role<D>(p, warp / 4, b, tmem, wc);
-    } else {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 136;\n" ::: "memory");
-    }
-    if (warp < 8) {
-    } else if (warp == 8) {
+    // warps 0-15: softmax, warpgroup g = warp / 4 owns tile g / 2, key half g % 2
+    if (warp < 16) {
+        softmax_role<D>(p, warp / 8, (warp / 4) & 1, b, tmem, reinterpret_cast<float*>(smem + C::kXchgOff), wc);
+    } else if (warp == kMmaWarp) {
         if (lane == 0) mma_role<D>(p, sQ, sKV, b, tmem, wc);
-    } else if (warp == 9) {
+    } else if (warp == kLoadWarp) {
         if (lane == 0) load_role<D>(p, &tq, &tk, &tv, sQ, sKV, b, wc);
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 8) tmem_dealloc(tmem, C::kTmemCols);
+    if (warp == kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
 }
 
 template <int D>
