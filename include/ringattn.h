@@ -161,6 +161,15 @@ int ringattn_sync_status(ra_stream_t stream);
  */
 int ringattn_selftest_timeout(long long timeout_ns, ra_stream_t stream);
 
+/*
+ * ringattn_last_timeout -- host only.  Where the last timeout that ringattn_sync_status
+ * reported happened: info[0] = shared-memory address of the barrier whose wait ran out,
+ * info[1] = CTA index, info[2] = thread index within the CTA (all 0 if none yet).
+ * info must hold 3 ints.  A diagnostic for reports; the values are not stable across
+ * library versions.
+ */
+int ringattn_last_timeout(int* info);
+
 /* ringattn_strerror -- static description of a status code. */
 const char* ringattn_strerror(int status);
 

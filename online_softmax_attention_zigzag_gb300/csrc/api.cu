@@ -18,7 +18,7 @@ namespace {
 // Device error word: bounded waits that run out write RA_ERR_TIMEOUT here.  It is a
 // static device variable, so the library allocates nothing; host code reaches it
 // through the address cudaGetSymbolAddress returns for the current device.
-__device__ int g_err_word;
+__device__ int g_err_word[4];  // status, record set, barrier address, (block << 10 | thread)
 
 constexpr int kMaxDevices = 64;
 
@@ -30,6 +30,7 @@ struct DeviceInfo {
 };
 
 std::mutex g_mu;
+int g_last_timeout[3] = {0, 0, 0};  // barrier address, CTA, thread of the last recorded timeout
 DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -313,11 +314,17 @@ int ringattn_sync_status(ra_stream_t stream) {
     DeviceInfo* dev = nullptr;
     int st = device_info(&dev);
     if (st != RA_OK) return st;
-    int word = 0;
-    if (cudaMemcpy(&word, dev->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return RA_ERR_CUDA;
-    if (word != 0) {
-        const int zero = 0;
-        if (cudaMemcpy(dev->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return RA_ERR_CUDA;
+    int rec[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(rec, dev->err, sizeof(rec), cudaMemcpyDeviceToHost) != cudaSuccess) return RA_ERR_CUDA;
+    if (rec[0] != 0) {
+        {
+            std::lock_guard<std::mutex> lock(g_mu);
+            g_last_timeout[0] = rec[2];
+            g_last_timeout[1] = rec[3] >> 10;
+            g_last_timeout[2] = rec[3] & 1023;
+        }
+        const int zero[4] = {0, 0, 0, 0};
+        if (cudaMemcpy(dev->err, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return RA_ERR_CUDA;
         return RA_ERR_TIMEOUT;
     }
     return RA_OK;
@@ -330,6 +337,15 @@ int ringattn_selftest_timeout(long long timeout_ns, ra_stream_t stream) {
     if (st != RA_OK) return st;
     return ra::launch_selftest_timeout(dev->err, static_cast<unsigned long long>(timeout_ns),
                                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ringattn_last_timeout(int* info) {
+    if (!info) return RA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_mu);
+    info[0] = g_last_timeout[0];
+    info[1] = g_last_timeout[1];
+    info[2] = g_last_timeout[2];
+    return RA_OK;
 }
 
 const char* ringattn_strerror(int status) {

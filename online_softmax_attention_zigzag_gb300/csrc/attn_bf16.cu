@@ -54,7 +54,7 @@ struct Cfg {
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = 2 * kTileBytes;
     static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
-    static constexpr int kNumBars = 15 + 2 * kStages;
+    static constexpr int kNumBars = 13 + 2 * kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kXchgOff = kMiscOff + 16;              // softmax exchange: 2 x 8 x 128 floats
     static constexpr int kSmemBytes = kXchgOff + 2 * 8 * kTile * 4 + 1024;  // + slack to align the base
@@ -70,7 +70,6 @@ struct Bars {
     uint64_t* o_done;    // [2] mma -> softmax (last PV of an item done)
     uint64_t* o_free;    // [2] softmax (128 threads) -> mma (O read out)
     uint64_t* drain;     // [1] mma, on abort only
-    uint64_t* tok;       // [2] softmax turn: tok[x] completes when the other tile's softmax is done
     uint64_t* kv_full;   // [stages]
     uint64_t* kv_empty;  // [stages]
 };
@@ -390,7 +389,7 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, int h, const Bars& 
     float* xs = xm + 4 * kTile;
     const bool causal = p.ring.causal != 0;
     const bool poller = h == 0 && wq == 0;  // the warp that waits on the tile's barriers
-    uint32_t sit = 0, iit = 0, tit = 0;
+    uint32_t sit = 0, iit = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
         if (round * (int)gridDim.x >= p.n_items) break;
@@ -400,7 +399,6 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, int h, const Bars& 
         decode_item(p, item, it);
         const int my_hq = x ? it.hq[1] : it.hq[0];
         if (my_hq < 0) continue;
-        const bool pair = it.hq[1] >= 0;  // two tiles: their softmax phases alternate
         const int nj = count_kv_tiles(p, it);
         const size_t grow = static_cast<size_t>((x ? it.qrow[1] : it.qrow[0]) + row);
         float* orow = p.out + grow * D + h * kOHalf;
@@ -421,16 +419,8 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, int h, const Bars& 
         for_each_kv_tile(p, it, [&](int, int kpos) -> bool {
             // One warp of the tile polls; the other seven wait in the named barrier, which
             // costs no issue slots (spinning warps would steal them from the ones computing).
-            // Turn-taking: tile 0's softmax and tile 1's alternate (0, 1, 0, 1, ...), so each
-            // runs alone on the SM's schedulers while the tensor core works on the other
-            // tile's MMAs.  Tile 0's first wait passes at once (it waits on the phase before
-            // the first).
             bool w_ok = true;
-            if (poller) {
-                if (pair) w_ok = mbar_wait(&b.tok[x], (tit & 1u) ^ (x == 0 ? 1u : 0u), wc);
-                w_ok = __all_sync(0xffffffffu, w_ok && mbar_wait(&b.s_full[x], sit & 1u, wc));
-            }
-            if (pair) ++tit;
+            if (poller) w_ok = __all_sync(0xffffffffu, mbar_wait(&b.s_full[x], sit & 1u, wc));
             w_ok = unit_bar_and(x, w_ok);
             const uint32_t par = sit & 1u;
             ++sit;
@@ -520,7 +510,6 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, int h, const Bars& 
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&b.p_full[x]);
-            if (pair) mbar_arrive(&b.tok[x ^ 1]);  // the other tile's turn
             ++j;
             return true;
         });
@@ -573,9 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     b.o_done = bars + 8;
     b.o_free = bars + 10;
     b.drain = bars + 12;
-    b.tok = bars + 13;
-    b.kv_full = bars + 15;
-    b.kv_empty = bars + 15 + C::kStages;
+    b.kv_full = bars + 13;
+    b.kv_empty = bars + 13 + C::kStages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
 
@@ -590,8 +578,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&b.o_free[x], 256);
         }
         mbar_init(b.drain, 1);
-        mbar_init(&b.tok[0], 256);
-        mbar_init(&b.tok[1], 256);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&b.kv_full[s], 1);
             mbar_init(&b.kv_empty[s], 1);

@@ -50,15 +50,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // unwinds too.
 struct WaitCtl {
     volatile int* abort_flag;  // shared memory
-    int* err;                  // device error word (may be null)
+    int* err;                  // device error record (may be null): status, set, barrier, where
     uint64_t timeout_ns;
 };
 
 constexpr int kErrTimeout = -5;  // RA_ERR_TIMEOUT
 
-__device__ __forceinline__ void raise_abort(const WaitCtl& w) {
+// Record the abort; the first wait to run out also records which barrier (its
+// shared-memory address) and which thread of which CTA gave up.
+__device__ __forceinline__ void raise_abort(const WaitCtl& w, uint64_t* bar) {
     *w.abort_flag = 1;
-    if (w.err) atomicExch(w.err, kErrTimeout);
+    if (w.err) {
+        atomicExch(w.err, kErrTimeout);
+        if (atomicCAS(w.err + 1, 0, 1) == 0) {
+            w.err[2] = static_cast<int>(smem_u32(bar));
+            w.err[3] = static_cast<int>((blockIdx.x << 10) | threadIdx.x);
+        }
+    }
 }
 
 // Wait until `bar` completes the phase with parity `parity`; false on abort/timeout.
@@ -74,7 +82,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
         if ((i & 63u) == 0u) {
             if (*w.abort_flag) return false;
             if (globaltimer_ns() - t0 > w.timeout_ns) {
-                raise_abort(w);
+                raise_abort(w, bar);
                 return false;
             }
         }
@@ -89,6 +97,38 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         "[%4];" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
+}
+// Same, with an L2 cache policy (from make_policy_*) attached to the loaded lines.
+__device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                                 int y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+// L2 policies: keep lines that many CTAs re-read (K, V); let streamed lines (Q, out) go first.
+__device__ __forceinline__ uint64_t make_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t make_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint4 ld_stream_u4(const uint4* src, uint64_t policy) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(src), "l"(policy));
+    return v;
+}
+__device__ __forceinline__ void st_stream_f4(float4* dst, float4 v, uint64_t policy) {
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "l"(policy)
+                 : "memory");
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

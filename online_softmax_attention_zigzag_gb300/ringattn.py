@@ -28,7 +28,7 @@ RA_ERR_TIMEOUT = -5
 EXPORTS = (
     "ringattn_fwd", "ringattn_fwd_natural", "ringattn_fwd_f32", "ringattn_fwd_hop",
     "ringattn_fwd_hop_f32", "ringattn_merge", "ringattn_permute", "ringattn_rank_work",
-    "ringattn_sync_status", "ringattn_selftest_timeout", "ringattn_strerror",
+    "ringattn_sync_status", "ringattn_selftest_timeout", "ringattn_strerror", "ringattn_last_timeout",
 )
 
 
@@ -64,6 +64,7 @@ def lib() -> ctypes.CDLL:
             "ringattn_rank_work": [_I, _I, _I, _I, _I, _P, _P, _P],
             "ringattn_sync_status": [_P],
             "ringattn_selftest_timeout": [_LL, _P],
+            "ringattn_last_timeout": [_P],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -191,6 +192,13 @@ def rank_work(S: int, c: int, causal: int, layout: int, tile: int = 128):
 def sync_status(stream=None) -> int:
     """ringattn_sync_status: synchronise, return RA_OK or RA_ERR_TIMEOUT / RA_ERR_CUDA."""
     return lib().ringattn_sync_status(ctypes.c_void_p(_stream(stream)))
+
+
+def last_timeout():
+    """ringattn_last_timeout: (barrier smem address, CTA, thread) of the last timeout."""
+    info = (ctypes.c_int * 3)()
+    _check("ringattn_last_timeout", lib().ringattn_last_timeout(info))
+    return tuple(info)
 
 
 def selftest_timeout(timeout_ns: int, stream=None) -> None:
