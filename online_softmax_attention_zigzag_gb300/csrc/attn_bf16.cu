@@ -84,24 +84,30 @@ struct Item {
     int pmax;     // last natural query position in the item
 };
 
+// Items are ordered KV-head-major (all of one KV head's items, then the next), and
+// within a KV head by decreasing causal work (last query tiles first): the K/V tiles in
+// use at any time are then one head's, which stay in L2, and the snake assignment of
+// items to CTAs still deals out decreasing work.
 __device__ __forceinline__ void decode_item(const AttnBf16Params& p, int item, Item& it) {
     const Ring& R = p.ring;
     int t0, t1;
     if (p.pair_mode == kPairHeads) {
-        const int per = R.Hq / 2, gh = R.g / 2;
-        const int pi = item / per, rem = item - pi * per;
+        const int gh = R.g / 2, per_kv = p.n_tiles * gh;
+        it.hk = item / per_kv;
+        const int rem = item - it.hk * per_kv;
+        const int pi = rem / gh;
         t0 = t1 = p.n_tiles - 1 - pi;
-        it.hk = rem / gh;
-        it.hq[0] = it.hk * R.g + 2 * (rem - it.hk * gh);
+        it.hq[0] = it.hk * R.g + 2 * (rem - pi * gh);
         it.hq[1] = it.hq[0] + 1;
     } else if (p.pair_mode == kPairPositions) {
-        const int pi = item / R.Hq, h = item - pi * R.Hq;
+        const int per_h = p.n_tiles / 2;
+        const int h = item / per_h, pi = item - h * per_h;
         t1 = p.n_tiles - 1 - 2 * pi;
         t0 = t1 - 1;
         it.hk = h / R.g;
         it.hq[0] = it.hq[1] = h;
     } else {
-        const int pi = item / R.Hq, h = item - pi * R.Hq;
+        const int h = item / p.n_tiles, pi = item - h * p.n_tiles;
         t0 = t1 = p.n_tiles - 1 - pi;
         it.hk = h / R.g;
         it.hq[0] = h;
@@ -189,6 +195,9 @@ __device__ void load_role(const AttnBf16Params& p, const CUtensorMap* tq, const 
     using C = Cfg<D>;
     uint32_t kv_idx = 0, qit[2] = {0, 0};
     bool ok = true;
+    // K/V tiles are re-read by every query tile of their head group: keep them in L2;
+    // Q tiles are read once: let them go first
+    const uint64_t keep = make_policy_evict_last(), stream = make_policy_evict_first();
     for (int round = 0; ok; ++round) {
         if (round * (int)gridDim.x >= p.n_items) break;
         const int item = item_of_round(round);
@@ -206,7 +215,7 @@ __device__ void load_role(const AttnBf16Params& p, const CUtensorMap* tq, const 
             const int qrow = x ? it.qrow[1] : it.qrow[0];
 #pragma unroll
             for (int bx = 0; bx < C::kBoxes; ++bx)
-                tma_load_2d(sQ + x * C::kTileBytes + bx * C::kBoxBytes, tq, &b.q_full[x], bx * 64, qrow);
+                tma_load_2d_hint(sQ + x * C::kTileBytes + bx * C::kBoxBytes, tq, &b.q_full[x], bx * 64, qrow, stream);
         }
         if (!ok) break;
         for_each_kv_tile(p, it, [&](int row, int) -> bool {
@@ -216,7 +225,8 @@ __device__ void load_role(const AttnBf16Params& p, const CUtensorMap* tq, const 
                 mbar_arrive_expect_tx(&b.kv_full[s], C::kTileBytes);
                 const CUtensorMap* map = kv ? tv : tk;
                 for (int bx = 0; bx < C::kBoxes; ++bx)
-                    tma_load_2d(sKV + s * C::kTileBytes + bx * C::kBoxBytes, map, &b.kv_full[s], bx * 64, row);
+                    tma_load_2d_hint(sKV + s * C::kTileBytes + bx * C::kBoxBytes, map, &b.kv_full[s], bx * 64, row,
+                                     keep);
                 ++kv_idx;
             }
             return true;
@@ -525,6 +535,7 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, int h, const Bars& 
         const float lr_all = lr + xs[((h ^ 1) * 2 + 1) * kTile + row];
         tc_fence_after();
         const float inv = (lr_all > 0.f) ? 1.f / lr_all : 0.f;
+        const uint64_t out_policy = make_policy_evict_first();  // written once, read by the host
 #pragma unroll
         for (int cc = 0; cc < kOHalf; cc += 32) {
             uint32_t o0[32];
@@ -533,8 +544,10 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, int h, const Bars& 
             float4* dst = reinterpret_cast<float4*>(orow + cc);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                dst[i] = make_float4(__uint_as_float(o0[4 * i]) * inv, __uint_as_float(o0[4 * i + 1]) * inv,
-                                     __uint_as_float(o0[4 * i + 2]) * inv, __uint_as_float(o0[4 * i + 3]) * inv);
+                st_stream_f4(dst + i,
+                             make_float4(__uint_as_float(o0[4 * i]) * inv, __uint_as_float(o0[4 * i + 1]) * inv,
+                                         __uint_as_float(o0[4 * i + 2]) * inv, __uint_as_float(o0[4 * i + 3]) * inv),
+                             out_policy);
         }
         tc_fence_before();
         mbar_arrive(&b.o_free[x]);
