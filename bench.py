@@ -199,6 +199,19 @@ def run_reference(args, w, rank):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ multi-GPU helpers
+def max_over_ranks(values, dist, device):
+    """Element-wise max of per-rank timings (the slowest replica sets the step time)."""
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_value(flop_per_step: float, world: int, ms_per_step: float) -> float:
+    """TFLOP/s of all replicas together: every rank runs one step of the workload."""
+    return world * flop_per_step / (ms_per_step * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ GPU arm
 def time_events(fn, reps, stream):
     """Mean device time (ms) of fn() over reps calls, CUDA events on `stream`."""
@@ -398,12 +411,10 @@ def main():
 
     ms_step = ms_total / args.steps
     if dist is not None:
-        t = torch.tensor([ms_step, e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, e2e_ms = t.tolist()
+        ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms], dist, dev)
     flop = w.flops()
-    value = world * flop / (ms_step * 1e-3) / 1e12
-    e2e_value = world * flop / (e2e_ms * 1e-3) / 1e12
+    value = whole_job_value(flop, world, ms_step)
+    e2e_value = whole_job_value(flop, world, e2e_ms)
     bf16_peak, bf16_sust, hbm_peak, peak_src = peaks()
     achieved = flop / (attn_ms * 1e-3) / 1e12
     traffic = traffic_for(w.name)
