@@ -31,7 +31,8 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from online_softmax_attention_zigzag_gb300.configs import WORKLOADS, CAUSAL_GQA_S32K  # noqa: E402
+from online_softmax_attention_zigzag_gb300.configs import (  # noqa: E402
+    CAUSAL_GQA_S32K, CAUSAL_MHA_S4K, WORKLOADS, with_layout)
 from online_softmax_attention_zigzag_gb300.inputs import make_qkv, sample_rows  # noqa: E402
 
 METRIC = "causal-adjusted attention TFLOP/s and % of GB300 bf16 tensor peak, 1 GPU"
@@ -55,6 +56,8 @@ def parse():
                     help="skip the 128k workload and the natural-order step measured beside the headline")
     ap.add_argument("--per-hop-sweep", action="store_true",
                     help="instead of the headline: fused vs per-hop + merge over the workload's kv_block sweep")
+    ap.add_argument("--per-rank", action="store_true",
+                    help="instead of the headline: one launch per virtual rank, both layouts (4k MHA and the workload)")
     return ap.parse_args()
 
 
@@ -283,6 +286,39 @@ def per_hop_sweep(ra, w, dev, stream):
     return out
 
 
+def per_rank(ra, workloads, dev, stream):
+    """One ringattn_fwd_rank launch per virtual rank, contiguous and zigzag: device time,
+    128x128 tiles and visible (query, key) pairs of each rank.  The time of a ring step is
+    the slowest rank's; zigzag evens the ranks out."""
+    out = []
+    for w0 in workloads:
+        for layout in (0, 1):
+            w = with_layout(w0, layout)
+            q_h, k_h, v_h = make_qkv(w)
+            qr, kr, vr = (torch.empty(x.shape, dtype=x.dtype, device=dev) for x in (q_h, k_h, v_h))
+            for src, dst in ((q_h, qr), (k_h, kr), (v_h, vr)):
+                ra.permute(src.to(dev), dst, c=w.c, layout=w.layout, inverse=0)
+            o = torch.empty((w.bhq, w.seq, w.d), dtype=torch.float32, device=dev)
+            l = torch.empty((w.bhq, w.seq), dtype=torch.float32, device=dev)
+            kw = dict(c=w.c, causal=w.causal, layout=w.layout, kv_block=w.kv_block)
+            units, pairs, tiles = ra.rank_work(w.seq, w.c, w.causal, w.layout, 128)
+            ranks = []
+            for r in range(w.c):
+                ms = time_events(lambda: ra.fwd_rank(qr, kr, vr, o, l, rank=r, **kw), 5, stream)
+                fl = 4.0 * w.d * w.bhq * float(pairs[r])
+                ranks.append({"rank": r, "kernel_ms": ms, "units": int(units[r]), "tiles_per_head": int(tiles[r]),
+                              "pairs_per_head": int(pairs[r]), "tflops": fl / (ms * 1e-3) / 1e12})
+            full_ms = time_events(lambda: ra.fwd(qr, kr, vr, o, l, **kw), 5, stream)
+            t = [x["kernel_ms"] for x in ranks]
+            out.append({"workload": w.name, "layout": "zigzag" if layout else "contiguous", "ranks": ranks,
+                        "max_over_min_ms": max(t) / min(t), "sum_ms": sum(t), "all_ranks_one_launch_ms": full_ms})
+            del qr, kr, vr, o, l
+            torch.cuda.empty_cache()
+    if ra.sync_status() != ra.RA_OK:
+        raise SystemExit("device wait timed out")
+    return out
+
+
 def main():
     args = parse()
     w = WORKLOADS[args.workload]
@@ -304,6 +340,13 @@ def main():
         if rank == 0:
             print(json.dumps({"metric": METRIC, "unit": UNIT, "mode": "per-hop sweep", "workload": w.name,
                               "sweep": res}), flush=True)
+        return
+    if args.per_rank:
+        dev = torch.device("cuda", local)
+        res = per_rank(ra, [CAUSAL_MHA_S4K, w], dev, torch.cuda.current_stream(dev))
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "unit": UNIT, "mode": "per-rank launches", "per_rank": res}),
+                  flush=True)
         return
     dist = None
     if world > 1:

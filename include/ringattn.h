@@ -78,6 +78,20 @@ int ringattn_fwd(const void* q, const void* k, const void* v, float* out, float*
                  ra_stream_t stream);
 
 /*
+ * ringattn_fwd_rank -- as ringattn_fwd, restricted to the query rows that virtual rank
+ * `rank` (0 <= rank < c) holds: its local rows of out and lse are written, every other
+ * row is left untouched.  This is one rank's share of the ring ("Interrogating
+ * parallelism, part 5", "What breaks the load balance?": under the causal mask rank i
+ * of a contiguous split does i+1 units of work, every zigzag rank 2c+1), so timing one
+ * call per rank measures the load balance of the two layouts.  Same requirements and
+ * rank-major layout as ringattn_fwd; the rows it writes are bitwise those of
+ * ringattn_fwd.
+ */
+int ringattn_fwd_rank(const void* q, const void* k, const void* v, float* out, float* lse,
+                      int S, int Hq, int Hkv, int d, int c, int causal, int layout, int kv_block,
+                      int rank, ra_stream_t stream);
+
+/*
  * ringattn_fwd_natural -- as ringattn_fwd, but q, k, v, out and lse are in NATURAL
  * sequence order: the zigzag/contiguous chunk map is applied in the kernel's tile
  * addressing, so no permutation pass is needed.  Same result, same requirements.

@@ -140,8 +140,10 @@ int select_hop(ra::Ring* R, int kv_block, int hop, int sub) {
 }
 
 int fwd_bf16(const void* q, const void* k, const void* v, float* out, float* lse, int S, int Hq, int Hkv, int d,
-             int c, int causal, int layout, int kv_block, int natural, int hop, int sub, cudaStream_t stream) {
+             int c, int causal, int layout, int kv_block, int natural, int hop, int sub, int rank,
+             cudaStream_t stream) {
     if (!q || !k || !v || !out || !lse) return RA_ERR_INVALID_ARG;
+    if (rank < -1 || rank >= c) return RA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
         return RA_ERR_INVALID_ARG;
     ra::Ring R;
@@ -157,7 +159,8 @@ int fwd_bf16(const void* q, const void* k, const void* v, float* out, float* lse
     ra::AttnBf16Params p;
     p.ring = R;
     p.natural = natural;
-    p.n_tiles = S / 128;
+    p.rank_sel = rank;
+    p.n_tiles = (rank >= 0 ? R.n_r : S) / 128;
     const int tiles_per_chunk = R.m / 128;
     if (R.g % 2 == 0) {
         p.pair_mode = ra::kPairHeads;
@@ -211,13 +214,20 @@ extern "C" {
 
 int ringattn_fwd(const void* q, const void* k, const void* v, float* out, float* lse, int S, int Hq, int Hkv, int d,
                  int c, int causal, int layout, int kv_block, ra_stream_t stream) {
-    return fwd_bf16(q, k, v, out, lse, S, Hq, Hkv, d, c, causal, layout, kv_block, 0, -1, 0,
+    return fwd_bf16(q, k, v, out, lse, S, Hq, Hkv, d, c, causal, layout, kv_block, 0, -1, 0, -1,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ringattn_fwd_rank(const void* q, const void* k, const void* v, float* out, float* lse, int S, int Hq, int Hkv,
+                      int d, int c, int causal, int layout, int kv_block, int rank, ra_stream_t stream) {
+    if (rank < 0) return RA_ERR_INVALID_ARG;
+    return fwd_bf16(q, k, v, out, lse, S, Hq, Hkv, d, c, causal, layout, kv_block, 0, -1, 0, rank,
                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 int ringattn_fwd_natural(const void* q, const void* k, const void* v, float* out, float* lse, int S, int Hq,
                          int Hkv, int d, int c, int causal, int layout, int kv_block, ra_stream_t stream) {
-    return fwd_bf16(q, k, v, out, lse, S, Hq, Hkv, d, c, causal, layout, kv_block, 1, -1, 0,
+    return fwd_bf16(q, k, v, out, lse, S, Hq, Hkv, d, c, causal, layout, kv_block, 1, -1, 0, -1,
                     reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -225,7 +235,7 @@ int ringattn_fwd_hop(const void* q, const void* k, const void* v, float* o_part,
                      int Hkv, int d, int c, int causal, int layout, int kv_block, int hop, int sub,
                      ra_stream_t stream) {
     if (hop < 0) return RA_ERR_INVALID_ARG;
-    return fwd_bf16(q, k, v, o_part, lse_part, S, Hq, Hkv, d, c, causal, layout, kv_block, 0, hop, sub,
+    return fwd_bf16(q, k, v, o_part, lse_part, S, Hq, Hkv, d, c, causal, layout, kv_block, 0, hop, sub, -1,
                     reinterpret_cast<cudaStream_t>(stream));
 }
 

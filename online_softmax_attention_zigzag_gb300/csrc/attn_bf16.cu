@@ -84,6 +84,15 @@ struct Item {
     int pmax;     // last natural query position in the item
 };
 
+// Natural tile index of local tile t of rank r (local rows: chunk r, then for zigzag
+// chunk 2c-1-r; "What breaks the load balance?").
+__device__ __forceinline__ int rank_tile(const Ring& R, int r, int t) {
+    const int x = t * kTile;
+    const int slot = x / R.m;
+    const int k = (slot == 0) ? r : 2 * R.c - 1 - r;
+    return (k * R.m + (x - slot * R.m)) / kTile;
+}
+
 // Items are ordered KV-head-major (all of one KV head's items, then the next), and
 // within a KV head by decreasing causal work (last query tiles first): the K/V tiles in
 // use at any time are then one head's, which stay in L2, and the snake assignment of
@@ -112,6 +121,10 @@ __device__ __forceinline__ void decode_item(const AttnBf16Params& p, int item, I
         it.hk = h / R.g;
         it.hq[0] = h;
         it.hq[1] = -1;
+    }
+    if (p.rank_sel >= 0) {  // tile indices count one rank's local tiles: map them to natural tiles
+        t0 = rank_tile(R, p.rank_sel, t0);
+        t1 = rank_tile(R, p.rank_sel, t1);
     }
     it.pos[0] = t0 * kTile;
     it.pos[1] = t1 * kTile;

@@ -30,7 +30,8 @@ struct AttnBf16Params {
     Ring ring;
     int natural;    // 1: tensors in natural order (chunk map folded into addressing)
     int pair_mode;
-    int n_tiles;    // 128-row query tiles per head (S / 128)
+    int rank_sel;   // -1: every rank's query rows; r >= 0: only virtual rank r's rows
+    int n_tiles;    // 128-row query tiles per head (S / 128, or S / (128 c) for one rank)
     int n_items;
     float* out;
     float* lse;

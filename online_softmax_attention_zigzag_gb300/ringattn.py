@@ -29,6 +29,7 @@ EXPORTS = (
     "ringattn_fwd", "ringattn_fwd_natural", "ringattn_fwd_f32", "ringattn_fwd_hop",
     "ringattn_fwd_hop_f32", "ringattn_merge", "ringattn_permute", "ringattn_rank_work",
     "ringattn_sync_status", "ringattn_selftest_timeout", "ringattn_strerror", "ringattn_last_timeout",
+    "ringattn_fwd_rank",
 )
 
 
@@ -56,6 +57,7 @@ def lib() -> ctypes.CDLL:
         sig = {
             "ringattn_fwd": _ATTN + [_P],
             "ringattn_fwd_natural": _ATTN + [_P],
+            "ringattn_fwd_rank": _ATTN + [_I, _P],
             "ringattn_fwd_f32": _ATTN + [_P],
             "ringattn_fwd_hop": _ATTN + [_I, _I, _P],
             "ringattn_fwd_hop_f32": _ATTN + [_I, _I, _P],
@@ -125,6 +127,13 @@ def fwd(q, k, v, out, lse, *, c, causal, layout, kv_block, stream=None) -> None:
     ptrs, S, Hq, Hkv, d = _attn_args(q, k, v, out, lse, torch.bfloat16)
     _check("ringattn_fwd", lib().ringattn_fwd(*ptrs, S, Hq, Hkv, d, c, int(causal), layout, kv_block,
                                               ctypes.c_void_p(_stream(stream))))
+
+
+def fwd_rank(q, k, v, out, lse, *, c, causal, layout, kv_block, rank, stream=None) -> None:
+    """ringattn_fwd_rank: as :func:`fwd`, writing only the rows virtual rank ``rank`` holds."""
+    ptrs, S, Hq, Hkv, d = _attn_args(q, k, v, out, lse, torch.bfloat16)
+    _check("ringattn_fwd_rank", lib().ringattn_fwd_rank(*ptrs, S, Hq, Hkv, d, c, int(causal), layout, kv_block,
+                                                        int(rank), _stream(stream)))
 
 
 def fwd_natural(q, k, v, out, lse, *, c, causal, layout, kv_block, stream=None) -> None:

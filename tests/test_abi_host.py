@@ -89,6 +89,14 @@ def test_hop_rejects_bad_hop_and_sub(ra):
     assert L.ringattn_fwd_hop_f32(*base, 0, -1, S0) == -1
 
 
+def test_rank_rejects_bad_rank(ra):
+    L = ra.lib()
+    base = [P, P, P, P2, P2, 4096, 8, 8, 64, 4, 1, 1, 512]
+    assert L.ringattn_fwd_rank(*base, 4, S0) == -1          # rank >= c
+    assert L.ringattn_fwd_rank(*base, -1, S0) == -1
+    assert L.ringattn_fwd_rank(P, P, P, P2, P2, 4096, 8, 3, 64, 4, 1, 1, 512, 0, S0) == -1  # geometry too
+
+
 def test_f32_rejects(ra):
     L = ra.lib()
     assert L.ringattn_fwd_f32(P, P, P, P2, P2, 12, 1, 1, 129, 3, 0, 0, 4, S0) == -2   # d > 128

@@ -229,6 +229,40 @@ def test_bf16_natural_matches_rank_major(ra):
         assert torch.equal(on.cpu(), o) and torch.equal(ln.cpu(), l)
 
 
+@pytest.mark.parametrize("case", [
+    # Hq, Hkv, S, d, c, layout, causal
+    (8, 8, 4096, 64, 4, 0, 1),     # the 4096-token MHA workload, contiguous: position pairs
+    (8, 8, 4096, 64, 4, 1, 1),     # and zigzag
+    (6, 2, 1536, 128, 3, 1, 1),    # g = 3: single tiles
+    (8, 2, 2048, 128, 4, 1, 0),    # head pairs, non-causal
+])
+def test_bf16_rank_restricted_matches_full(ra, case):
+    """ringattn_fwd_rank writes exactly one rank's rows, bitwise equal to ringattn_fwd's."""
+    Hq, Hkv, S, d, c, layout, causal = case
+    n_r = S // c
+    q = _randn((Hq, S, d), 61, torch.bfloat16)
+    k = _randn((Hkv, S, d), 62, torch.bfloat16)
+    v = _randn((Hkv, S, d), 63, torch.bfloat16)
+    qd, kd, vd = (rank_major(x, S, c, layout).to(dev()) for x in (q, k, v))
+    kvb = S // (c * (2 if layout else 1))
+    of = torch.empty((Hq, S, d), dtype=torch.float32, device=dev())
+    lf = torch.empty((Hq, S), dtype=torch.float32, device=dev())
+    ra.fwd(qd, kd, vd, of, lf, c=c, causal=causal, layout=layout, kv_block=kvb)
+    o = torch.full((Hq, S, d), float("nan"), dtype=torch.float32, device=dev())
+    l = torch.full((Hq, S), float("nan"), dtype=torch.float32, device=dev())
+    for r in range(c):
+        ra.fwd_rank(qd, kd, vd, o, l, c=c, causal=causal, layout=layout, kv_block=kvb, rank=r)
+        torch.cuda.synchronize()
+        oc, lc = o.cpu(), l.cpu()
+        done = slice(0, (r + 1) * n_r)
+        assert torch.equal(oc[:, done], of.cpu()[:, done]) and torch.equal(lc[:, done], lf.cpu()[:, done])
+        assert torch.isnan(oc[:, (r + 1) * n_r:]).all() and torch.isnan(lc[:, (r + 1) * n_r:]).all()
+    ro, rl = oatt.full_attention(f64(q), f64(k), f64(v), bool(causal))
+    assert max_err(natural(o.cpu(), S, c, layout), ro) <= TOL_BF16_OUT
+    assert max_err(natural(l.cpu(), S, c, layout), rl) <= TOL_BF16_LSE
+    _status_ok(ra)
+
+
 @pytest.mark.parametrize("case", [(4, 2, 1024, 64, 2, 1, 1, 128), (2, 2, 1024, 128, 4, 0, 1, 128),
                                   (2, 1, 512, 64, 2, 0, 0, 256)])
 def test_bf16_hop_partials_and_merge(ra, case):
