@@ -30,6 +30,7 @@ class Workload:
     outlier_frac: float = 0.0
     outlier_factor: float = 1.0
     kv_sweep: tuple = field(default_factory=tuple)
+    doc_len: tuple = field(default_factory=tuple)   # (lo, hi): packed documents, all-gathered KV
 
     @property
     def bhq(self) -> int:
@@ -69,8 +70,19 @@ PROFILE_GQA_S16K = Workload("causal_gqa_S16384_h64x8_d128_c8_zigzag", seq=16384,
                             d=128, c=8, causal=1, layout=1, kv_block=1024,
                             q_scale=1.0 / math.sqrt(128.0))
 
+# All-gathered K/V with a document mask ("Interrogating parallelism, part 5", section "Why did
+# Llama 3 not use a ring?"): documents of 32..8192 tokens packed into one sequence, each
+# token attends causally within its own document; zigzag query chunks as in the ring.
+DOCMASK_GQA_S32K = Workload("docmask_gqa_S32768_h64x8_d128_c8_zigzag", seq=32768, hq=64, hkv=8,
+                            d=128, c=8, causal=1, layout=1, kv_block=2048,
+                            q_scale=1.0 / math.sqrt(128.0), doc_len=(32, 8192))
+# Small version for element-by-element checks: documents from 1 token up.
+DOCMASK_GQA_S4K = Workload("docmask_gqa_S4096_h8x2_d128_c4_zigzag", seq=4096, hq=8, hkv=2, d=128,
+                           c=4, causal=1, layout=1, kv_block=512, doc_len=(1, 2048))
+
 WORKLOADS = {w.name: w for w in (TINY_F32, CAUSAL_MHA_S4K, CAUSAL_GQA_S32K, CAUSAL_GQA_S128K,
-                                 NONCAUSAL_MHA_B2_S64K, PROFILE_GQA_S16K)}
+                                 NONCAUSAL_MHA_B2_S64K, PROFILE_GQA_S16K, DOCMASK_GQA_S32K,
+                                 DOCMASK_GQA_S4K)}
 
 
 def with_layout(w: Workload, layout: int) -> Workload:

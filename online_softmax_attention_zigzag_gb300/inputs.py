@@ -11,7 +11,7 @@ N(0, 1) without a seed; here every draw comes from a torch CPU generator with
 a fixed seed so that results repeat:
 
     Q: seed 0, K: seed 1, V: seed 2, Q outlier mask: seed 3, K outlier mask:
-    seed 4, sampled query rows: seed 1234.
+    seed 4, document lengths: seed 5, sampled query rows: seed 1234.
 
 Tensors are head-major and in natural sequence order, ``[B*H, S, d]``.
 """
@@ -21,6 +21,7 @@ import torch
 
 SEED_Q, SEED_K, SEED_V = 0, 1, 2
 SEED_Q_MASK, SEED_K_MASK = 3, 4
+SEED_DOCS = 5
 SEED_ROWS = 1234
 
 
@@ -63,6 +64,27 @@ def make_qkv(w) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
         q = q * w.q_scale
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     return q.to(dt).contiguous(), k.to(dt).contiguous(), v.to(dt).contiguous()
+
+
+def doc_ids(seq: int, lo: int, hi: int, seed: int = SEED_DOCS) -> torch.Tensor:
+    """Document id of every position of a packed sequence, int32 [seq], non-decreasing.
+
+    Documents are laid end to end; their lengths are drawn log-uniformly from
+    [lo, hi] (many short documents, a few long ones) until ``seq`` tokens are
+    filled, and the last one is cut to fit.  Ids count 0, 1, 2, ... in order.
+    """
+    g = _gen(seed)
+    ids = torch.empty(seq, dtype=torch.int32)
+    pos, doc = 0, 0
+    llo, lhi = float(torch.log(torch.tensor(float(lo)))), float(torch.log(torch.tensor(float(hi) + 1.0)))
+    while pos < seq:
+        u = float(torch.rand((), generator=g))
+        n = int(torch.exp(torch.tensor(llo + u * (lhi - llo))))
+        n = max(lo, min(hi, n, seq - pos))
+        ids[pos:pos + n] = doc
+        pos += n
+        doc += 1
+    return ids
 
 
 def sample_rows(bh: int, seq: int, n: int, seed: int = SEED_ROWS) -> tuple[torch.Tensor, torch.Tensor]:

@@ -23,6 +23,9 @@ numpy).  Each function names the passage it follows:
   partials over disjoint key sets.
 * :mod:`oracle.work` -- per-rank causal work in chunk units, exact pairs and
   128x128 tiles.
+* :mod:`oracle.docmask` -- attention over all-gathered keys and values under a
+  document mask, causal inside each document ("Interrogating parallelism,
+  part 5", section "Why did Llama 3 not use a ring?").
 
 Every function is pinned by ``tests/test_oracle_*.py`` against closed forms,
 brute force, library routines it does not call, or values the pages print.

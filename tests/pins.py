@@ -248,3 +248,95 @@ def pin_merge(merge_fn, full_fn):
     assert np.abs(oe - oa).max() == 0.0 and np.abs(le - la).max() == 0.0, "-inf partial not neutral"
     oz, lz = merge_fn(np.zeros_like(oa), ninf, np.zeros_like(oa), ninf)
     assert np.all(oz == 0.0) and np.all(np.isneginf(lz)), "two empty partials"
+
+
+# --------------------------------------------------------------------------- document mask
+
+def _segments(doc):
+    """[start, end) of every run of equal ids."""
+    doc = list(doc)
+    segs, a = [], 0
+    for i in range(1, len(doc) + 1):
+        if i == len(doc) or doc[i] != doc[a]:
+            segs.append((a, i))
+            a = i
+    return segs
+
+
+def brute_force_doc(q, k, v, doc):
+    """Pure-Python loops: keys j <= i of i's document, math.exp only; tiny inputs."""
+    Hq, S, d = q.shape
+    g = Hq // k.shape[0]
+    out = np.zeros((Hq, S, d))
+    lse = np.zeros((Hq, S))
+    for h in range(Hq):
+        kh = h // g
+        for i in range(S):
+            keys = [j for j in range(i + 1) if doc[j] == doc[i]]
+            sc = [sum(float(q[h][i][t]) * float(k[kh][j][t]) for t in range(d)) for j in keys]
+            M = max(sc)
+            w = [math.exp(s - M) for s in sc]
+            L = sum(w)
+            for t in range(d):
+                out[h][i][t] = sum(w[n] * float(v[kh][j][t]) for n, j in enumerate(keys)) / L
+            lse[h][i] = M + math.log(L)
+    return out, lse
+
+
+def pin_doc_brute(doc_fn):
+    for (Hq, Hkv, d, doc, seed) in ((2, 1, 3, [0, 0, 0, 1, 1, 2, 3, 3, 3, 3], 70),
+                                   (4, 2, 4, [5, 5, 6, 7, 7, 7, 7, 9], 71),
+                                   (1, 1, 2, [0, 1, 2, 3, 4], 72)):
+        S = len(doc)
+        q, k, v = rand((Hq, S, d), seed), rand((Hkv, S, d), seed + 100), rand((Hkv, S, d), seed + 200)
+        o, l = doc_fn(q, k, v, np.array(doc))
+        ob, lb = brute_force_doc(q, k, v, doc)
+        assert np.abs(o - ob).max() < 1e-12, "document-masked out differs from brute force"
+        assert np.abs(l - lb).max() < 1e-12, "document-masked lse differs from brute force"
+
+
+def pin_doc_segments_vs_torch(doc_fn):
+    """Each document on its own is plain causal attention (torch SDPA and logsumexp on the
+    document's slice): nothing leaks across a boundary and the diagonal is kept."""
+    rng = np.random.default_rng(73)
+    lens = [1, 7, 2, 33, 1, 1, 20, 64, 3, 18]
+    doc = np.repeat(np.arange(len(lens)) * 3 + 2, lens)        # ids need only be equal within a document
+    S = len(doc)
+    Hq, Hkv, d = 4, 2, 8
+    q, k, v = rng.standard_normal((Hq, S, d)), rng.standard_normal((Hkv, S, d)), rng.standard_normal((Hkv, S, d))
+    o, l = doc_fn(q, k, v, doc)
+    tk = torch.from_numpy(k).repeat_interleave(Hq // Hkv, dim=0)
+    tv = torch.from_numpy(v).repeat_interleave(Hq // Hkv, dim=0)
+    tq = torch.from_numpy(q)
+    for a, b in _segments(doc):
+        n = b - a
+        to = torch.nn.functional.scaled_dot_product_attention(
+            tq[None, :, a:b], tk[None, :, a:b], tv[None, :, a:b], is_causal=True, scale=1.0)[0]
+        sc = (tq[:, a:b] @ tk[:, a:b].transpose(-1, -2)).masked_fill(
+            torch.ones(n, n, dtype=torch.bool).triu(1), float("-inf"))
+        tl = torch.logsumexp(sc, dim=-1)
+        assert np.abs(o[:, a:b] - to.numpy()).max() < 1e-10, "document slice differs from torch SDPA"
+        assert np.abs(l[:, a:b] - tl.numpy()).max() < 1e-10, "document slice lse differs from logsumexp"
+
+
+def pin_doc_closed_forms(doc_fn):
+    S, d = 12, 5
+    q, k, v = rand((1, S, d), 74), rand((1, S, d), 75), rand((1, S, d), 76)
+    # every token its own document: it sees only itself
+    o, l = doc_fn(q, k, v, np.arange(S))
+    assert np.abs(o[0] - v[0]).max() < 1e-12, "single-token document is not v_i"
+    assert np.abs(l[0] - np.einsum("sd,sd->s", q[0], k[0])).max() < 1e-12, "single-token lse is not q_i.k_i"
+    # q = 0: the mean of V over [start of i's document, i], lse = ln of that count
+    doc = np.array([0, 0, 0, 0, 1, 1, 2, 2, 2, 2, 2, 3])
+    o, l = doc_fn(np.zeros((1, S, d)), k, v, doc)
+    for a, b in _segments(doc):
+        for i in range(a, b):
+            assert np.abs(o[0, i] - v[0, a:i + 1].mean(axis=0)).max() < 1e-12, "q=0 is not the in-document mean"
+            assert abs(l[0, i] - math.log(i - a + 1)) < 1e-12, "q=0 lse is not ln(i - start + 1)"
+
+
+def pin_doc_pairs(pairs_fn):
+    assert pairs_fn(np.arange(9)) == 9
+    assert pairs_fn(np.zeros(10, dtype=np.int64)) == 55
+    lens = [3, 1, 8, 2]
+    assert pairs_fn(np.repeat(np.arange(4), lens)) == sum(n * (n + 1) // 2 for n in lens)

@@ -150,3 +150,58 @@ def test_merge_mutants_caught():
     for fn in (unnormalised, lse_sum):
         with pytest.raises(AssertionError):
             pins.pin_merge(fn, attention.full_attention)
+
+
+# ---------------------------------------------------------------- document-mask mutants
+
+def _doc(q, k, v, doc, *, leak_earlier=False, no_diag=False, no_causal=False, gqa_mod=False, shift=False):
+    q = np.asarray(q, float); k = np.asarray(k, float); v = np.asarray(v, float)
+    doc = np.asarray(doc)
+    Hq, S, d = q.shape
+    Hkv = k.shape[0]
+    out = np.empty((Hq, S, v.shape[2])); lse = np.empty((Hq, S))
+    i = np.arange(S)[:, None]
+    j = np.arange(S)[None, :]
+    di = doc[np.maximum(np.arange(S) - 1, 0)] if shift else doc
+    same = (doc[None, :] <= di[:, None]) if leak_earlier else (doc[None, :] == di[:, None])
+    causal = (j < i) if no_diag else (j <= i)
+    vis = same if no_causal else (same & causal)
+    for h in range(Hq):
+        kh = h % Hkv if gqa_mod else h // (Hq // Hkv)
+        s = np.where(vis, q[h] @ k[kh].T, -np.inf)
+        M = s.max(1)
+        e = np.exp(s - M[:, None])
+        L = e.sum(1)
+        out[h] = (e @ v[kh]) / L[:, None]
+        lse[h] = M + np.log(L)
+    return out, lse
+
+
+DOC_MUTANTS = {
+    "attends_earlier_documents": dict(leak_earlier=True),
+    "drops_the_diagonal": dict(no_diag=True),
+    "not_causal_inside_a_document": dict(no_causal=True),
+    "gqa_head_map_mod": dict(gqa_mod=True),
+    "document_of_previous_token": dict(shift=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(DOC_MUTANTS))
+def test_doc_mutant_caught(name):
+    kw = DOC_MUTANTS[name]
+    fn = lambda q, k, v, doc: _doc(q, k, v, doc, **kw)  # noqa: E731
+    failures = 0
+    for pin in (pins.pin_doc_brute, pins.pin_doc_segments_vs_torch, pins.pin_doc_closed_forms):
+        try:
+            with np.errstate(invalid="ignore", divide="ignore"):
+                pin(fn)
+        except AssertionError:
+            failures += 1
+    assert failures > 0, f"mutant {name} passed every pin"
+
+
+def test_doc_copy_passes():
+    fn = lambda q, k, v, doc: _doc(q, k, v, doc)  # noqa: E731
+    pins.pin_doc_brute(fn)
+    pins.pin_doc_segments_vs_torch(fn)
+    pins.pin_doc_closed_forms(fn)

@@ -2,7 +2,7 @@
 import numpy as np
 import pytest
 
-from oracle import attention, layout, merge, ring, work
+from oracle import attention, docmask, layout, merge, ring, work
 from tests import pins
 
 
@@ -80,3 +80,30 @@ def test_ring_schedule_covers_each_key_once():
             # hop 0 is the rank's own block (no communication on the first round)
             own = layout.rank_positions(S, c, lay, r)
             assert np.array_equal(np.concatenate(msgs[: len(own) // kvb]), own)
+
+
+def test_doc_mask_vs_brute_force():
+    pins.pin_doc_brute(docmask.doc_attention)
+
+
+def test_doc_mask_each_document_is_causal_attention():
+    pins.pin_doc_segments_vs_torch(docmask.doc_attention)
+
+
+def test_doc_mask_closed_forms():
+    pins.pin_doc_closed_forms(docmask.doc_attention)
+
+
+def test_doc_mask_rows_match_whole():
+    rng = np.random.default_rng(77)
+    Hq, Hkv, S, d = 4, 2, 90, 6
+    q, k, v = rng.standard_normal((Hq, S, d)), rng.standard_normal((Hkv, S, d)), rng.standard_normal((Hkv, S, d))
+    doc = np.repeat(np.arange(6), [10, 1, 30, 4, 40, 5])
+    o, l = docmask.doc_attention(q, k, v, doc)
+    heads, posn = np.array([0, 1, 3, 3, 2]), np.array([0, 10, 11, 89, 45])
+    ro, rl = docmask.doc_attention_rows(q, k, v, doc, heads, posn, batch_rows=2)
+    assert np.abs(ro - o[heads, posn]).max() < 1e-12 and np.abs(rl - l[heads, posn]).max() < 1e-12
+
+
+def test_doc_pairs():
+    pins.pin_doc_pairs(docmask.doc_pairs)
