@@ -33,7 +33,7 @@ import torch  # noqa: E402
 
 from online_softmax_attention_zigzag_gb300.configs import (  # noqa: E402
     CAUSAL_GQA_S32K, CAUSAL_MHA_S4K, WORKLOADS, with_layout)
-from online_softmax_attention_zigzag_gb300.inputs import make_qkv, sample_rows  # noqa: E402
+from online_softmax_attention_zigzag_gb300.inputs import doc_ids, make_qkv, sample_rows  # noqa: E402
 
 METRIC = "causal-adjusted attention TFLOP/s and % of GB300 bf16 tensor peak, 1 GPU"
 UNIT = "TFLOP/s"
@@ -56,6 +56,8 @@ def parse():
                     help="skip the 128k workload and the natural-order step measured beside the headline")
     ap.add_argument("--per-hop-sweep", action="store_true",
                     help="instead of the headline: fused vs per-hop + merge over the workload's kv_block sweep")
+    ap.add_argument("--attention-only", action="store_true",
+                    help="instead of the headline: the attention kernel alone on the workload, --steps launches")
     ap.add_argument("--per-rank", action="store_true",
                     help="instead of the headline: one launch per virtual rank, both layouts (4k MHA and the workload)")
     return ap.parse_args()
@@ -229,8 +231,16 @@ def time_events(fn, reps, stream):
     return a.elapsed_time(b) / reps
 
 
+def doc_flops(w, doc) -> float:
+    """Attention FLOP of the visible pairs under the document mask: 4*d per pair, per head;
+    a document of L tokens holds L(L+1)/2 causal pairs."""
+    lens = torch.bincount(doc.to(torch.int64)).to(torch.float64)
+    return 4.0 * w.d * w.bhq * float((lens * (lens + 1) / 2).sum())
+
+
 def attention_only(ra, w, dev, stream, reps, peak):
-    """Fused kernel on rank-major device inputs of workload w: TFLOP/s and fraction of peak."""
+    """Fused kernel on rank-major device inputs of workload w: TFLOP/s and fraction of peak.
+    A workload with packed documents runs the document-masked all-gather kernel."""
     q_h, k_h, v_h = make_qkv(w)
     q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
     del q_h, k_h, v_h
@@ -240,13 +250,24 @@ def attention_only(ra, w, dev, stream, reps, peak):
     del q, k, v
     o = torch.empty((w.bhq, w.seq, w.d), dtype=torch.float32, device=dev)
     l = torch.empty((w.bhq, w.seq), dtype=torch.float32, device=dev)
-    kw = dict(c=w.c, causal=w.causal, layout=w.layout, kv_block=w.kv_block)
-    ms = time_events(lambda: ra.fwd(qr, kr, vr, o, l, **kw), reps, stream)
+    if w.doc_len:
+        doc = doc_ids(w.seq, *w.doc_len)
+        doc_d = doc.to(dev)
+        ds = torch.empty_like(doc_d)
+        ms = time_events(lambda: ra.fwd_docmask(qr, kr, vr, o, l, doc_d, ds, c=w.c, layout=w.layout), reps, stream)
+        flop = doc_flops(w, doc)
+        what = {"kernel": "doc_start_kernel + attn_bf16_kernel<%d, true>" % w.d,
+                "documents": int(doc[-1]) + 1, "flop": "visible pairs only (causal inside each document)"}
+    else:
+        kw = dict(c=w.c, causal=w.causal, layout=w.layout, kv_block=w.kv_block)
+        ms = time_events(lambda: ra.fwd(qr, kr, vr, o, l, **kw), reps, stream)
+        flop = w.flops()
+        what = {"kernel": "attn_bf16_kernel<%d, false>" % w.d}
     if ra.sync_status() != ra.RA_OK:
         raise SystemExit("device wait timed out")
-    tf = w.flops() / (ms * 1e-3) / 1e12
+    tf = flop / (ms * 1e-3) / 1e12
     return {"workload": w.name, "kernel_ms": ms, "achieved": tf, "unit": "TFLOP/s", "peak": peak,
-            "frac": tf / peak, "launches": reps + 1}
+            "frac": tf / peak, "launches": reps + 1, **what}
 
 
 def per_hop_sweep(ra, w, dev, stream):
@@ -341,6 +362,14 @@ def main():
             print(json.dumps({"metric": METRIC, "unit": UNIT, "mode": "per-hop sweep", "workload": w.name,
                               "sweep": res}), flush=True)
         return
+    if args.attention_only:
+        dev = torch.device("cuda", local)
+        res = attention_only(ra, w, dev, torch.cuda.current_stream(dev), max(1, args.steps), peaks()[0])
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "unit": UNIT, "mode": "attention kernel only", **res}), flush=True)
+        return
+    if w.doc_len:
+        raise SystemExit("packed-document workloads are timed with --attention-only")
     if args.per_rank:
         dev = torch.device("cuda", local)
         res = per_rank(ra, [CAUSAL_MHA_S4K, w], dev, torch.cuda.current_stream(dev))
@@ -468,8 +497,8 @@ def main():
     if not args.no_extra and w.name == CAUSAL_GQA_S32K.name:
         del qr, kr, vr, o_r, l_r
         torch.cuda.empty_cache()
-        extra = attention_only(ra, WORKLOADS["causal_gqa_S131072_h32x8_d128_c16_zigzag"], dev, stream, 5,
-                               peaks()[0])
+        extra = [attention_only(ra, WORKLOADS[name], dev, stream, 5, peaks()[0])
+                 for name in ("causal_gqa_S131072_h32x8_d128_c16_zigzag", "docmask_gqa_S32768_h64x8_d128_c8_zigzag")]
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -489,7 +518,7 @@ def main():
                        "replicas": "one independent replica per GPU"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
                          "frac": achieved / bf16_peak, "traffic": traffic,
-                         "kernel": "attn_bf16_kernel<%d>" % w.d, "kernel_ms": attn_ms,
+                         "kernel": "attn_bf16_kernel<%d, false>" % w.d, "kernel_ms": attn_ms,
                          "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
                          "frac_of_sustained": (achieved / bf16_sust) if bf16_sust else None},
             "natural_step": {"ms_per_step": nat_ms, "value": flop / (nat_ms * 1e-3) / 1e12, "unit": UNIT,

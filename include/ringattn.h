@@ -42,7 +42,7 @@
  *    CUDA runtime call or launch failed.  Device-side waits are bounded; one that
  *    runs out records RA_ERR_TIMEOUT, read with ringattn_sync_status.  No exception
  *    crosses the ABI and there is no CPU fallback.
- *  - The library allocates no device memory per call.
+ *  - The library allocates no device memory per call; scratch it needs is passed in.
  */
 #ifndef RINGATTN_H
 #define RINGATTN_H
@@ -90,6 +90,34 @@ int ringattn_fwd(const void* q, const void* k, const void* v, float* out, float*
 int ringattn_fwd_rank(const void* q, const void* k, const void* v, float* out, float* lse,
                       int S, int Hq, int Hkv, int d, int c, int causal, int layout, int kv_block,
                       int rank, ra_stream_t stream);
+
+/*
+ * ringattn_fwd_docmask -- all-gathered K/V under a document mask, bf16 in, fp32 out
+ * ("Interrogating parallelism, part 5", section "Why did Llama 3 not use a ring?": the
+ * keys and values are all-gathered first, then each rank computes attention for its
+ * local query chunks; this carries the document mask that keeps attention inside each
+ * document of a packed sequence).  For every rank's query rows:
+ *     out[h,i,:] = sum_j softmax_j(q_i . k_j) v_j   over j <= i with doc_id[j] == doc_id[i]
+ * (causal inside a document), lse as for ringattn_fwd.  Keys are visited in natural
+ * order from the first key of the earliest document a query tile touches; key tiles
+ * outside every row's document are skipped.
+ * q, k, v, out, lse: as ringattn_fwd (rank-major for c and layout; one message per
+ * chunk, no kv_block).
+ * doc_id:    [S] int32 device, NATURAL order, the document of every position; ids must
+ *            not decrease along the sequence (documents packed one after another).  One
+ *            packing is shared by every head; batch entries with different packings
+ *            are separate calls.  Ids that decrease give an unspecified result (never
+ *            an out-of-bounds access).
+ * doc_start: [S] int32 device scratch owned by the caller, distinct from doc_id; the
+ *            call overwrites it with the first position of every position's document
+ *            (computed from doc_id on `stream` before the attention kernel runs).
+ * Requirements as ringattn_fwd otherwise: d in {64, 128}, S/(c*(layout?2:1)) a
+ * multiple of 128, Hq % Hkv == 0, 16-byte aligned q, k, v, out, lse; 4-byte aligned
+ * doc_id and doc_start.
+ */
+int ringattn_fwd_docmask(const void* q, const void* k, const void* v, float* out, float* lse,
+                         const int* doc_id, int* doc_start, int S, int Hq, int Hkv, int d, int c,
+                         int layout, ra_stream_t stream);
 
 /*
  * ringattn_fwd_natural -- as ringattn_fwd, but q, k, v, out and lse are in NATURAL

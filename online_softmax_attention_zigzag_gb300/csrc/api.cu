@@ -141,7 +141,7 @@ int select_hop(ra::Ring* R, int kv_block, int hop, int sub) {
 
 int fwd_bf16(const void* q, const void* k, const void* v, float* out, float* lse, int S, int Hq, int Hkv, int d,
              int c, int causal, int layout, int kv_block, int natural, int hop, int sub, int rank,
-             cudaStream_t stream) {
+             cudaStream_t stream, const int* doc_id = nullptr, int* doc_start = nullptr) {
     if (!q || !k || !v || !out || !lse) return RA_ERR_INVALID_ARG;
     if (rank < -1 || rank >= c) return RA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
@@ -174,6 +174,7 @@ int fwd_bf16(const void* q, const void* k, const void* v, float* out, float* lse
     }
     p.out = out;
     p.lse = lse;
+    p.doc_start = doc_start;
     p.err = dev->err;
     p.timeout_ns = wait_timeout_ns();
 
@@ -183,6 +184,7 @@ int fwd_bf16(const void* q, const void* k, const void* v, float* out, float* lse
         encode_bf16_map(&tv, v, static_cast<long long>(Hkv) * S, d) != RA_OK)
         return RA_ERR_CUDA;
     const int grid = p.n_items < dev->sms ? p.n_items : dev->sms;
+    if (doc_id && ra::launch_doc_start(doc_id, doc_start, S, stream) != 0) return RA_ERR_CUDA;
     return ra::launch_attn_bf16(p, tq, tk, tv, grid, stream);
 }
 
@@ -223,6 +225,20 @@ int ringattn_fwd_rank(const void* q, const void* k, const void* v, float* out, f
     if (rank < 0) return RA_ERR_INVALID_ARG;
     return fwd_bf16(q, k, v, out, lse, S, Hq, Hkv, d, c, causal, layout, kv_block, 0, -1, 0, rank,
                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ringattn_fwd_docmask(const void* q, const void* k, const void* v, float* out, float* lse, const int* doc_id,
+                         int* doc_start, int S, int Hq, int Hkv, int d, int c, int layout, ra_stream_t stream) {
+    if (!doc_id || !doc_start || static_cast<const void*>(doc_id) == static_cast<const void*>(doc_start))
+        return RA_ERR_INVALID_ARG;
+    if (((reinterpret_cast<uintptr_t>(doc_id) | reinterpret_cast<uintptr_t>(doc_start)) & 3u) != 0)
+        return RA_ERR_INVALID_ARG;
+    if (c < 1 || (layout != 0 && layout != 1)) return RA_ERR_INVALID_ARG;
+    const int nch = c * (layout == 1 ? 2 : 1);
+    if (S < 1 || S % nch != 0) return RA_ERR_INVALID_ARG;
+    // kv_block plays no part here (no ring messages): pass the chunk, always valid
+    return fwd_bf16(q, k, v, out, lse, S, Hq, Hkv, d, c, 1, layout, S / nch, 0, -1, 0, -1,
+                    reinterpret_cast<cudaStream_t>(stream), doc_id, doc_start);
 }
 
 int ringattn_fwd_natural(const void* q, const void* k, const void* v, float* out, float* lse, int S, int Hq,

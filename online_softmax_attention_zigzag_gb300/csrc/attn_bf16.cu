@@ -10,20 +10,28 @@
 // chunks i and 2c-1-i, "What breaks the load balance?").  Under the causal mask,
 // key tiles that lie wholly after a query tile are never visited.
 //
-// Design (one CTA per SM, persistent):
-//   * a work item is two 128-row query tiles that share every K/V tile: two query
-//     heads of one KV group at the same positions, or two adjacent tiles of one head;
-//   * warp 9 (one thread) streams Q tiles and, in ring order, K and V tiles into
+// A second mode ("Interrogating parallelism, part 5", "Why did Llama 3 not use a
+// ring?") takes the K/V of every rank as all-gathered and applies a document mask:
+// keys are visited in natural order from the start of the earliest document the item
+// touches, and a key is visible to a row when it lies between the start of the row's
+// document and the row itself.
+//
+// Design (one CTA per SM, persistent, 576 threads):
+//   * a work item is two 128-row query tiles (units) that share every K/V tile: two
+//     query heads of one KV group at the same positions, or two adjacent tiles of one
+//     head; items are ordered KV-head-major, then by decreasing causal work;
+//   * warp 17 (one thread) streams Q tiles and, in visiting order, K and V tiles into
 //     shared memory with TMA (128-byte swizzle), through a ring of stages guarded by
 //     mbarriers;
-//   * warp 8 (one thread) issues tcgen05.mma: S_x = Q_x K^T into TMEM, and after
+//   * warp 16 (one thread) issues tcgen05.mma: S_x = Q_x K^T into TMEM, and after
 //     softmax O_x += P_x V with P_x read from TMEM;
-//   * warpgroups 0 and 1 each own one query tile (thread = row): they read S from
-//     TMEM, apply the causal mask on diagonal tiles, update the running max and sum
-//     with exp2, write P (bf16) back to TMEM, rescale O in TMEM when the running max
-//     rose by more than 2^8, and at the end write out = O / (sum of the bf16 P) and
-//     lse = m + ln(sum of the exact p).
-//   The two warpgroups alternate, so one's softmax overlaps the other's MMAs.
+//   * warps 0-15 are four softmax warpgroups, two per unit, each owning 64 of the 128
+//     key columns of its unit's score tile (thread = row).  They read S from TMEM,
+//     mask, exchange partial row maxima through shared memory, update the running max
+//     and sums with exp2, write P (bf16) back to TMEM, rescale O in TMEM when the
+//     running max rose by more than 2^8, and at the end write out = O / (sum of the
+//     bf16 P) and lse = m + ln(sum of the exact p).
+//   One unit's softmax overlaps the other unit's MMAs.
 //
 // TMEM (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256) -- P_x is stored
 // as packed bf16 pairs in the upper half of S_x's columns -- O_0 [256, 256+D),
@@ -82,6 +90,7 @@ struct Item {
     int r;        // virtual rank holding the units
     int qrow[2];  // row of each unit's first query in q / out / lse
     int pmax;     // last natural query position in the item
+    int klo;      // document mask: first natural key position visited (a multiple of 128)
 };
 
 // Natural tile index of local tile t of rank r (local rows: chunk r, then for zigzag
@@ -97,6 +106,7 @@ __device__ __forceinline__ int rank_tile(const Ring& R, int r, int t) {
 // within a KV head by decreasing causal work (last query tiles first): the K/V tiles in
 // use at any time are then one head's, which stay in L2, and the snake assignment of
 // items to CTAs still deals out decreasing work.
+template <bool DOC>
 __device__ __forceinline__ void decode_item(const AttnBf16Params& p, int item, Item& it) {
     const Ring& R = p.ring;
     int t0, t1;
@@ -143,12 +153,25 @@ __device__ __forceinline__ void decode_item(const AttnBf16Params& p, int item, I
     it.qrow[0] = it.hq[0] * R.S + (p.natural ? it.pos[0] : rbase + local0);
     it.qrow[1] = (it.hq[1] < 0) ? -1 : it.hq[1] * R.S + (p.natural ? it.pos[1] : rbase + local1);
     it.pmax = max(it.pos[0], it.pos[1]) + kTile - 1;
+    // document mask: no key before the start of the document of the item's first row is
+    // visible to any of its rows (starts do not decrease along the sequence)
+    it.klo = DOC ? (__ldg(p.doc_start + min(it.pos[0], it.pos[1])) / kTile) * kTile : 0;
+}
+
+// Row of natural key position pos of KV head hk in k / v (rank-major unless p.natural).
+__device__ __forceinline__ int kv_row_of(const AttnBf16Params& p, int hk, int pos) {
+    const Ring& R = p.ring;
+    if (p.natural) return hk * R.S + pos;
+    const int k = pos / R.m;                            // natural chunk
+    const bool second = R.layout == 1 && k >= R.c;      // zigzag: the rank's second chunk
+    const int s = second ? 2 * R.c - 1 - k : k;         // rank holding it
+    return hk * R.S + s * R.n_r + (second ? R.m : 0) + (pos - k * R.m);
 }
 
 // Visit the item's key tiles in ring order: f(kv_row, key_pos).  kv_row is the row of
 // the tile's first key in k / v; key_pos its natural position.
 template <class F>
-__device__ __forceinline__ void for_each_kv_tile(const AttnBf16Params& p, const Item& it, F&& f) {
+__device__ __forceinline__ void for_each_ring_tile(const AttnBf16Params& p, const Item& it, F&& f) {
     const Ring& R = p.ring;
     for (int hop = R.hop_lo; hop < R.hop_hi; ++hop) {
         int s = it.r - hop;
@@ -168,7 +191,7 @@ __device__ __forceinline__ void for_each_kv_tile(const AttnBf16Params& p, const 
     }
 }
 
-__device__ __forceinline__ int count_kv_tiles(const AttnBf16Params& p, const Item& it) {
+__device__ __forceinline__ int count_ring_tiles(const AttnBf16Params& p, const Item& it) {
     const Ring& R = p.ring;
     int n = 0;
     for (int hop = R.hop_lo; hop < R.hop_hi; ++hop) {
@@ -184,6 +207,27 @@ __device__ __forceinline__ int count_kv_tiles(const AttnBf16Params& p, const Ite
         }
     }
     return n;
+}
+
+// With the document mask the K/V of every rank have been gathered: the keys are visited
+// in natural order, from the item's first document start to its last row.
+template <bool DOC, class F>
+__device__ __forceinline__ void for_each_kv_tile(const AttnBf16Params& p, const Item& it, F&& f) {
+    if constexpr (DOC) {
+        for (int pos = it.klo; pos <= it.pmax; pos += kTile)
+            if (!f(kv_row_of(p, it.hk, pos), pos)) return;
+    } else {
+        for_each_ring_tile(p, it, f);
+    }
+}
+
+template <bool DOC>
+__device__ __forceinline__ int count_kv_tiles(const AttnBf16Params& p, const Item& it) {
+    if constexpr (DOC) {
+        return (it.pmax + 1 - it.klo) / kTile;
+    } else {
+        return count_ring_tiles(p, it);
+    }
 }
 
 // Snake order over persistent CTAs: items are sorted by decreasing work, so
@@ -202,7 +246,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
 }
 
 // ------------------------------------------------------------------ TMA producer
-template <int D>
+template <int D, bool DOC>
 __device__ void load_role(const AttnBf16Params& p, const CUtensorMap* tq, const CUtensorMap* tk,
                           const CUtensorMap* tv, uint8_t* sQ, uint8_t* sKV, const Bars& b, const WaitCtl& wc) {
     using C = Cfg<D>;
@@ -216,8 +260,8 @@ __device__ void load_role(const AttnBf16Params& p, const CUtensorMap* tq, const 
         const int item = item_of_round(round);
         if (item >= p.n_items) continue;
         Item it;
-        decode_item(p, item, it);
-        if (count_kv_tiles(p, it) == 0) continue;
+        decode_item<DOC>(p, item, it);
+        if (count_kv_tiles<DOC>(p, it) == 0) continue;
         const int nx = (it.hq[1] >= 0) ? 2 : 1;
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
@@ -231,7 +275,7 @@ __device__ void load_role(const AttnBf16Params& p, const CUtensorMap* tq, const 
                 tma_load_2d_hint(sQ + x * C::kTileBytes + bx * C::kBoxBytes, tq, &b.q_full[x], bx * 64, qrow, stream);
         }
         if (!ok) break;
-        for_each_kv_tile(p, it, [&](int row, int) -> bool {
+        for_each_kv_tile<DOC>(p, it, [&](int row, int) -> bool {
             for (int kv = 0; kv < 2; ++kv) {
                 const uint32_t s = kv_idx % C::kStages;
                 if (!mbar_wait(&b.kv_empty[s], ((kv_idx / C::kStages) & 1u) ^ 1u, wc, 32)) { ok = false; return false; }
@@ -294,7 +338,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, int x, uint32_t v_base, 
     }
 }
 
-template <int D>
+template <int D, bool DOC>
 __device__ void mma_role(const AttnBf16Params& p, uint8_t* sQ, uint8_t* sKV, const Bars& b, uint32_t tmem,
                          const WaitCtl& wc) {
     using C = Cfg<D>;
@@ -306,8 +350,8 @@ __device__ void mma_role(const AttnBf16Params& p, uint8_t* sQ, uint8_t* sKV, con
         const int item = item_of_round(round);
         if (item >= p.n_items) continue;
         Item it;
-        decode_item(p, item, it);
-        const int nj = count_kv_tiles(p, it);
+        decode_item<DOC>(p, item, it);
+        const int nj = count_kv_tiles<DOC>(p, it);
         if (nj == 0) continue;
         const int nx = (it.hq[1] >= 0) ? 2 : 1;
 #pragma unroll
@@ -394,7 +438,7 @@ __device__ __forceinline__ bool unit_bar_and(int x, bool ok) {
 // x; thread t of the warpgroup owns row t.  The two halves of a tile exchange their
 // partial row maxima through shared memory once per key tile, so both compute P against
 // the same reference max; row sums stay per half until the epilogue.
-template <int D>
+template <int D, bool DOC>
 __device__ void softmax_role(const AttnBf16Params& p, int x, int h, const Bars& b, uint32_t tmem, float* xchg,
                              const WaitCtl& wc) {
     using C = Cfg<D>;
@@ -419,10 +463,10 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, int h, const Bars& 
         const int item = item_of_round(round);
         if (item >= p.n_items) continue;
         Item it;
-        decode_item(p, item, it);
+        decode_item<DOC>(p, item, it);
         const int my_hq = x ? it.hq[1] : it.hq[0];
         if (my_hq < 0) continue;
-        const int nj = count_kv_tiles(p, it);
+        const int nj = count_kv_tiles<DOC>(p, it);
         const size_t grow = static_cast<size_t>((x ? it.qrow[1] : it.qrow[0]) + row);
         float* orow = p.out + grow * D + h * kOHalf;
         if (nj == 0) {  // a message with no visible key for this tile
@@ -434,12 +478,13 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, int h, const Bars& 
         }
         const int tpos = x ? it.pos[1] : it.pos[0];
         const int qpos = tpos + row;
+        const int doc_lo = DOC ? __ldg(p.doc_start + qpos) : 0;  // first key of my document
         // l: sum of the exact p (for lse); lr: sum of p as rounded to bf16 for the P V
         // product, so that out = O / lr weighs every key consistently (a key that
         // dominates the row then comes out exactly, whatever its rounding)
         float m = -INFINITY, l = 0.f, lr = 0.f;
         int j = 0;
-        for_each_kv_tile(p, it, [&](int, int kpos) -> bool {
+        for_each_kv_tile<DOC>(p, it, [&](int, int kpos) -> bool {
             // One warp of the tile polls; the other seven wait in the named barrier, which
             // costs no issue slots (spinning warps would steal them from the ones computing).
             bool w_ok = true;
@@ -464,7 +509,14 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, int h, const Bars& 
                 for (int i = 0; i < kHalf; ++i) s[i] = 0.f;
             }
             const int kcol = kpos + h * kHalf;  // natural position of my first key column
-            if (causal && kcol + kHalf - 1 > qpos - row) {  // my half may cross the diagonal
+            if constexpr (DOC) {
+                // my keys [lo, hi] are visible: my document's start up to my own position
+                const int hi = qpos - kcol, lo = doc_lo - kcol;
+                if (lo > 0 || hi < kHalf - 1) {
+#pragma unroll
+                    for (int i = 0; i < kHalf; ++i) s[i] = (i > hi || i < lo) ? -INFINITY : s[i];
+                }
+            } else if (causal && kcol + kHalf - 1 > qpos - row) {  // my half may cross the diagonal
                 const int lim = qpos - kcol;                // my keys [0, lim] are visible
 #pragma unroll
                 for (int i = 0; i < kHalf; ++i) s[i] = (i > lim) ? -INFINITY : s[i];
@@ -570,7 +622,7 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, int h, const Bars& 
     }
 }
 
-template <int D>
+template <int D, bool DOC>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bf16_kernel(const __grid_constant__ AttnBf16Params p, const __grid_constant__ CUtensorMap tq,
                      const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
@@ -628,11 +680,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // warps 0-15: softmax, warpgroup g = warp / 4 owns tile g / 2, key half g % 2
     if (warp < 16) {
-        softmax_role<D>(p, warp / 8, (warp / 4) & 1, b, tmem, reinterpret_cast<float*>(smem + C::kXchgOff), wc);
+        softmax_role<D, DOC>(p, warp / 8, (warp / 4) & 1, b, tmem, reinterpret_cast<float*>(smem + C::kXchgOff), wc);
     } else if (warp == kMmaWarp) {
-        if (lane == 0) mma_role<D>(p, sQ, sKV, b, tmem, wc);
+        if (lane == 0) mma_role<D, DOC>(p, sQ, sKV, b, tmem, wc);
     } else if (warp == kLoadWarp) {
-        if (lane == 0) load_role<D>(p, &tq, &tk, &tv, sQ, sKV, b, wc);
+        if (lane == 0) load_role<D, DOC>(p, &tq, &tk, &tv, sQ, sKV, b, wc);
     }
 
     tc_fence_before();
@@ -641,11 +693,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <int D>
+template <int D, bool DOC>
 int launch_d(const AttnBf16Params& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
              int grid, cudaStream_t stream) {
     using C = Cfg<D>;
-    auto kern = attn_bf16_kernel<D>;
+    auto kern = attn_bf16_kernel<D, DOC>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
         return -4;
     kern<<<grid, kThreads, C::kSmemBytes, stream>>>(p, tq, tk, tv);
@@ -660,8 +712,11 @@ size_t attn_bf16_smem_bytes(int d) {
 
 int launch_attn_bf16(const AttnBf16Params& p, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv, int grid, cudaStream_t stream) {
-    if (p.ring.d == 128) return launch_d<128>(p, tq, tk, tv, grid, stream);
-    if (p.ring.d == 64) return launch_d<64>(p, tq, tk, tv, grid, stream);
+    const bool doc = p.doc_start != nullptr;
+    if (p.ring.d == 128) return doc ? launch_d<128, true>(p, tq, tk, tv, grid, stream)
+                                    : launch_d<128, false>(p, tq, tk, tv, grid, stream);
+    if (p.ring.d == 64) return doc ? launch_d<64, true>(p, tq, tk, tv, grid, stream)
+                                   : launch_d<64, false>(p, tq, tk, tv, grid, stream);
     return -2;
 }
 

@@ -35,6 +35,9 @@ struct AttnBf16Params {
     int n_items;
     float* out;
     float* lse;
+    // document mask over all-gathered K/V: first natural position of the document of
+    // every natural position (null: the ring, with or without the causal mask)
+    const int* doc_start;
     int* err;
     unsigned long long timeout_ns;
 };
@@ -57,6 +60,7 @@ int launch_permute(const void* src, void* dst, int S, int H, int row_bytes, int 
 int launch_merge(float* o_run, float* lse_run, const float* o_part, const float* lse_part, long long rows,
                  int d, cudaStream_t stream);
 int launch_selftest_timeout(int* err, unsigned long long timeout_ns, cudaStream_t stream);
+int launch_doc_start(const int* doc_id, int* doc_start, int S, cudaStream_t stream);
 
 // Shared-memory footprint of the bf16 kernel for head dimension d.
 size_t attn_bf16_smem_bytes(int d);

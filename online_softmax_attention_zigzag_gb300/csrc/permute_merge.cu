@@ -178,6 +178,28 @@ int launch_merge(float* o_run, float* lse_run, const float* o_part, const float*
     return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
+// ------------------------------------------------------------------ document starts
+// For a packed sequence whose document ids do not decrease, the first position of the
+// document of token i is the first position whose id is not below doc_id[i]: a binary
+// search over [0, i] (thread per token).  Whatever the ids, the result lies in [0, i].
+__global__ void doc_start_kernel(const int* __restrict__ doc_id, int* __restrict__ doc_start, int S) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= S) return;
+    const int id = doc_id[i];
+    int lo = 0, hi = i;
+    while (lo < hi) {
+        const int mid = lo + (hi - lo) / 2;
+        if (doc_id[mid] < id) lo = mid + 1;
+        else hi = mid;
+    }
+    doc_start[i] = lo;
+}
+
+int launch_doc_start(const int* doc_id, int* doc_start, int S, cudaStream_t stream) {
+    doc_start_kernel<<<(S + 255) / 256, 256, 0, stream>>>(doc_id, doc_start, S);
+    return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
 int launch_selftest_timeout(int* err, unsigned long long timeout_ns, cudaStream_t stream) {
     selftest_timeout_kernel<<<1, 32, 0, stream>>>(err, timeout_ns);
     return cudaGetLastError() == cudaSuccess ? 0 : -4;

@@ -29,7 +29,7 @@ EXPORTS = (
     "ringattn_fwd", "ringattn_fwd_natural", "ringattn_fwd_f32", "ringattn_fwd_hop",
     "ringattn_fwd_hop_f32", "ringattn_merge", "ringattn_permute", "ringattn_rank_work",
     "ringattn_sync_status", "ringattn_selftest_timeout", "ringattn_strerror", "ringattn_last_timeout",
-    "ringattn_fwd_rank",
+    "ringattn_fwd_rank", "ringattn_fwd_docmask",
 )
 
 
@@ -58,6 +58,7 @@ def lib() -> ctypes.CDLL:
             "ringattn_fwd": _ATTN + [_P],
             "ringattn_fwd_natural": _ATTN + [_P],
             "ringattn_fwd_rank": _ATTN + [_I, _P],
+            "ringattn_fwd_docmask": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
             "ringattn_fwd_f32": _ATTN + [_P],
             "ringattn_fwd_hop": _ATTN + [_I, _I, _P],
             "ringattn_fwd_hop_f32": _ATTN + [_I, _I, _P],
@@ -134,6 +135,17 @@ def fwd_rank(q, k, v, out, lse, *, c, causal, layout, kv_block, rank, stream=Non
     ptrs, S, Hq, Hkv, d = _attn_args(q, k, v, out, lse, torch.bfloat16)
     _check("ringattn_fwd_rank", lib().ringattn_fwd_rank(*ptrs, S, Hq, Hkv, d, c, int(causal), layout, kv_block,
                                                         int(rank), _stream(stream)))
+
+
+def fwd_docmask(q, k, v, out, lse, doc_id, doc_start, *, c, layout, stream=None) -> None:
+    """ringattn_fwd_docmask: all-gathered K/V, causal inside each document of ``doc_id``
+    (int32 [S], natural order, non-decreasing); ``doc_start`` is int32 [S] scratch."""
+    ptrs, S, Hq, Hkv, d = _attn_args(q, k, v, out, lse, torch.bfloat16)
+    for t, name in ((doc_id, "doc_id"), (doc_start, "doc_start")):
+        if tuple(t.shape) != (S,):
+            raise ValueError(f"{name} must be [S]")
+    ptrs += [_dev(doc_id, "doc_id", torch.int32), _dev(doc_start, "doc_start", torch.int32)]
+    _check("ringattn_fwd_docmask", lib().ringattn_fwd_docmask(*ptrs, S, Hq, Hkv, d, c, layout, _stream(stream)))
 
 
 def fwd_natural(q, k, v, out, lse, *, c, causal, layout, kv_block, stream=None) -> None:

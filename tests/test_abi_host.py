@@ -97,6 +97,19 @@ def test_rank_rejects_bad_rank(ra):
     assert L.ringattn_fwd_rank(P, P, P, P2, P2, 4096, 8, 3, 64, 4, 1, 1, 512, 0, S0) == -1  # geometry too
 
 
+def test_docmask_rejects(ra):
+    L = ra.lib()
+    D1, D2 = ctypes.c_void_p(0x30000), ctypes.c_void_p(0x40000)
+    geo = [4096, 8, 2, 128, 4, 1]
+    assert L.ringattn_fwd_docmask(P, P, P, P2, P2, NUL, D2, *geo, S0) == -1          # null ids
+    assert L.ringattn_fwd_docmask(P, P, P, P2, P2, D1, D1, *geo, S0) == -1           # scratch aliases ids
+    assert L.ringattn_fwd_docmask(P, P, P, P2, P2, ctypes.c_void_p(0x30002), D2, *geo, S0) == -1  # alignment
+    assert L.ringattn_fwd_docmask(P, P, P, P2, P2, D1, D2, 4100, 8, 2, 128, 4, 1, S0) == -1       # S % 2c
+    assert L.ringattn_fwd_docmask(P, P, P, P2, P2, D1, D2, 4096, 8, 3, 128, 4, 1, S0) == -1       # Hq % Hkv
+    assert L.ringattn_fwd_docmask(P, P, P, P2, P2, D1, D2, 4096, 8, 2, 96, 4, 1, S0) == -2        # d
+    assert L.ringattn_fwd_docmask(P, P, P, P2, P2, D1, D2, 4096, 8, 2, 128, 4, 2, S0) == -1       # layout
+
+
 def test_f32_rejects(ra):
     L = ra.lib()
     assert L.ringattn_fwd_f32(P, P, P, P2, P2, 12, 1, 1, 129, 3, 0, 0, 4, S0) == -2   # d > 128
