@@ -42,7 +42,8 @@
  *    CUDA runtime call or launch failed.  Device-side waits are bounded; one that
  *    runs out records RA_ERR_TIMEOUT, read with ringattn_sync_status.  No exception
  *    crosses the ABI and there is no CPU fallback.
- *  - The library allocates no device memory per call; scratch it needs is passed in.
+ *  - The library allocates no device memory per call; scratch it needs is passed in,
+ *    except for ringattn_fwd_docmask_noalloc, which uses a static device array.
  */
 #ifndef RINGATTN_H
 #define RINGATTN_H
@@ -118,6 +119,39 @@ int ringattn_fwd_rank(const void* q, const void* k, const void* v, float* out, f
 int ringattn_fwd_docmask(const void* q, const void* k, const void* v, float* out, float* lse,
                          const int* doc_id, int* doc_start, int S, int Hq, int Hkv, int d, int c,
                          int layout, ra_stream_t stream);
+
+/*
+ * ringattn_fwd_docmask_noalloc -- ringattn_fwd_docmask for callers that cannot allocate
+ * device memory.  The pages have no counterpart: this is a convenience of the library.
+ *
+ * Who needs it: code that must not call cudaMalloc at the point where it runs attention
+ * -- for example a host that runs under a fixed memory budget handed out up front, a
+ * plug-in whose host process owns every allocation, or code that must not make the
+ * implicit device synchronisation cudaMalloc/cudaFree can cause.  Such a caller is
+ * handed q, k, v, out, lse and doc_id by whoever owns its memory, but has no way to get
+ * the extra [S] int32 scratch that ringattn_fwd_docmask asks for.
+ *
+ * What it does: exactly ringattn_fwd_docmask, same arguments minus doc_start, same
+ * result, with the document starts kept in a static device array inside the library
+ * (RINGATTN_DOCMASK_NOALLOC_MAX_S int32 entries, 1 MiB, held by every GPU that loads the
+ * library until the process exits).  The call allocates nothing and frees nothing.
+ *
+ * Limits and sharing:
+ *  - S > RINGATTN_DOCMASK_NOALLOC_MAX_S is rejected with RA_ERR_UNSUPPORTED before any
+ *    device work; use ringattn_fwd_docmask with caller-owned scratch for longer sequences.
+ *  - Every call on a device shares the one array, and the array keeps what the last call
+ *    wrote.  Each call rewrites entries [0, S) on `stream` before reading them, so stale
+ *    contents never matter to a call on its own; but two calls whose work overlaps on the
+ *    GPU (different streams, no ordering between them) race on the array and give wrong
+ *    results.  Order such calls on one stream or with events.
+ *  - The first call on each device looks up the array's device address (once, with that
+ *    device current); make that first call before any stream capture begins.
+ * Requirements and errors otherwise as ringattn_fwd_docmask.
+ */
+#define RINGATTN_DOCMASK_NOALLOC_MAX_S 262144
+int ringattn_fwd_docmask_noalloc(const void* q, const void* k, const void* v, float* out, float* lse,
+                                 const int* doc_id, int S, int Hq, int Hkv, int d, int c, int layout,
+                                 ra_stream_t stream);
 
 /*
  * ringattn_fwd_natural -- as ringattn_fwd, but q, k, v, out and lse are in NATURAL

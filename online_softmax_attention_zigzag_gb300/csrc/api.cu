@@ -210,6 +210,31 @@ int fwd_f32(const float* q, const float* k, const float* v, float* out, float* l
     return ra::launch_attn_f32(p, stream);
 }
 
+// Scratch of ringattn_fwd_docmask_noalloc: the document start of every position, for
+// callers that cannot allocate it.  A file-scope device array, so it exists on every
+// device that loads the library and is never allocated or freed by a call.  In host
+// code the name is only a stand-in for the symbol: the device address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+__device__ __align__(256) int g_doc_start_scratch[RINGATTN_DOCMASK_NOALLOC_MAX_S];
+
+int* g_doc_scratch_addr[kMaxDevices];  // per device; guarded by g_mu
+
+// Device address of g_doc_start_scratch on the current device (set-up on first use).
+int doc_scratch(int** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return RA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return RA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_doc_scratch_addr[dev]) {
+        int* ptr = nullptr;
+        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_doc_start_scratch) != cudaSuccess || !ptr)
+            return RA_ERR_CUDA;
+        g_doc_scratch_addr[dev] = ptr;
+    }
+    *out = g_doc_scratch_addr[dev];
+    return RA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -239,6 +264,26 @@ int ringattn_fwd_docmask(const void* q, const void* k, const void* v, float* out
     // kv_block plays no part here (no ring messages): pass the chunk, always valid
     return fwd_bf16(q, k, v, out, lse, S, Hq, Hkv, d, c, 1, layout, S / nch, 0, -1, 0, -1,
                     reinterpret_cast<cudaStream_t>(stream), doc_id, doc_start);
+}
+
+int ringattn_fwd_docmask_noalloc(const void* q, const void* k, const void* v, float* out, float* lse,
+                                 const int* doc_id, int S, int Hq, int Hkv, int d, int c, int layout,
+                                 ra_stream_t stream) {
+    if (!doc_id || (reinterpret_cast<uintptr_t>(doc_id) & 3u) != 0) return RA_ERR_INVALID_ARG;
+    if (S > RINGATTN_DOCMASK_NOALLOC_MAX_S) return RA_ERR_UNSUPPORTED;  // beyond the static scratch
+    if (c < 1 || (layout != 0 && layout != 1)) return RA_ERR_INVALID_ARG;
+    const int nch = c * (layout == 1 ? 2 : 1);
+    if (S < 1 || S % nch != 0) return RA_ERR_INVALID_ARG;
+    // the device check comes before the symbol lookup, which needs a usable device
+    DeviceInfo* dev = nullptr;
+    int st = device_info(&dev);
+    if (st != RA_OK) return st;
+    int* scratch = nullptr;
+    if ((st = doc_scratch(&scratch)) != RA_OK) return st;
+    // doc_start_kernel rewrites scratch[0, S) on `stream` before the attention kernel
+    // reads it, so nothing left by an earlier call is ever read
+    return fwd_bf16(q, k, v, out, lse, S, Hq, Hkv, d, c, 1, layout, S / nch, 0, -1, 0, -1,
+                    reinterpret_cast<cudaStream_t>(stream), doc_id, scratch);
 }
 
 int ringattn_fwd_natural(const void* q, const void* k, const void* v, float* out, float* lse, int S, int Hq,

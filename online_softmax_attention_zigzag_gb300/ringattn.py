@@ -29,8 +29,11 @@ EXPORTS = (
     "ringattn_fwd", "ringattn_fwd_natural", "ringattn_fwd_f32", "ringattn_fwd_hop",
     "ringattn_fwd_hop_f32", "ringattn_merge", "ringattn_permute", "ringattn_rank_work",
     "ringattn_sync_status", "ringattn_selftest_timeout", "ringattn_strerror", "ringattn_last_timeout",
-    "ringattn_fwd_rank", "ringattn_fwd_docmask",
+    "ringattn_fwd_rank", "ringattn_fwd_docmask", "ringattn_fwd_docmask_noalloc",
 )
+
+# Longest sequence ringattn_fwd_docmask_noalloc takes (its static scratch, int32 [S]).
+DOCMASK_NOALLOC_MAX_S = 262144
 
 
 class RingAttnError(RuntimeError):
@@ -59,6 +62,7 @@ def lib() -> ctypes.CDLL:
             "ringattn_fwd_natural": _ATTN + [_P],
             "ringattn_fwd_rank": _ATTN + [_I, _P],
             "ringattn_fwd_docmask": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
+            "ringattn_fwd_docmask_noalloc": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
             "ringattn_fwd_f32": _ATTN + [_P],
             "ringattn_fwd_hop": _ATTN + [_I, _I, _P],
             "ringattn_fwd_hop_f32": _ATTN + [_I, _I, _P],
@@ -146,6 +150,21 @@ def fwd_docmask(q, k, v, out, lse, doc_id, doc_start, *, c, layout, stream=None)
             raise ValueError(f"{name} must be [S]")
     ptrs += [_dev(doc_id, "doc_id", torch.int32), _dev(doc_start, "doc_start", torch.int32)]
     _check("ringattn_fwd_docmask", lib().ringattn_fwd_docmask(*ptrs, S, Hq, Hkv, d, c, layout, _stream(stream)))
+
+
+def fwd_docmask_noalloc(q, k, v, out, lse, doc_id, *, c, layout, stream=None) -> None:
+    """ringattn_fwd_docmask_noalloc: :func:`fwd_docmask` without the scratch argument, for
+    callers that cannot allocate device memory; the document starts live in the library's
+    static device array, shared by every call (order overlapping calls on one stream)."""
+    ptrs, S, Hq, Hkv, d = _attn_args(q, k, v, out, lse, torch.bfloat16)
+    if tuple(doc_id.shape) != (S,):
+        raise ValueError("doc_id must be [S]")
+    if S > DOCMASK_NOALLOC_MAX_S:
+        raise ValueError(f"S = {S} exceeds the static scratch of ringattn_fwd_docmask_noalloc "
+                         f"({DOCMASK_NOALLOC_MAX_S} positions); use fwd_docmask with caller-owned scratch")
+    ptrs.append(_dev(doc_id, "doc_id", torch.int32))
+    _check("ringattn_fwd_docmask_noalloc",
+           lib().ringattn_fwd_docmask_noalloc(*ptrs, S, Hq, Hkv, d, c, layout, _stream(stream)))
 
 
 def fwd_natural(q, k, v, out, lse, *, c, causal, layout, kv_block, stream=None) -> None:

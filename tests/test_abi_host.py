@@ -110,6 +110,20 @@ def test_docmask_rejects(ra):
     assert L.ringattn_fwd_docmask(P, P, P, P2, P2, D1, D2, 4096, 8, 2, 128, 4, 2, S0) == -1       # layout
 
 
+def test_docmask_noalloc_rejects(ra):
+    L = ra.lib()
+    D1 = ctypes.c_void_p(0x30000)
+    hdr = open(os.path.join(ROOT, "include", "ringattn.h")).read()
+    assert int(re.search(r"#define RINGATTN_DOCMASK_NOALLOC_MAX_S (\d+)", hdr).group(1)) == ra.DOCMASK_NOALLOC_MAX_S
+    big = ra.DOCMASK_NOALLOC_MAX_S + 256
+    assert L.ringattn_fwd_docmask_noalloc(P, P, P, P2, P2, NUL, 4096, 8, 2, 128, 4, 1, S0) == -1  # null ids
+    assert L.ringattn_fwd_docmask_noalloc(P, P, P, P2, P2, ctypes.c_void_p(0x30002), 4096, 8, 2, 128, 4, 1,
+                                          S0) == -1                                                # alignment
+    assert L.ringattn_fwd_docmask_noalloc(P, P, P, P2, P2, D1, big, 8, 2, 128, 4, 1, S0) == -2     # beyond scratch
+    assert L.ringattn_fwd_docmask_noalloc(P, P, P, P2, P2, D1, 4100, 8, 2, 128, 4, 1, S0) == -1    # S % 2c
+    assert L.ringattn_fwd_docmask_noalloc(P, P, P, P2, P2, D1, 4096, 8, 2, 128, 4, 2, S0) == -1    # layout
+
+
 def test_f32_rejects(ra):
     L = ra.lib()
     assert L.ringattn_fwd_f32(P, P, P, P2, P2, 12, 1, 1, 129, 3, 0, 0, 4, S0) == -2   # d > 128
