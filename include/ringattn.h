@@ -154,6 +154,39 @@ int ringattn_fwd_docmask_noalloc(const void* q, const void* k, const void* v, fl
                                  ra_stream_t stream);
 
 /*
+ * ringattn_fwd_host -- ringattn_fwd_natural on HOST buffers: copies q, k, v to the device,
+ * computes, and copies out and lse back, with the copies overlapped with the attention.
+ * The computation is that of ringattn_fwd_natural (same sources, same result); the KV
+ * heads are split into G groups (G divides Hkv, at most 16, each group at least four
+ * waves of work items), and while group g computes on `stream`, the inputs of later
+ * groups travel host->device and the results of earlier groups device->host, on two
+ * streams the library creates once per device and keeps until exit.
+ * q_h, k_h, v_h: HOST [Hq|Hkv, S, d] bf16, natural order.  out_h: HOST [Hq, S, d] fp32,
+ *     lse_h: HOST [Hq, S] fp32, natural order.  Page-locked memory (cudaHostAlloc or
+ *     cudaHostRegister) is needed for the copies to run asynchronously and overlap;
+ *     pageable memory gives the same result with copies that block the calling thread.
+ *     The host buffers must stay valid, and out_h/lse_h unread, until `stream` has
+ *     completed the call (e.g. cudaStreamSynchronize(stream)).
+ * workspace: DEVICE buffer of at least ringattn_host_workspace_bytes(S, Hq, Hkv, d)
+ *     bytes, 256-byte aligned, owned by the caller; it receives the device copies.  Calls
+ *     sharing one workspace must be ordered (same stream, or events).
+ * stream: the work starts after everything queued on `stream` before the call, and
+ *     `stream` completes only after the last result has reached the host.
+ * Requirements as ringattn_fwd otherwise.  Arguments are validated before anything is
+ * enqueued; RA_ERR_CUDA can leave part of the work enqueued.
+ */
+int ringattn_fwd_host(const void* q_h, const void* k_h, const void* v_h, float* out_h, float* lse_h,
+                      int S, int Hq, int Hkv, int d, int c, int causal, int layout, int kv_block,
+                      void* workspace, long long workspace_bytes, ra_stream_t stream);
+
+/*
+ * ringattn_host_workspace_bytes -- host only.  Device workspace that ringattn_fwd_host
+ * needs for this geometry: q, k, v (bf16) and out, lse (fp32), each rounded up to 256
+ * bytes.  Writes the count to *bytes.
+ */
+int ringattn_host_workspace_bytes(int S, int Hq, int Hkv, int d, long long* bytes);
+
+/*
  * ringattn_fwd_natural -- as ringattn_fwd, but q, k, v, out and lse are in NATURAL
  * sequence order: the zigzag/contiguous chunk map is applied in the kernel's tile
  * addressing, so no permutation pass is needed.  Same result, same requirements.

@@ -235,6 +235,129 @@ int doc_scratch(int** out) {
     return RA_OK;
 }
 
+// ------------------------------------------------------------------ host-buffer path
+// ringattn_fwd_host runs the natural-order kernel once per group of KV heads, so that the
+// copies of one group overlap the attention of another: H2D of group g+1 and D2H of group
+// g-1 run on two internal streams (one per copy direction) while group g computes on the
+// caller's stream.  Streams and events are created once per device and kept until exit.
+constexpr int kMaxGroups = 16;
+
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t in[kMaxGroups] = {}, out[kMaxGroups] = {};
+    std::mutex mu;  // one call enqueues at a time per device
+};
+
+HostPipe g_pipe[kMaxDevices];
+
+int host_pipe(HostPipe** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return RA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return RA_ERR_UNSUPPORTED;
+    HostPipe& hp = g_pipe[dev];
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!hp.ready) {
+        const unsigned ef = cudaEventDisableTiming;
+        if (cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&hp.start, ef) != cudaSuccess ||
+            cudaEventCreateWithFlags(&hp.done, ef) != cudaSuccess)
+            return RA_ERR_CUDA;
+        for (int i = 0; i < kMaxGroups; ++i)
+            if (cudaEventCreateWithFlags(&hp.in[i], ef) != cudaSuccess ||
+                cudaEventCreateWithFlags(&hp.out[i], ef) != cudaSuccess)
+                return RA_ERR_CUDA;
+        hp.ready = true;
+    }
+    *out = &hp;
+    return RA_OK;
+}
+
+// Byte offsets of the device copies inside the host path's workspace, each 256-byte aligned:
+// q, k, v (bf16), out, lse (fp32), all [H, S, ...] in natural order; off[5] = total.
+void host_workspace_layout(int S, int Hq, int Hkv, int d, long long off[6]) {
+    const long long sz[5] = {2LL * Hq * S * d, 2LL * Hkv * S * d, 2LL * Hkv * S * d, 4LL * Hq * S * d,
+                             4LL * Hq * S};
+    long long o = 0;
+    for (int i = 0; i < 5; ++i) {
+        off[i] = o;
+        o += (sz[i] + 255) / 256 * 256;
+    }
+    off[5] = o;
+}
+
+// Number of KV-head groups: as many as divide Hkv (at most kMaxGroups) while every group
+// still holds at least four waves of work items, so that no launch is mostly tail.
+int host_groups(int S, int Hq, int Hkv, int sms) {
+    const long long items = static_cast<long long>(S / 128) * Hq / 2;  // about two tiles per item
+    int best = 1;
+    for (int gcount = 1; gcount <= Hkv && gcount <= kMaxGroups; ++gcount)
+        if (Hkv % gcount == 0 && items / gcount >= 4LL * sms) best = gcount;
+    return best;
+}
+
+int fwd_host(const void* q_h, const void* k_h, const void* v_h, float* out_h, float* lse_h, int S, int Hq,
+             int Hkv, int d, int c, int causal, int layout, int kv_block, void* ws, size_t ws_bytes,
+             cudaStream_t stream) {
+    if (!q_h || !k_h || !v_h || !out_h || !lse_h || !ws) return RA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return RA_ERR_INVALID_ARG;
+    ra::Ring R;
+    int st = make_ring(S, Hq, Hkv, d, c, causal, layout, kv_block, &R);
+    if (st != RA_OK) return st;
+    if (d != 64 && d != 128) return RA_ERR_UNSUPPORTED;
+    if (R.m % 128 != 0 || kv_block % 128 != 0) return RA_ERR_UNSUPPORTED;
+    long long off[6];
+    host_workspace_layout(S, Hq, Hkv, d, off);
+    if (static_cast<long long>(ws_bytes) < off[5]) return RA_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != RA_OK) return st;
+    HostPipe* hp = nullptr;
+    if ((st = host_pipe(&hp)) != RA_OK) return st;
+
+    char* base = static_cast<char*>(ws);
+    const int G = host_groups(S, Hq, Hkv, dev->sms);
+    const int hq_g = Hq / G, hkv_g = Hkv / G;
+    const size_t q_b = 2ull * hq_g * S * d, kv_b = 2ull * hkv_g * S * d;
+    const size_t o_b = 4ull * hq_g * S * d, l_b = 4ull * hq_g * S;
+    std::lock_guard<std::mutex> lock(hp->mu);
+    // the copies start only after the work already queued on `stream`
+    if (cudaEventRecord(hp->start, stream) != cudaSuccess || cudaStreamWaitEvent(hp->h2d, hp->start, 0) != cudaSuccess)
+        return RA_ERR_CUDA;
+    for (int gi = 0; gi < G; ++gi) {
+        char* qd = base + off[0] + gi * q_b;
+        char* kd = base + off[1] + gi * kv_b;
+        char* vd = base + off[2] + gi * kv_b;
+        if (cudaMemcpyAsync(kd, static_cast<const char*>(k_h) + gi * kv_b, kv_b, cudaMemcpyHostToDevice,
+                            hp->h2d) != cudaSuccess ||
+            cudaMemcpyAsync(vd, static_cast<const char*>(v_h) + gi * kv_b, kv_b, cudaMemcpyHostToDevice,
+                            hp->h2d) != cudaSuccess ||
+            cudaMemcpyAsync(qd, static_cast<const char*>(q_h) + gi * q_b, q_b, cudaMemcpyHostToDevice,
+                            hp->h2d) != cudaSuccess ||
+            cudaEventRecord(hp->in[gi], hp->h2d) != cudaSuccess)
+            return RA_ERR_CUDA;
+    }
+    for (int gi = 0; gi < G; ++gi) {
+        float* od = reinterpret_cast<float*>(base + off[3] + gi * o_b);
+        float* ld = reinterpret_cast<float*>(base + off[4] + gi * l_b);
+        if (cudaStreamWaitEvent(stream, hp->in[gi], 0) != cudaSuccess) return RA_ERR_CUDA;
+        st = fwd_bf16(base + off[0] + gi * q_b, base + off[1] + gi * kv_b, base + off[2] + gi * kv_b, od, ld, S,
+                      hq_g, hkv_g, d, c, causal, layout, kv_block, 1, -1, 0, -1, stream);
+        if (st != RA_OK) return st;
+        if (cudaEventRecord(hp->out[gi], stream) != cudaSuccess || cudaStreamWaitEvent(hp->d2h, hp->out[gi], 0) != cudaSuccess ||
+            cudaMemcpyAsync(reinterpret_cast<char*>(out_h) + gi * o_b, od, o_b, cudaMemcpyDeviceToHost, hp->d2h) !=
+                cudaSuccess ||
+            cudaMemcpyAsync(reinterpret_cast<char*>(lse_h) + gi * l_b, ld, l_b, cudaMemcpyDeviceToHost, hp->d2h) !=
+                cudaSuccess)
+            return RA_ERR_CUDA;
+    }
+    // `stream` completes only once the last result has reached the host
+    if (cudaEventRecord(hp->done, hp->d2h) != cudaSuccess || cudaStreamWaitEvent(stream, hp->done, 0) != cudaSuccess)
+        return RA_ERR_CUDA;
+    return RA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -284,6 +407,22 @@ int ringattn_fwd_docmask_noalloc(const void* q, const void* k, const void* v, fl
     // reads it, so nothing left by an earlier call is ever read
     return fwd_bf16(q, k, v, out, lse, S, Hq, Hkv, d, c, 1, layout, S / nch, 0, -1, 0, -1,
                     reinterpret_cast<cudaStream_t>(stream), doc_id, scratch);
+}
+
+int ringattn_host_workspace_bytes(int S, int Hq, int Hkv, int d, long long* bytes) {
+    if (!bytes || S < 1 || Hq < 1 || Hkv < 1 || d < 1) return RA_ERR_INVALID_ARG;
+    long long off[6];
+    host_workspace_layout(S, Hq, Hkv, d, off);
+    *bytes = off[5];
+    return RA_OK;
+}
+
+int ringattn_fwd_host(const void* q_h, const void* k_h, const void* v_h, float* out_h, float* lse_h, int S, int Hq,
+                      int Hkv, int d, int c, int causal, int layout, int kv_block, void* workspace,
+                      long long workspace_bytes, ra_stream_t stream) {
+    if (workspace_bytes < 0) return RA_ERR_INVALID_ARG;
+    return fwd_host(q_h, k_h, v_h, out_h, lse_h, S, Hq, Hkv, d, c, causal, layout, kv_block, workspace,
+                    static_cast<size_t>(workspace_bytes), reinterpret_cast<cudaStream_t>(stream));
 }
 
 int ringattn_fwd_natural(const void* q, const void* k, const void* v, float* out, float* lse, int S, int Hq,

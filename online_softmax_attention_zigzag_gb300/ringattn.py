@@ -30,6 +30,7 @@ EXPORTS = (
     "ringattn_fwd_hop_f32", "ringattn_merge", "ringattn_permute", "ringattn_rank_work",
     "ringattn_sync_status", "ringattn_selftest_timeout", "ringattn_strerror", "ringattn_last_timeout",
     "ringattn_fwd_rank", "ringattn_fwd_docmask", "ringattn_fwd_docmask_noalloc",
+    "ringattn_fwd_host", "ringattn_host_workspace_bytes",
 )
 
 # Longest sequence ringattn_fwd_docmask_noalloc takes (its static scratch, int32 [S]).
@@ -63,6 +64,8 @@ def lib() -> ctypes.CDLL:
             "ringattn_fwd_rank": _ATTN + [_I, _P],
             "ringattn_fwd_docmask": [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
             "ringattn_fwd_docmask_noalloc": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
+            "ringattn_fwd_host": _ATTN + [_P, _LL, _P],
+            "ringattn_host_workspace_bytes": [_I, _I, _I, _I, _P],
             "ringattn_fwd_f32": _ATTN + [_P],
             "ringattn_fwd_hop": _ATTN + [_I, _I, _P],
             "ringattn_fwd_hop_f32": _ATTN + [_I, _I, _P],
@@ -165,6 +168,43 @@ def fwd_docmask_noalloc(q, k, v, out, lse, doc_id, *, c, layout, stream=None) ->
     ptrs.append(_dev(doc_id, "doc_id", torch.int32))
     _check("ringattn_fwd_docmask_noalloc",
            lib().ringattn_fwd_docmask_noalloc(*ptrs, S, Hq, Hkv, d, c, layout, _stream(stream)))
+
+
+def host_workspace_bytes(S: int, Hq: int, Hkv: int, d: int) -> int:
+    """ringattn_host_workspace_bytes (host only)."""
+    n = ctypes.c_longlong(0)
+    _check("ringattn_host_workspace_bytes", lib().ringattn_host_workspace_bytes(S, Hq, Hkv, d, ctypes.byref(n)))
+    return n.value
+
+
+def _host(t: torch.Tensor, name: str, dtype):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError(f"{name} must be a CPU tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def fwd_host(q_h, k_h, v_h, out_h, lse_h, workspace, *, c, causal, layout, kv_block, stream=None) -> None:
+    """ringattn_fwd_host: natural-order HOST tensors (pin them for overlap) in, HOST out and
+    lse out; ``workspace`` is a CUDA uint8 tensor of at least :func:`host_workspace_bytes`.
+    Asynchronous on ``stream``: synchronise it before reading out_h / lse_h."""
+    if q_h.dim() != 3 or k_h.dim() != 3 or v_h.dim() != 3:
+        raise ValueError("q, k, v must be [H, S, d]")
+    Hq, S, d = q_h.shape
+    Hkv = k_h.shape[0]
+    if tuple(k_h.shape) != (Hkv, S, d) or tuple(v_h.shape) != (Hkv, S, d):
+        raise ValueError("k and v must be [Hkv, S, d] with q's S and d")
+    if tuple(out_h.shape) != (Hq, S, d) or tuple(lse_h.shape) != (Hq, S):
+        raise ValueError("out must be [Hq, S, d] and lse [Hq, S]")
+    ptrs = [_host(q_h, "q", torch.bfloat16), _host(k_h, "k", torch.bfloat16), _host(v_h, "v", torch.bfloat16),
+            _host(out_h, "out", torch.float32), _host(lse_h, "lse", torch.float32)]
+    ws = _dev(workspace, "workspace")
+    _check("ringattn_fwd_host", lib().ringattn_fwd_host(
+        *ptrs, S, Hq, Hkv, d, c, causal, layout, kv_block, ws, workspace.numel() * workspace.element_size(),
+        _stream(stream)))
 
 
 def fwd_natural(q, k, v, out, lse, *, c, causal, layout, kv_block, stream=None) -> None:

@@ -124,6 +124,27 @@ def test_docmask_noalloc_rejects(ra):
     assert L.ringattn_fwd_docmask_noalloc(P, P, P, P2, P2, D1, 4096, 8, 2, 128, 4, 2, S0) == -1    # layout
 
 
+def test_host_path_workspace_and_rejects(ra):
+    L = ra.lib()
+    n = ctypes.c_longlong(0)
+    assert L.ringattn_host_workspace_bytes(1000, 3, 1, 64, ctypes.byref(n)) == 0
+    # q, k, v bf16 and out, lse fp32, each rounded up to 256 bytes
+    sizes = [2 * 3 * 1000 * 64, 2 * 1000 * 64, 2 * 1000 * 64, 4 * 3 * 1000 * 64, 4 * 3 * 1000]
+    assert n.value == sum((x + 255) // 256 * 256 for x in sizes)
+    assert L.ringattn_host_workspace_bytes(0, 3, 1, 64, ctypes.byref(n)) == -1
+    assert L.ringattn_host_workspace_bytes(1000, 3, 1, 64, NUL) == -1
+    need = ra.host_workspace_bytes(4096, 8, 2, 128)
+    W = ctypes.c_void_p(0x100000)
+    geo = [4096, 8, 2, 128, 4, 1, 1, 512]
+    assert L.ringattn_fwd_host(NUL, P, P, P2, P2, *geo, W, need, S0) == -1                   # null input
+    assert L.ringattn_fwd_host(P, P, P, P2, P2, *geo, NUL, need, S0) == -1                   # null workspace
+    assert L.ringattn_fwd_host(P, P, P, P2, P2, *geo, ctypes.c_void_p(0x100010), need, S0) == -1  # alignment
+    assert L.ringattn_fwd_host(P, P, P, P2, P2, *geo, W, need - 1, S0) == -1                 # too small
+    assert L.ringattn_fwd_host(P, P, P, P2, P2, *geo, W, -5, S0) == -1
+    assert L.ringattn_fwd_host(P, P, P, P2, P2, 4096, 8, 3, 128, 4, 1, 1, 512, W, need, S0) == -1  # Hq % Hkv
+    assert L.ringattn_fwd_host(P, P, P, P2, P2, 4096, 8, 2, 96, 4, 1, 1, 512, W, need, S0) == -2   # d
+
+
 def test_f32_rejects(ra):
     L = ra.lib()
     assert L.ringattn_fwd_f32(P, P, P, P2, P2, 12, 1, 1, 129, 3, 0, 0, 4, S0) == -2   # d > 128
