@@ -26,6 +26,11 @@ numpy).  Each function names the passage it follows:
 * :mod:`oracle.docmask` -- attention over all-gathered keys and values under a
   document mask, causal inside each document ("Interrogating parallelism,
   part 5", section "Why did Llama 3 not use a ring?").
+* :mod:`oracle.ulysses` -- Ulysses: the all-to-all from sequence shards to head
+  shards and back, message by message, with full-sequence attention on each
+  rank's heads in between ("Ring Attention and Ulysses shard a sequence two
+  different ways...", section "Ulysses: an all-to-all relayout instead of a
+  rotation").
 
 Every function is pinned by ``tests/test_oracle_*.py`` against closed forms,
 brute force, library routines it does not call, or values the pages print.

@@ -340,3 +340,67 @@ def pin_doc_pairs(pairs_fn):
     assert pairs_fn(np.zeros(10, dtype=np.int64)) == 55
     lens = [3, 1, 8, 2]
     assert pairs_fn(np.repeat(np.arange(4), lens)) == sum(n * (n + 1) // 2 for n in lens)
+
+
+# --------------------------------------------------------------------------- Ulysses relayout
+
+def _positions_by_hand(S, c, lay, r):
+    """Natural positions of rank r's tokens in local order, restated from the pages'
+    chunking ("What breaks the load balance?") with plain Python ranges."""
+    nch = 2 * c if lay == 1 else c
+    m = S // nch
+    chunks = [r, 2 * c - 1 - r] if lay == 1 else [r]
+    return [ch * m + i for ch in chunks for i in range(m)]
+
+
+def pin_ulysses_relayout(to_heads_fn, to_seq_fn):
+    """Sequence-sharded -> head-sharded moves token p, head h of the sequence to
+    position p of head h on the rank that keeps h ("Ulysses: an all-to-all relayout
+    instead of a rotation"); the inverse brings every value home.  Checked element by
+    element with loops, on shards cut from a natural tensor by hand."""
+    for (S, H, c, lay, row) in ((12, 4, 2, 1, 3), (12, 6, 3, 0, 2), (16, 4, 4, 1, 1), (8, 3, 1, 0, 2)):
+        X = rand((S, H, row), S * 7 + H + c)
+        shards = [X[_positions_by_hand(S, c, lay, r)] for r in range(c)]
+        heads_of = lambda r: np.arange(r * (H // c), (r + 1) * (H // c))  # noqa: E731
+        parts = to_heads_fn(shards, heads_of, S, c, lay)
+        assert len(parts) == c
+        for r in range(c):
+            hs = list(heads_of(r))
+            assert parts[r].shape == (len(hs), S, row), "head shard has the wrong shape"
+            for i, h in enumerate(hs):
+                for p in range(S):
+                    assert np.array_equal(parts[r][i, p], X[p, h]), "a value landed in the wrong place"
+        back = to_seq_fn(parts, heads_of, H, S, c, lay)
+        for r in range(c):
+            assert np.array_equal(back[r], shards[r]), "the inverse relayout does not restore the shards"
+
+
+def pin_ulysses_attention(ulysses_fn):
+    """Ulysses gives plain attention (torch SDPA, float64) at every token and head, in
+    the sequence-sharded layout, for MHA, GQA and GQA with more ranks than KV heads."""
+    cases = [
+        # Hq, Hkv, S, d, c, layout, causal
+        (4, 4, 16, 5, 2, 1, True),
+        (4, 2, 24, 3, 2, 0, True),
+        (4, 1, 16, 4, 4, 1, True),
+        (6, 3, 12, 2, 3, 0, False),
+    ]
+    for (Hq, Hkv, S, d, c, lay, causal) in cases:
+        seed = Hq * 100 + S + c
+        q, k, v = rand((Hq, S, d), seed), rand((Hkv, S, d), seed + 1), rand((Hkv, S, d), seed + 2)
+        g = Hq // Hkv
+        tq = torch.from_numpy(q)
+        tk = torch.from_numpy(k).repeat_interleave(g, dim=0)
+        tv = torch.from_numpy(v).repeat_interleave(g, dim=0)
+        to = torch.nn.functional.scaled_dot_product_attention(tq[None], tk[None], tv[None], is_causal=causal,
+                                                              scale=1.0)[0].numpy()
+        sc = tq @ tk.transpose(-1, -2)
+        if causal:
+            sc = sc.masked_fill(torch.ones(S, S, dtype=torch.bool).triu(1), float("-inf"))
+        tl = torch.logsumexp(sc, dim=-1).numpy()
+        order = [p for r in range(c) for p in _positions_by_hand(S, c, lay, r)]
+        seq = lambda x: np.ascontiguousarray(np.swapaxes(x, 0, 1)[order])  # noqa: E731  [S, H, d]
+        o, l = ulysses_fn(seq(q), seq(k), seq(v), c, lay, causal)
+        assert o.shape == (S, Hq, d) and l.shape == (S, Hq)
+        assert np.abs(o - seq(to)).max() < 1e-10, "Ulysses out differs from attention"
+        assert np.abs(l - tl.T[order]).max() < 1e-10, "Ulysses lse differs from logsumexp"

@@ -205,3 +205,56 @@ def test_doc_copy_passes():
     pins.pin_doc_brute(fn)
     pins.pin_doc_segments_vs_torch(fn)
     pins.pin_doc_closed_forms(fn)
+
+
+# ---------------------------------------------------------------- Ulysses relayout mutants
+
+def _to_heads(shards, heads_of, S, c, lay, *, local_order=False, contiguous_map=False):
+    row = shards[0].shape[2:]
+    out = [np.zeros((len(heads_of(r)), S) + row) for r in range(c)]
+    for s in range(c):
+        if local_order:                 # tokens stored where they sit on the sender, not by position
+            pos = np.arange(s * shards[s].shape[0], (s + 1) * shards[s].shape[0])
+        else:
+            pos = layout.rank_positions(S, c, 0 if contiguous_map else lay, s)
+        for r in range(c):
+            out[r][:, pos] = np.swapaxes(shards[s][:, heads_of(r)], 0, 1)
+    return out
+
+
+def _to_seq(parts, heads_of, H, S, c, lay):
+    from oracle import ulysses
+    return ulysses.heads_to_seq(parts, heads_of, H, S, c, lay)
+
+
+@pytest.mark.parametrize("kw", [dict(local_order=True), dict(contiguous_map=True)])
+def test_ulysses_relayout_mutant_caught(kw):
+    with pytest.raises(AssertionError):
+        pins.pin_ulysses_relayout(lambda *a: _to_heads(*a, **kw), _to_seq)
+
+
+def test_ulysses_relayout_unmutated_copy_passes():
+    pins.pin_ulysses_relayout(_to_heads, _to_seq)
+
+
+def test_ulysses_attention_mutants_caught():
+    from oracle import ulysses
+
+    def wrong_heads(q_seq, k_seq, v_seq, c, lay, causal):
+        # every rank takes KV head (rank) instead of the KV heads its query heads use
+        q_seq, k_seq, v_seq = (np.asarray(x, float) for x in (q_seq, k_seq, v_seq))
+        S, Hq, d = q_seq.shape
+        Hkv = k_seq.shape[1]
+        out = np.empty((S, Hq, d)); lse = np.empty((S, Hq))
+        order = layout.rank_major_order(S, c, lay)
+        qn = np.empty_like(q_seq); kn = np.empty_like(k_seq); vn = np.empty_like(v_seq)
+        qn[order], kn[order], vn[order] = q_seq, k_seq, v_seq
+        for h in range(Hq):
+            r = h // (Hq // c)
+            o, l = attention.full_attention(qn[:, h][None], kn[:, r % Hkv][None], vn[:, r % Hkv][None], causal)
+            out[:, h] = o[0][order]; lse[:, h] = l[0][order]
+        return out, lse
+
+    with pytest.raises(AssertionError):
+        pins.pin_ulysses_attention(wrong_heads)
+    pins.pin_ulysses_attention(ulysses.ulysses_attention)

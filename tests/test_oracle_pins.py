@@ -107,3 +107,20 @@ def test_doc_mask_rows_match_whole():
 
 def test_doc_pairs():
     pins.pin_doc_pairs(docmask.doc_pairs)
+
+
+def test_ulysses_relayout_moves_every_value_home():
+    from oracle import ulysses
+    pins.pin_ulysses_relayout(ulysses.seq_to_heads, ulysses.heads_to_seq)
+
+
+def test_ulysses_attention_is_attention():
+    from oracle import ulysses
+    pins.pin_ulysses_attention(ulysses.ulysses_attention)
+
+
+def test_ulysses_kv_heads_replicate_when_ranks_outnumber_them():
+    from oracle import ulysses
+    # 8 query heads over 2 KV heads on 4 ranks: ranks 0-1 need KV head 0, ranks 2-3 KV head 1
+    assert [list(ulysses.kv_heads(8, 2, 4, r)) for r in range(4)] == [[0], [0], [1], [1]]
+    assert [list(ulysses.kv_heads(8, 4, 2, r)) for r in range(2)] == [[0, 1], [2, 3]]
