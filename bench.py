@@ -56,6 +56,8 @@ def parse():
                     help="skip the 128k workload and the natural-order step measured beside the headline")
     ap.add_argument("--per-hop-sweep", action="store_true",
                     help="instead of the headline: fused vs per-hop + merge over the workload's kv_block sweep")
+    ap.add_argument("--ulysses", action="store_true",
+                    help="instead of the headline: Ulysses on one GPU (relayouts + attention) on the workload")
     ap.add_argument("--attention-only", action="store_true",
                     help="instead of the headline: the attention kernel alone on the workload, --steps launches")
     ap.add_argument("--per-rank", action="store_true",
@@ -270,6 +272,37 @@ def attention_only(ra, w, dev, stream, reps, peak):
             "frac": tf / peak, "launches": reps + 1, **what}
 
 
+def ulysses_only(ra, w, dev, stream, reps, peak, hbm_peak):
+    """Ulysses on one GPU for workload w: the all-to-all relayout of q, k, v to head
+    shards, attention of every rank's heads over the whole sequence, relayout of out and
+    lse back.  TFLOP/s of the whole call, and GB/s of the q relayout alone."""
+    q_h, k_h, v_h = make_qkv(w)
+    seq = []
+    for x in (q_h, k_h, v_h):
+        xd = x.to(dev)
+        xs = torch.empty((w.seq, xd.shape[0], w.d), dtype=xd.dtype, device=dev)
+        ra.relayout(xd, xs, c=w.c, layout=w.layout, to_heads=0)   # natural heads -> sequence shards
+        seq.append(xs)
+        del xd
+    del q_h, k_h, v_h
+    qs, ks, vs = seq
+    o = torch.empty((w.seq, w.bhq, w.d), dtype=torch.float32, device=dev)
+    l = torch.empty((w.seq, w.bhq), dtype=torch.float32, device=dev)
+    ws = torch.empty(ra.host_workspace_bytes(w.seq, w.bhq, w.bhkv, w.d), dtype=torch.uint8, device=dev)
+    ms = time_events(lambda: ra.ulysses_fwd(qs, ks, vs, o, l, ws, c=w.c, causal=w.causal, layout=w.layout),
+                     reps, stream)
+    qh = torch.empty((w.bhq, w.seq, w.d), dtype=qs.dtype, device=dev)
+    ms_q = time_events(lambda: ra.relayout(qs, qh, c=w.c, layout=w.layout, to_heads=1), reps, stream)
+    if ra.sync_status() != ra.RA_OK:
+        raise SystemExit("device wait timed out")
+    tf = w.flops() / (ms * 1e-3) / 1e12
+    qbytes = 2 * qs.numel() * qs.element_size()
+    return {"workload": w.name, "mode": "Ulysses (relayout q, k, v; attention per head group; relayout out, lse)",
+            "ms": ms, "achieved": tf, "unit": "TFLOP/s", "peak": peak, "frac": tf / peak,
+            "relayout_q": {"kernel": "relayout_kernel<uint4>", "ms": ms_q, "bytes": qbytes,
+                           "GB/s": qbytes / (ms_q * 1e-3) / 1e9, "frac": qbytes / (ms_q * 1e-3) / 1e9 / hbm_peak}}
+
+
 def per_hop_sweep(ra, w, dev, stream):
     """Fused kernel vs the ring-faithful per-hop path (one partial per message, folded in
     with the merge kernel) for each kv_block of the workload's sweep."""
@@ -361,6 +394,12 @@ def main():
         if rank == 0:
             print(json.dumps({"metric": METRIC, "unit": UNIT, "mode": "per-hop sweep", "workload": w.name,
                               "sweep": res}), flush=True)
+        return
+    if args.ulysses:
+        dev = torch.device("cuda", local)
+        res = ulysses_only(ra, w, dev, torch.cuda.current_stream(dev), max(1, args.steps), peaks()[0], peaks()[2])
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "unit": UNIT, **res}), flush=True)
         return
     if args.attention_only:
         dev = torch.device("cuda", local)
@@ -500,6 +539,7 @@ def main():
         torch.cuda.empty_cache()
         extra = [attention_only(ra, WORKLOADS[name], dev, stream, 5, peaks()[0])
                  for name in ("causal_gqa_S131072_h32x8_d128_c16_zigzag", "docmask_gqa_S32768_h64x8_d128_c8_zigzag")]
+        extra.append(ulysses_only(ra, w, dev, stream, 5, peaks()[0], peaks()[2]))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

@@ -187,6 +187,46 @@ int ringattn_fwd_host(const void* q_h, const void* k_h, const void* v_h, float* 
 int ringattn_host_workspace_bytes(int S, int Hq, int Hkv, int d, long long* bytes);
 
 /*
+ * ringattn_relayout -- the data movement of one Ulysses all-to-all, every virtual rank
+ * on this GPU ("Ring Attention and Ulysses shard a sequence two different ways...",
+ * section "Ulysses: an all-to-all relayout instead of a rotation": an all-to-all swaps
+ * the sequence-sharded layout for a head-sharded one, and back after attention).
+ *   sequence-sharded: [S, H, row] -- tokens in rank-major order (rank r's tokens are its
+ *       chunk for `layout`: contiguous chunk r, or zigzag chunks r then 2c-1-r), heads
+ *       inner: each rank's shard is its tokens with every head, as an activation is held;
+ *   head-sharded:     [H, S, row] -- heads outer, tokens in natural order: rank r's share
+ *       is heads [r*H/c, (r+1)*H/c) over the whole sequence.
+ * to_heads = 1 moves src (sequence-sharded) to dst (head-sharded); 0 the reverse.  A row
+ * is one (token, head) vector of row_bytes bytes.  Bit-exact copy; every dst byte is
+ * written.  src and dst must not overlap.
+ * Requires row_bytes a multiple of 4 and 4-byte aligned src, dst (16-byte rows on
+ * 16-byte aligned buffers move as 16-byte vectors), S a multiple of the chunk count,
+ * (S/chunks) * H * row_bytes/4 < 2^31 and H * chunks < 65536 (else RA_ERR_UNSUPPORTED).
+ */
+int ringattn_relayout(const void* src, void* dst, int S, int H, int row_bytes, int c, int layout,
+                      int to_heads, ra_stream_t stream);
+
+/*
+ * ringattn_ulysses_fwd -- attention by Ulysses' scheme, every virtual rank on this GPU
+ * (same page and section as ringattn_relayout): relayout q, k, v from sequence shards to
+ * head shards, attend every rank's heads over the whole sequence (one launch of the fused
+ * kernel for all ranks, natural order, no ring), relayout out and lse back.  The result
+ * is the same attention as ringattn_fwd's, in the sequence-sharded layout.
+ * q_seq: [S, Hq, d] bf16, k_seq, v_seq: [S, Hkv, d] bf16, out_seq: [S, Hq, d] fp32,
+ *     lse_seq: [S, Hq] fp32 -- all sequence-sharded (rank-major tokens, heads inner).
+ * Rank r takes query heads [r*Hq/c, (r+1)*Hq/c), so Hq % c == 0; it uses the KV heads of
+ * those query heads (h / (Hq/Hkv)), which puts one KV head on c/Hkv ranks when c > Hkv
+ * (on one GPU each KV head is stored once).
+ * workspace: DEVICE, at least ringattn_host_workspace_bytes(S, Hq, Hkv, d) bytes,
+ *     256-byte aligned, caller-owned: it holds the head-sharded q, k, v, out, lse.
+ * Requires d in {64, 128}, S a multiple of 128 and of the chunk count, 16-byte aligned
+ * q_seq, k_seq, v_seq, out_seq and 4-byte aligned lse_seq.
+ */
+int ringattn_ulysses_fwd(const void* q_seq, const void* k_seq, const void* v_seq, float* out_seq,
+                         float* lse_seq, int S, int Hq, int Hkv, int d, int c, int causal, int layout,
+                         void* workspace, long long workspace_bytes, ra_stream_t stream);
+
+/*
  * ringattn_fwd_natural -- as ringattn_fwd, but q, k, v, out and lse are in NATURAL
  * sequence order: the zigzag/contiguous chunk map is applied in the kernel's tile
  * addressing, so no permutation pass is needed.  Same result, same requirements.

@@ -425,6 +425,67 @@ int ringattn_fwd_host(const void* q_h, const void* k_h, const void* v_h, float* 
                     static_cast<size_t>(workspace_bytes), reinterpret_cast<cudaStream_t>(stream));
 }
 
+int ringattn_relayout(const void* src, void* dst, int S, int H, int row_bytes, int c, int layout, int to_heads,
+                      ra_stream_t stream) {
+    if (!src || !dst || src == dst) return RA_ERR_INVALID_ARG;
+    if (S < 1 || H < 1 || row_bytes < 1 || c < 1) return RA_ERR_INVALID_ARG;
+    if ((layout != 0 && layout != 1) || (to_heads != 0 && to_heads != 1)) return RA_ERR_INVALID_ARG;
+    if (S % (c * (layout == 1 ? 2 : 1)) != 0) return RA_ERR_INVALID_ARG;
+    if (((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 3u) != 0) return RA_ERR_INVALID_ARG;
+    if (!ra::relayout_fits(S, H, row_bytes, c, layout)) return RA_ERR_UNSUPPORTED;
+    const long long bytes = static_cast<long long>(H) * S * row_bytes;
+    const char* a = static_cast<const char*>(src);
+    const char* b = static_cast<const char*>(dst);
+    if (a < b + bytes && b < a + bytes) return RA_ERR_INVALID_ARG;  // overlapping buffers
+    DeviceInfo* dev = nullptr;
+    int st = device_info(&dev);
+    if (st != RA_OK) return st;
+    return ra::launch_relayout(src, dst, S, H, row_bytes, c, layout, to_heads, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ringattn_ulysses_fwd(const void* q_seq, const void* k_seq, const void* v_seq, float* out_seq, float* lse_seq,
+                         int S, int Hq, int Hkv, int d, int c, int causal, int layout, void* workspace,
+                         long long workspace_bytes, ra_stream_t stream) {
+    if (!q_seq || !k_seq || !v_seq || !out_seq || !lse_seq || !workspace) return RA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < 0) return RA_ERR_INVALID_ARG;
+    if (!aligned16(q_seq) || !aligned16(k_seq) || !aligned16(v_seq) || !aligned16(out_seq) ||
+        (reinterpret_cast<uintptr_t>(lse_seq) & 3u) != 0)
+        return RA_ERR_INVALID_ARG;
+    if (c < 1 || Hq < 1 || Hq % c != 0) return RA_ERR_INVALID_ARG;  // each rank gets Hq/c query heads
+    // the sequence shards: the ring's chunking for (c, layout) (no messages: kv_block 1)
+    ra::Ring R;
+    int st = make_ring(S, Hq, Hkv, d, c, causal, layout, 1, &R);
+    if (st != RA_OK) return st;
+    // the attention: every rank's heads over the whole sequence (c = 1 in the kernel)
+    if ((st = make_ring(S, Hq, Hkv, d, 1, causal, 0, S, &R)) != RA_OK) return st;
+    if (d != 64 && d != 128) return RA_ERR_UNSUPPORTED;
+    if (S % 128 != 0) return RA_ERR_UNSUPPORTED;
+    if (!ra::relayout_fits(S, Hq, 4 * d, c, layout) || !ra::relayout_fits(S, Hkv, 2 * d, c, layout))
+        return RA_ERR_UNSUPPORTED;
+    long long off[6];
+    host_workspace_layout(S, Hq, Hkv, d, off);
+    if (workspace_bytes < off[5]) return RA_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != RA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    void *qh = ws + off[0], *kh = ws + off[1], *vh = ws + off[2];
+    float* oh = reinterpret_cast<float*>(ws + off[3]);
+    float* lh = reinterpret_cast<float*>(ws + off[4]);
+    // all-to-all: sequence shards -> head shards
+    if (ra::launch_relayout(q_seq, qh, S, Hq, 2 * d, c, layout, 1, s) != 0 ||
+        ra::launch_relayout(k_seq, kh, S, Hkv, 2 * d, c, layout, 1, s) != 0 ||
+        ra::launch_relayout(v_seq, vh, S, Hkv, 2 * d, c, layout, 1, s) != 0)
+        return RA_ERR_CUDA;
+    // local attention of every rank's heads over the whole sequence, one launch for all ranks
+    if ((st = fwd_bf16(qh, kh, vh, oh, lh, S, Hq, Hkv, d, 1, causal, 0, S, 1, -1, 0, -1, s)) != RA_OK) return st;
+    // all-to-all back: head shards -> sequence shards
+    if (ra::launch_relayout(oh, out_seq, S, Hq, 4 * d, c, layout, 0, s) != 0 ||
+        ra::launch_relayout(lh, lse_seq, S, Hq, 4, c, layout, 0, s) != 0)
+        return RA_ERR_CUDA;
+    return RA_OK;
+}
+
 int ringattn_fwd_natural(const void* q, const void* k, const void* v, float* out, float* lse, int S, int Hq,
                          int Hkv, int d, int c, int causal, int layout, int kv_block, ra_stream_t stream) {
     return fwd_bf16(q, k, v, out, lse, S, Hq, Hkv, d, c, causal, layout, kv_block, 1, -1, 0, -1,

@@ -61,6 +61,11 @@ int launch_merge(float* o_run, float* lse_run, const float* o_part, const float*
                  int d, cudaStream_t stream);
 int launch_selftest_timeout(int* err, unsigned long long timeout_ns, cudaStream_t stream);
 int launch_doc_start(const int* doc_id, int* doc_start, int S, cudaStream_t stream);
+// Ulysses relayout between sequence-sharded [S, H, row] (rank-major tokens) and
+// head-sharded [H, S, row] (natural tokens); relayout_fits checks the index ranges.
+bool relayout_fits(long long S, int H, int row_bytes, int c, int layout);
+int launch_relayout(const void* src, void* dst, int S, int H, int row_bytes, int c, int layout, int to_heads,
+                    cudaStream_t stream);
 
 // Shared-memory footprint of the bf16 kernel for head dimension d.
 size_t attn_bf16_smem_bytes(int d);

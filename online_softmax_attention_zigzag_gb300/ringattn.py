@@ -30,7 +30,7 @@ EXPORTS = (
     "ringattn_fwd_hop_f32", "ringattn_merge", "ringattn_permute", "ringattn_rank_work",
     "ringattn_sync_status", "ringattn_selftest_timeout", "ringattn_strerror", "ringattn_last_timeout",
     "ringattn_fwd_rank", "ringattn_fwd_docmask", "ringattn_fwd_docmask_noalloc",
-    "ringattn_fwd_host", "ringattn_host_workspace_bytes",
+    "ringattn_fwd_host", "ringattn_host_workspace_bytes", "ringattn_relayout", "ringattn_ulysses_fwd",
 )
 
 # Longest sequence ringattn_fwd_docmask_noalloc takes (its static scratch, int32 [S]).
@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
             "ringattn_fwd_docmask_noalloc": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P],
             "ringattn_fwd_host": _ATTN + [_P, _LL, _P],
             "ringattn_host_workspace_bytes": [_I, _I, _I, _I, _P],
+            "ringattn_relayout": [_P, _P, _I, _I, _I, _I, _I, _I, _P],
+            "ringattn_ulysses_fwd": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _LL, _P],
             "ringattn_fwd_f32": _ATTN + [_P],
             "ringattn_fwd_hop": _ATTN + [_I, _I, _P],
             "ringattn_fwd_hop_f32": _ATTN + [_I, _I, _P],
@@ -205,6 +207,40 @@ def fwd_host(q_h, k_h, v_h, out_h, lse_h, workspace, *, c, causal, layout, kv_bl
     _check("ringattn_fwd_host", lib().ringattn_fwd_host(
         *ptrs, S, Hq, Hkv, d, c, causal, layout, kv_block, ws, workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+def relayout(src, dst, *, c, layout, to_heads, stream=None) -> None:
+    """ringattn_relayout: to_heads=1 moves sequence-sharded [S, H, ...] (rank-major tokens)
+    to head-sharded [H, S, ...] (natural tokens); to_heads=0 the reverse."""
+    if src.dtype != dst.dtype or src.numel() != dst.numel():
+        raise ValueError("src and dst must have the same dtype and size")
+    if src.dim() < 2 or dst.dim() < 2:
+        raise ValueError("src and dst must be at least [S, H] / [H, S]")
+    S, H = (src.shape[0], src.shape[1]) if to_heads else (src.shape[1], src.shape[0])
+    if (tuple(dst.shape[:2]) != ((H, S) if to_heads else (S, H))) or dst.shape[2:] != src.shape[2:]:
+        raise ValueError("dst must be src with its first two axes swapped")
+    row_bytes = src.element_size() * (src.numel() // max(1, H * S))
+    _check("ringattn_relayout", lib().ringattn_relayout(
+        _dev(src, "src"), _dev(dst, "dst"), S, H, row_bytes, c, layout, int(to_heads), _stream(stream)))
+
+
+def ulysses_fwd(q_seq, k_seq, v_seq, out_seq, lse_seq, workspace, *, c, causal, layout, stream=None) -> None:
+    """ringattn_ulysses_fwd: sequence-sharded q [S, Hq, d], k, v [S, Hkv, d] bf16 in;
+    out [S, Hq, d], lse [S, Hq] fp32 out; workspace a CUDA uint8 tensor of at least
+    :func:`host_workspace_bytes` (S, Hq, Hkv, d)."""
+    if q_seq.dim() != 3 or k_seq.dim() != 3 or v_seq.dim() != 3:
+        raise ValueError("q, k, v must be [S, H, d]")
+    S, Hq, d = q_seq.shape
+    Hkv = k_seq.shape[1]
+    if tuple(k_seq.shape) != (S, Hkv, d) or tuple(v_seq.shape) != (S, Hkv, d):
+        raise ValueError("k and v must be [S, Hkv, d] with q's S and d")
+    if tuple(out_seq.shape) != (S, Hq, d) or tuple(lse_seq.shape) != (S, Hq):
+        raise ValueError("out must be [S, Hq, d] and lse [S, Hq]")
+    ptrs = [_dev(q_seq, "q", torch.bfloat16), _dev(k_seq, "k", torch.bfloat16), _dev(v_seq, "v", torch.bfloat16),
+            _dev(out_seq, "out", torch.float32), _dev(lse_seq, "lse", torch.float32)]
+    _check("ringattn_ulysses_fwd", lib().ringattn_ulysses_fwd(
+        *ptrs, S, Hq, Hkv, d, c, causal, layout, _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def fwd_natural(q, k, v, out, lse, *, c, causal, layout, kv_block, stream=None) -> None:
