@@ -31,6 +31,10 @@ numpy).  Each function names the passage it follows:
   rank's heads in between ("Ring Attention and Ulysses shard a sequence two
   different ways...", section "Ulysses: an all-to-all relayout instead of a
   rotation").
+* :mod:`oracle.backward` -- the exact gradient of that attention with respect
+  to q, k and v, and the ring's backward (KV blocks travel with their dK, dV
+  accumulators); the pages give only the forward, so the gradient is the
+  definition.
 
 Every function is pinned by ``tests/test_oracle_*.py`` against closed forms,
 brute force, library routines it does not call, or values the pages print.

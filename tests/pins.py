@@ -404,3 +404,86 @@ def pin_ulysses_attention(ulysses_fn):
         assert o.shape == (S, Hq, d) and l.shape == (S, Hq)
         assert np.abs(o - seq(to)).max() < 1e-10, "Ulysses out differs from attention"
         assert np.abs(l - tl.T[order]).max() < 1e-10, "Ulysses lse differs from logsumexp"
+
+
+# --------------------------------------------------------------------------- backward
+
+def _torch_grads(q, k, v, dout, causal):
+    """float64 autograd through torch SDPA (scale 1, GQA by repeating KV heads)."""
+    g = q.shape[0] // k.shape[0]
+    tq, tk, tv = (torch.from_numpy(np.array(x)).requires_grad_(True) for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(
+        tq[None], tk.repeat_interleave(g, dim=0)[None], tv.repeat_interleave(g, dim=0)[None],
+        is_causal=causal, scale=1.0)[0]
+    o.backward(torch.from_numpy(np.array(dout)))
+    return tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy()
+
+
+def pin_grad_vs_autograd(grad_fn):
+    for causal in (False, True):
+        for (Hq, Hkv, S, d, seed) in ((2, 2, 19, 4, 31), (8, 2, 24, 8, 32), (3, 1, 9, 5, 33)):
+            q, k, v = rand((Hq, S, d), seed), rand((Hkv, S, d), seed + 1), rand((Hkv, S, d), seed + 2)
+            do = rand((Hq, S, d), seed + 3)
+            got = grad_fn(q, k, v, do, causal)
+            want = _torch_grads(q, k, v, do, causal)
+            for name, a, b in zip(("dq", "dk", "dv"), got, want):
+                assert np.abs(a - b).max() < 1e-10, f"{name} differs from torch autograd"
+
+
+def pin_grad_finite_differences(grad_fn):
+    """Central differences of sum(out * dout), the forward done by the pure-Python brute
+    force, on a tiny GQA case."""
+    Hq, Hkv, S, d = 2, 1, 5, 3
+    q, k, v, do = rand((Hq, S, d), 41), rand((Hkv, S, d), 42), rand((Hkv, S, d), 43), rand((Hq, S, d), 44)
+    for causal in (False, True):
+        dq, dk, dv = grad_fn(q, k, v, do, causal)
+
+        def loss(qq, kk, vv):
+            o, _ = brute_force(qq, kk, vv, causal)
+            return float((o * do).sum())
+
+        eps = 1e-6
+        for name, x, gx in (("dq", q, dq), ("dk", k, dk), ("dv", v, dv)):
+            for idx in np.ndindex(*x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += eps
+                xm[idx] -= eps
+                args_p = [xp if y is x else y for y in (q, k, v)]
+                args_m = [xm if y is x else y for y in (q, k, v)]
+                fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+                assert abs(fd - gx[idx]) < 1e-7, f"{name}{idx} differs from finite differences"
+
+
+def pin_grad_closed_forms(grad_fn):
+    Hq, Hkv, S, d = 2, 1, 10, 4
+    q, k, v, do = rand((Hq, S, d), 51), rand((Hkv, S, d), 52), rand((Hkv, S, d), 53), rand((Hq, S, d), 54)
+    for causal in (False, True):
+        # no gradient flowing in: nothing flows out
+        for gx in grad_fn(q, k, v, np.zeros_like(do), causal):
+            assert np.abs(gx).max() == 0.0, "dout = 0 must give zero gradients"
+        # the same value at every key: out does not depend on the scores
+        dq, dk, dv = grad_fn(q, k, np.tile(v[:, :1], (1, S, 1)), do, causal)
+        assert np.abs(dq).max() < 1e-12 and np.abs(dk).max() < 1e-12, "constant V must give dq = dk = 0"
+        # uniform weights (q = 0): dv_j = sum over the rows that see j of dout_i / |A(i)|
+        _, _, dv = grad_fn(np.zeros_like(q), k, v, do, causal)
+        for j in range(S):
+            rows = range(j, S) if causal else range(S)
+            want = sum(do[h, i] / ((i + 1) if causal else S) for h in range(Hq) for i in rows)
+            assert np.abs(dv[0, j] - want).max() < 1e-12, "q = 0 dv is not the weighted dout sum"
+    # causal row 0 sees one key with weight 1: its dq is exactly zero
+    dq, _, _ = grad_fn(q, k, v, do, True)
+    assert np.abs(dq[:, 0]).max() < 1e-12, "causal row 0 must have dq = 0"
+
+
+def pin_ring_backward(ring_grad_fn, grad_fn):
+    cases = [
+        # (Hq, Hkv, S, d, c, layout, causal, kv_block)
+        (2, 2, 16, 4, 2, 1, True, 2), (4, 2, 24, 3, 3, 1, True, 4), (2, 1, 12, 5, 3, 0, False, 2),
+        (2, 2, 16, 4, 4, 0, True, 4), (4, 4, 32, 2, 2, 1, False, 8),
+    ]
+    for (Hq, Hkv, S, d, c, lay, causal, kvb) in cases:
+        seed = S + c
+        q, k, v = rand((Hq, S, d), seed), rand((Hkv, S, d), seed + 1), rand((Hkv, S, d), seed + 2)
+        do = rand((Hq, S, d), seed + 3)
+        for a, b in zip(ring_grad_fn(q, k, v, do, c, lay, causal, kvb), grad_fn(q, k, v, do, causal)):
+            assert np.abs(a - b).max() < 1e-12, "ring backward differs from the full gradient"

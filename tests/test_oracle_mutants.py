@@ -258,3 +258,55 @@ def test_ulysses_attention_mutants_caught():
     with pytest.raises(AssertionError):
         pins.pin_ulysses_attention(wrong_heads)
     pins.pin_ulysses_attention(ulysses.ulysses_attention)
+
+
+# ---------------------------------------------------------------- backward mutants
+
+def _grad(q, k, v, dout, causal, *, flip=False, no_delta=False, dk_untransposed=False, overwrite=False):
+    from oracle import backward as ob
+    q, k, v, dout = (np.asarray(x, float) for x in (q, k, v, dout))
+    Hq, S, d = q.shape
+    g = Hq // k.shape[0]
+    dq = np.zeros_like(q); dk = np.zeros_like(k); dv = np.zeros_like(v)
+    for h in range(Hq):
+        hk = h // g
+        P, _ = ob._probs(q[h], k[hk], causal)
+        D = 0.0 if no_delta else np.einsum("sd,sd->s", dout[h], P @ v[hk])[:, None]
+        dP = dout[h] @ v[hk].T
+        dS = P * ((D - dP) if flip else (dP - D))
+        dq[h] = dS @ k[hk]
+        t = (dS @ q[h]) if dk_untransposed else (dS.T @ q[h])
+        if overwrite:
+            dk[hk] = t
+            dv[hk] = P.T @ dout[h]
+        else:
+            dk[hk] += t
+            dv[hk] += P.T @ dout[h]
+    return dq, dk, dv
+
+
+GRAD_MUTANTS = {
+    "dS_sign_flipped": dict(flip=True),
+    "delta_dropped": dict(no_delta=True),
+    "dK_not_transposed": dict(dk_untransposed=True),
+    "gqa_grads_overwritten": dict(overwrite=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(GRAD_MUTANTS))
+def test_grad_mutant_caught(name):
+    kw = GRAD_MUTANTS[name]
+    fn = lambda q, k, v, do, causal: _grad(q, k, v, do, causal, **kw)  # noqa: E731
+    failures = 0
+    for pin in (pins.pin_grad_vs_autograd, pins.pin_grad_closed_forms):
+        try:
+            pin(fn)
+        except AssertionError:
+            failures += 1
+    assert failures > 0, f"mutant {name} passed every pin"
+
+
+def test_grad_unmutated_copy_passes():
+    fn = lambda q, k, v, do, causal: _grad(q, k, v, do, causal)  # noqa: E731
+    pins.pin_grad_vs_autograd(fn)
+    pins.pin_grad_closed_forms(fn)

@@ -124,3 +124,42 @@ def test_ulysses_kv_heads_replicate_when_ranks_outnumber_them():
     # 8 query heads over 2 KV heads on 4 ranks: ranks 0-1 need KV head 0, ranks 2-3 KV head 1
     assert [list(ulysses.kv_heads(8, 2, 4, r)) for r in range(4)] == [[0], [0], [1], [1]]
     assert [list(ulysses.kv_heads(8, 4, 2, r)) for r in range(2)] == [[0, 1], [2, 3]]
+
+
+def test_backward_vs_torch_autograd():
+    from oracle import backward
+    pins.pin_grad_vs_autograd(backward.attention_grad)
+
+
+def test_backward_vs_finite_differences():
+    from oracle import backward
+    pins.pin_grad_finite_differences(backward.attention_grad)
+
+
+def test_backward_closed_forms():
+    from oracle import backward
+    pins.pin_grad_closed_forms(backward.attention_grad)
+
+
+def test_ring_backward_is_the_gradient():
+    from oracle import backward
+    pins.pin_ring_backward(backward.ring_backward, backward.attention_grad)
+
+
+def test_backward_abs_sums_bound_the_gradients():
+    from oracle import backward
+    rng = np.random.default_rng(5)
+    q, k, v, do = (rng.standard_normal(s) for s in ((4, 20, 3), (2, 20, 3), (2, 20, 3), (4, 20, 3)))
+    for causal in (False, True):
+        for g, a in zip(backward.attention_grad(q, k, v, do, causal), backward.grad_abs_sums(q, k, v, do, causal)):
+            assert (np.abs(g) <= a + 1e-12).all() and (a >= 0).all()
+
+
+def test_backward_dq_rows_match_whole():
+    from oracle import backward
+    rng = np.random.default_rng(9)
+    q, k, v, do = (rng.standard_normal(s) for s in ((4, 30, 5), (2, 30, 5), (2, 30, 5), (4, 30, 5)))
+    heads, posn = np.array([0, 3, 1, 2, 3]), np.array([0, 29, 7, 15, 1])
+    for causal in (False, True):
+        dq, _, _ = backward.attention_grad(q, k, v, do, causal)
+        assert np.abs(backward.dq_rows(q, k, v, do, heads, posn, causal) - dq[heads, posn]).max() < 1e-12
