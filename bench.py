@@ -56,6 +56,8 @@ def parse():
                     help="skip the 128k workload and the natural-order step measured beside the headline")
     ap.add_argument("--per-hop-sweep", action="store_true",
                     help="instead of the headline: fused vs per-hop + merge over the workload's kv_block sweep")
+    ap.add_argument("--backward", action="store_true",
+                    help="instead of the headline: the backward pass (ringattn_bwd) on the workload")
     ap.add_argument("--ulysses", action="store_true",
                     help="instead of the headline: Ulysses on one GPU (relayouts + attention) on the workload")
     ap.add_argument("--attention-only", action="store_true",
@@ -303,6 +305,39 @@ def ulysses_only(ra, w, dev, stream, reps, peak, hbm_peak):
                            "GB/s": qbytes / (ms_q * 1e-3) / 1e9, "frac": qbytes / (ms_q * 1e-3) / 1e9 / hbm_peak}}
 
 
+def backward_only(ra, w, dev, stream, reps, peak):
+    """ringattn_bwd on workload w (rank-major device tensors, the forward's out and lse):
+    TFLOP/s of the whole call (delta, dq and dk/dv kernels) with the backward counted as
+    2.5 forward passes (five tile products of 2*d FLOP per visible pair against two)."""
+    q_h, k_h, v_h = make_qkv(w)
+    g = torch.Generator().manual_seed(221)
+    do_h = torch.randn((w.bhq, w.seq, w.d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    t = []
+    for x in (q_h, k_h, v_h, do_h):
+        xd = x.to(dev)
+        xr = torch.empty_like(xd)
+        ra.permute(xd, xr, c=w.c, layout=w.layout, inverse=0)
+        t.append(xr)
+        del xd
+    qr, kr, vr, dor = t
+    o = torch.empty((w.bhq, w.seq, w.d), dtype=torch.float32, device=dev)
+    l = torch.empty((w.bhq, w.seq), dtype=torch.float32, device=dev)
+    kw = dict(c=w.c, causal=w.causal, layout=w.layout, kv_block=w.kv_block)
+    ra.fwd(qr, kr, vr, o, l, **kw)
+    dq = torch.empty_like(o)
+    dk = torch.empty((w.bhkv, w.seq, w.d), dtype=torch.float32, device=dev)
+    dv = torch.empty_like(dk)
+    delta = torch.empty_like(l)
+    ms = time_events(lambda: ra.bwd(qr, kr, vr, o, l, dor, dq, dk, dv, delta, **kw), reps, stream)
+    if ra.sync_status() != ra.RA_OK:
+        raise SystemExit("device wait timed out")
+    flop = 2.5 * w.flops()
+    tf = flop / (ms * 1e-3) / 1e12
+    return {"workload": w.name, "mode": "backward (ringattn_bwd: delta, dq, dk/dv kernels)", "ms": ms,
+            "achieved": tf, "unit": "TFLOP/s", "peak": peak, "frac": tf / peak,
+            "flop": "2.5 x the causal-adjusted forward FLOP"}
+
+
 def per_hop_sweep(ra, w, dev, stream):
     """Fused kernel vs the ring-faithful per-hop path (one partial per message, folded in
     with the merge kernel) for each kv_block of the workload's sweep."""
@@ -394,6 +429,12 @@ def main():
         if rank == 0:
             print(json.dumps({"metric": METRIC, "unit": UNIT, "mode": "per-hop sweep", "workload": w.name,
                               "sweep": res}), flush=True)
+        return
+    if args.backward:
+        dev = torch.device("cuda", local)
+        res = backward_only(ra, w, dev, torch.cuda.current_stream(dev), max(1, args.steps), peaks()[0])
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "unit": UNIT, **res}), flush=True)
         return
     if args.ulysses:
         dev = torch.device("cuda", local)

@@ -227,6 +227,28 @@ int ringattn_ulysses_fwd(const void* q_seq, const void* k_seq, const void* v_seq
                          void* workspace, long long workspace_bytes, ra_stream_t stream);
 
 /*
+ * ringattn_bwd -- gradients of ringattn_fwd with respect to q, k and v (bf16 in, fp32 out).
+ * The pages give no backward pass (the training FLOP count of "Interrogating parallelism,
+ * part 5" implies one); this computes the exact gradient of the forward's attention:
+ * with P_ij = exp(q_i . k_j - lse_i) over visible keys, D_i = dout_i . out_i and
+ * dS_ij = P_ij (dout_i . v_j - D_i):
+ *     dq_i = sum_j dS_ij k_j,   dk_j = sum_i dS_ij q_i,   dv_j = sum_i P_ij dout_i,
+ * a KV head summing over the query heads that use it.  The ring order is kept: each query
+ * tile meets the KV blocks hop by hop, and each KV block travels the ring with its dk, dv
+ * accumulators (only the order of fp32 sums depends on it).  P and dS are rounded to bf16
+ * for the tensor-core products; all sums are fp32.
+ * q, k, v, dout: bf16, rank-major as in ringattn_fwd (dout: [Hq, S, d]).
+ * out, lse: ringattn_fwd's outputs for these q, k, v (fp32, rank-major).
+ * dq: [Hq, S, d], dk, dv: [Hkv, S, d] fp32, rank-major, fully overwritten.
+ * delta: [Hq, S] fp32 DEVICE scratch owned by the caller; overwritten with D.
+ * Requirements as ringattn_fwd (d in {64, 128}, chunks and kv_block multiples of 128,
+ * Hq % Hkv == 0), every pointer 16-byte aligned.
+ */
+int ringattn_bwd(const void* q, const void* k, const void* v, const float* out, const float* lse,
+                 const void* dout, float* dq, float* dk, float* dv, float* delta, int S, int Hq,
+                 int Hkv, int d, int c, int causal, int layout, int kv_block, ra_stream_t stream);
+
+/*
  * ringattn_fwd_natural -- as ringattn_fwd, but q, k, v, out and lse are in NATURAL
  * sequence order: the zigzag/contiguous chunk map is applied in the kernel's tile
  * addressing, so no permutation pass is needed.  Same result, same requirements.

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libringattn.so")
-SOURCES = ["api.cu", "attn_bf16.cu", "attn_f32.cu", "permute_merge.cu", "ulysses.cu"]
+SOURCES = ["api.cu", "attn_bf16.cu", "attn_f32.cu", "permute_merge.cu", "ulysses.cu", "attn_bwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

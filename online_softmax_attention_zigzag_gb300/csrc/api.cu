@@ -486,6 +486,44 @@ int ringattn_ulysses_fwd(const void* q_seq, const void* k_seq, const void* v_seq
     return RA_OK;
 }
 
+int ringattn_bwd(const void* q, const void* k, const void* v, const float* out, const float* lse, const void* dout,
+                 float* dq, float* dk, float* dv, float* delta, int S, int Hq, int Hkv, int d, int c, int causal,
+                 int layout, int kv_block, ra_stream_t stream) {
+    if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !delta) return RA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) || !aligned16(dout) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(delta))
+        return RA_ERR_INVALID_ARG;
+    ra::Ring R;
+    int st = make_ring(S, Hq, Hkv, d, c, causal, layout, kv_block, &R);
+    if (st != RA_OK) return st;
+    if (d != 64 && d != 128) return RA_ERR_UNSUPPORTED;
+    if (R.m % 128 != 0 || kv_block % 128 != 0) return RA_ERR_UNSUPPORTED;
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != RA_OK) return st;
+    if ((st = get_encoder()) != RA_OK) return st;
+    ra::AttnBwdParams p;
+    p.ring = R;
+    p.natural = 0;
+    p.n_tiles = S / 128;
+    p.n_items = 0;
+    p.lse = lse;
+    p.delta = delta;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.err = dev->err;
+    p.timeout_ns = wait_timeout_ns();
+    CUtensorMap tq, tk, tv, tdo;
+    if (encode_bf16_map(&tq, q, static_cast<long long>(Hq) * S, d) != RA_OK ||
+        encode_bf16_map(&tk, k, static_cast<long long>(Hkv) * S, d) != RA_OK ||
+        encode_bf16_map(&tv, v, static_cast<long long>(Hkv) * S, d) != RA_OK ||
+        encode_bf16_map(&tdo, dout, static_cast<long long>(Hq) * S, d) != RA_OK)
+        return RA_ERR_CUDA;
+    return ra::launch_attn_bwd(p, out, dout, tq, tk, tv, tdo, dev->sms, reinterpret_cast<cudaStream_t>(stream)) == 0
+               ? RA_OK
+               : RA_ERR_CUDA;
+}
+
 int ringattn_fwd_natural(const void* q, const void* k, const void* v, float* out, float* lse, int S, int Hq,
                          int Hkv, int d, int c, int causal, int layout, int kv_block, ra_stream_t stream) {
     return fwd_bf16(q, k, v, out, lse, S, Hq, Hkv, d, c, causal, layout, kv_block, 1, -1, 0, -1,

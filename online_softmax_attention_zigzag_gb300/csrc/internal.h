@@ -42,6 +42,21 @@ struct AttnBf16Params {
     unsigned long long timeout_ns;
 };
 
+// Backward pass (attn_bwd.cu): gradients of the fused forward, in the forward's layout.
+struct AttnBwdParams {
+    Ring ring;
+    int natural;       // 1: tensors in natural order
+    int n_tiles;       // 128-row tiles per head (S / 128)
+    int n_items;       // dq kernel: Hq * n_tiles; dk/dv kernel: Hkv * n_tiles
+    const float* lse;  // [Hq, S] natural log, from the forward
+    const float* delta;  // [Hq, S] dout . out per row (bwd_delta_kernel)
+    float* dq;
+    float* dk;
+    float* dv;
+    int* err;
+    unsigned long long timeout_ns;
+};
+
 struct AttnF32Params {
     Ring ring;
     int kv_block;
@@ -65,6 +80,10 @@ int launch_doc_start(const int* doc_id, int* doc_start, int S, cudaStream_t stre
 // head-sharded [H, S, row] (natural tokens); relayout_fits checks the index ranges.
 bool relayout_fits(long long S, int H, int row_bytes, int c, int layout);
 int launch_relayout(const void* src, void* dst, int S, int H, int row_bytes, int c, int layout, int to_heads,
+                    cudaStream_t stream);
+
+int launch_attn_bwd(const AttnBwdParams& p, const float* out, const void* dout, const CUtensorMap& tq,
+                    const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo, int sms,
                     cudaStream_t stream);
 
 // Shared-memory footprint of the bf16 kernel for head dimension d.

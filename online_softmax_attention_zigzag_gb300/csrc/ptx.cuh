@@ -130,6 +130,14 @@ __device__ __forceinline__ void st_stream_f4(float4* dst, float4 v, uint64_t pol
                  "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "l"(policy)
                  : "memory");
 }
+// 1-D bulk copy global -> shared that completes `bytes` on `bar`; both addresses
+// 16-byte aligned and bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load_1d(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(smem_dst)),
+                 "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -31,6 +31,7 @@ EXPORTS = (
     "ringattn_sync_status", "ringattn_selftest_timeout", "ringattn_strerror", "ringattn_last_timeout",
     "ringattn_fwd_rank", "ringattn_fwd_docmask", "ringattn_fwd_docmask_noalloc",
     "ringattn_fwd_host", "ringattn_host_workspace_bytes", "ringattn_relayout", "ringattn_ulysses_fwd",
+    "ringattn_bwd",
 )
 
 # Longest sequence ringattn_fwd_docmask_noalloc takes (its static scratch, int32 [S]).
@@ -67,6 +68,7 @@ def lib() -> ctypes.CDLL:
             "ringattn_fwd_host": _ATTN + [_P, _LL, _P],
             "ringattn_host_workspace_bytes": [_I, _I, _I, _I, _P],
             "ringattn_relayout": [_P, _P, _I, _I, _I, _I, _I, _I, _P],
+            "ringattn_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P],
             "ringattn_ulysses_fwd": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _LL, _P],
             "ringattn_fwd_f32": _ATTN + [_P],
             "ringattn_fwd_hop": _ATTN + [_I, _I, _P],
@@ -241,6 +243,20 @@ def ulysses_fwd(q_seq, k_seq, v_seq, out_seq, lse_seq, workspace, *, c, causal, 
     _check("ringattn_ulysses_fwd", lib().ringattn_ulysses_fwd(
         *ptrs, S, Hq, Hkv, d, c, causal, layout, _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def bwd(q, k, v, out, lse, dout, dq, dk, dv, delta, *, c, causal, layout, kv_block, stream=None) -> None:
+    """ringattn_bwd: gradients of :func:`fwd` (rank-major tensors).  q, dout [Hq, S, d] and
+    k, v [Hkv, S, d] bf16; out [Hq, S, d], lse [Hq, S] fp32 from the forward; dq, dk, dv
+    fp32 like q, k, v; delta [Hq, S] fp32 scratch."""
+    ptrs, S, Hq, Hkv, d = _attn_args(q, k, v, out, lse, torch.bfloat16)
+    if tuple(dout.shape) != (Hq, S, d) or tuple(dq.shape) != (Hq, S, d):
+        raise ValueError("dout and dq must be [Hq, S, d]")
+    if tuple(dk.shape) != (Hkv, S, d) or tuple(dv.shape) != (Hkv, S, d) or tuple(delta.shape) != (Hq, S):
+        raise ValueError("dk, dv must be [Hkv, S, d] and delta [Hq, S]")
+    ptrs += [_dev(dout, "dout", torch.bfloat16), _dev(dq, "dq", torch.float32), _dev(dk, "dk", torch.float32),
+             _dev(dv, "dv", torch.float32), _dev(delta, "delta", torch.float32)]
+    _check("ringattn_bwd", lib().ringattn_bwd(*ptrs, S, Hq, Hkv, d, c, causal, layout, kv_block, _stream(stream)))
 
 
 def fwd_natural(q, k, v, out, lse, *, c, causal, layout, kv_block, stream=None) -> None:

@@ -131,15 +131,17 @@ def ring_backward(q, k, v, dout, c: int, lay: int, causal: bool, kv_block: int):
     return dq, dk, dv
 
 
-def dq_rows(q, k, v, dout, heads, positions, causal: bool):
+def dq_rows(q, k, v, dout, heads, positions, causal: bool, with_abs: bool = False):
     """dq at selected (query head, natural position) rows only: each row's gradient needs
-    only its own row of P (and its own D), so long sequences can be checked row by row."""
+    only its own row of P (and its own D), so long sequences can be checked row by row.
+    with_abs: also return sum_j |dS_ij| |k_j| per entry (as grad_abs_sums)."""
     heads = np.asarray(heads, dtype=np.int64)
     positions = np.asarray(positions, dtype=np.int64)
     Hq = q.shape[0]
     g = Hq // k.shape[0]
     d = q.shape[2]
     res = np.empty((len(heads), d))
+    res_abs = np.empty((len(heads), d))
     for h in np.unique(heads):
         idx = np.nonzero(heads == h)[0]
         qh, kh, vh, doh = (_f64(x[int(hh)]) for x, hh in ((q, h), (k, h // g), (v, h // g), (dout, h)))
@@ -152,4 +154,5 @@ def dq_rows(q, k, v, dout, heads, positions, causal: bool):
             D = doh[i] @ (P @ vh[:n_keys])
             dS = P * (vh[:n_keys] @ doh[i] - D)
             res[n] = dS @ kh[:n_keys]
-    return res
+            res_abs[n] = np.abs(dS) @ np.abs(kh[:n_keys])
+    return (res, res_abs) if with_abs else res

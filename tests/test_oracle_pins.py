@@ -163,3 +163,6 @@ def test_backward_dq_rows_match_whole():
     for causal in (False, True):
         dq, _, _ = backward.attention_grad(q, k, v, do, causal)
         assert np.abs(backward.dq_rows(q, k, v, do, heads, posn, causal) - dq[heads, posn]).max() < 1e-12
+        aq, _, _ = backward.grad_abs_sums(q, k, v, do, causal)
+        _, ra_ = backward.dq_rows(q, k, v, do, heads, posn, causal, with_abs=True)
+        assert np.abs(ra_ - aq[heads, posn]).max() < 1e-12
