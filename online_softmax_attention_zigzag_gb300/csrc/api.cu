@@ -75,11 +75,11 @@ int get_encoder() {
     return RA_OK;
 }
 
-// [rows, d] bf16 tensor, boxes of 128 rows x 64 columns, 128-byte swizzle.
-int encode_bf16_map(CUtensorMap* map, const void* base, long long rows, int d) {
+// [rows, d] bf16 tensor, boxes of box_rows rows x 64 columns, 128-byte swizzle.
+int encode_bf16_map(CUtensorMap* map, const void* base, long long rows, int d, int box_rows = 128) {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
-    cuuint32_t box[2] = {64, 128};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -514,10 +514,11 @@ int ringattn_bwd(const void* q, const void* k, const void* v, const float* out, 
     p.err = dev->err;
     p.timeout_ns = wait_timeout_ns();
     CUtensorMap tq, tk, tv, tdo;
-    if (encode_bf16_map(&tq, q, static_cast<long long>(Hq) * S, d) != RA_OK ||
-        encode_bf16_map(&tk, k, static_cast<long long>(Hkv) * S, d) != RA_OK ||
-        encode_bf16_map(&tv, v, static_cast<long long>(Hkv) * S, d) != RA_OK ||
-        encode_bf16_map(&tdo, dout, static_cast<long long>(Hq) * S, d) != RA_OK)
+    // the backward kernels move 64-row boxes (half tiles are their streaming unit)
+    if (encode_bf16_map(&tq, q, static_cast<long long>(Hq) * S, d, 64) != RA_OK ||
+        encode_bf16_map(&tk, k, static_cast<long long>(Hkv) * S, d, 64) != RA_OK ||
+        encode_bf16_map(&tv, v, static_cast<long long>(Hkv) * S, d, 64) != RA_OK ||
+        encode_bf16_map(&tdo, dout, static_cast<long long>(Hq) * S, d, 64) != RA_OK)
         return RA_ERR_CUDA;
     return ra::launch_attn_bwd(p, out, dout, tq, tk, tv, tdo, dev->sms, reinterpret_cast<cudaStream_t>(stream)) == 0
                ? RA_OK

@@ -12,22 +12,27 @@
 //
 // Three kernels, all on the caller's stream:
 //   * bwd_delta_kernel   D_i = dout_i . out_i, one warp per row (HBM-bound);
-//   * bwd_dq_kernel      one 128-row query tile per work item: per key tile
+//   * bwd_kernel<D, true>   (dq) one 128-row query tile per work item: per key tile
 //                        S = Q K^T and dP = dO V^T into TMEM, then dS (bf16) into TMEM,
 //                        then dQ += dS K with dS read from TMEM;
-//   * bwd_dkdv_kernel    one 128-row key tile per work item: per query tile
+//   * bwd_kernel<D, false>  (dk/dv) one 128-row key tile per work item: per query tile
 //                        S^T = K Q^T and dP^T = V dO^T, then P^T and dS^T (bf16) into
 //                        TMEM, then dV += P^T dO and dK += dS^T Q.
 // Splitting dq from dk/dv recomputes S and dP once more (7 tile products instead of 5)
 // but needs no atomics and gives a deterministic result.
 //
-// Each CTA is persistent: warps 0-7 compute (warpgroup h handles key or query columns
-// [64h, 64h+64) of the 128 x 128 tile, thread = TMEM lane = row), warp 8 issues the
-// MMAs (one thread), warp 9 the TMA loads (one thread).  Every operand form used here
+// Each CTA is persistent: warps 0-7 compute (warpgroup h handles columns [64h, 64h+64)
+// of the 128 x 128 tile product, thread = TMEM lane = row), warp 8 issues the MMAs (one
+// thread), warp 9 the TMA loads (one thread).  The compute warps copy S (S^T) and dP
+// (dP^T) from TMEM into registers and release those columns at once, so the next tile's
+// products run on the tensor cores while this tile's exponentials are computed; the
+// streamed operands move through separate shared-memory rings (three slots for the one
+// the next tile's first product needs, two for the other).  Every operand form used here
 // (both operands K-major from shared memory; A from TMEM with an MN-major B) is one the
-// forward kernel uses too.  TMEM: S [0,128), dP [128,256), accumulators from 256.  The
-// packed bf16 P / dS of column half h overwrite the first 32 columns of that half's own
-// S / dP columns, so the halves never touch each other's columns.
+// forward kernel uses too.
+//   dq TMEM:    S [0,128), dP [128,256), dQ [256, 256+D), dS in [384 + 64b, +64), b = j%2.
+//   dk/dv TMEM: S^T [0,128), dP^T [128,256), dV [256,384), dK [384,512); warpgroup h puts
+//               P^T in [128+64h, +32) and dS^T in [128+64h+32, +32) over its own dP^T.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -43,23 +48,18 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 256;
 
+// Shared memory of both kernels: two resident tiles (Q, dO or K, V), then ring A (three
+// slots: K for dq, Q for dk/dv) and ring B (two slots: V for dq, dO for dk/dv).
 template <int D>
 struct BwdCfg {
     static constexpr int kTileBytes = kTile * D * 2;  // one 128 x D bf16 tile
-    static constexpr int kBoxBytes = kTile * 64 * 2;  // one 128 x 64 TMA box
-    static constexpr int kBoxes = D / 64;
-    static constexpr int kStages = (D == 128) ? 2 : 4;
-    // dq kernel: Q, dO resident; stages of (K, V)
-    static constexpr int kDqStageBytes = 2 * kTileBytes;
-    static constexpr int kDqKVOff = 2 * kTileBytes;
-    static constexpr int kDqBarOff = kDqKVOff + kStages * kDqStageBytes;
-    // dk/dv kernel: K, V resident; stages of (Q, dO, lse[128], delta[128])
-    static constexpr int kKvStageBytes = 2 * kTileBytes + 1024;
-    static constexpr int kKvQOff = 2 * kTileBytes;
-    static constexpr int kKvBarOff = kKvQOff + kStages * kKvStageBytes;
-    static constexpr int kNumBars = 16 + 2 * kStages;
-    static constexpr int kDqSmem = kDqBarOff + kNumBars * 8 + 16 + 1024;  // + slack to align the base
-    static constexpr int kKvSmem = kKvBarOff + kNumBars * 8 + 16 + 1024;
+    static constexpr int kBoxBytes = kTile * 64 * 2;  // one 128-row, 64-column block
+    static constexpr int kSlotsA = 3, kSlotsB = 2;
+    static constexpr int kAOff = 2 * kTileBytes;
+    static constexpr int kBOff = kAOff + kSlotsA * kTileBytes;
+    static constexpr int kBarOff = kBOff + kSlotsB * kTileBytes;
+    static constexpr int kNumBars = 32;
+    static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;  // + slack to align the base
 };
 
 // Rank-major (or natural) row of natural position pos of head `head`.
@@ -187,29 +187,34 @@ __device__ __forceinline__ void issue_kk(uint32_t d_tmem, uint32_t a_base, uint3
     }
 }
 
-// D[tmem] (+)= A B: A (128 x 128, bf16 packed in TMEM by column halves: keys or queries
-// [64h, 64h+64) in columns a_col + 64h + [0, 32)), B (128 x D) from shared memory as an
-// MN-major operand (the tile's rows are the contraction index).
+// D[tmem] (+)= A B: A (128 x 128, bf16 packed in TMEM: columns [64h, 64h+64) of the
+// product in TMEM columns a_tmem + h * a_half + [0, 32)), B (128 x D) from shared memory
+// as an MN-major operand (the tile's rows are the contraction index).
 template <int D>
-__device__ __forceinline__ void issue_tm(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_base, bool accumulate) {
+__device__ __forceinline__ void issue_tm(uint32_t d_tmem, uint32_t a_tmem, uint32_t a_half, uint32_t b_base,
+                                         bool accumulate) {
     using C = BwdCfg<D>;
     constexpr uint32_t idesc = idesc_bf16(kTile, D, 1);
     const uint64_t bd = sdesc_sw128(b_base, C::kBoxBytes, 1024);
 #pragma unroll
     for (int kk = 0; kk < kTile / 16; ++kk) {
-        const uint32_t acol = (kk / 4) * 64 + (kk % 4) * 8;
+        const uint32_t acol = (kk / 4) * a_half + (kk % 4) * 8;
         mma_ts(d_tmem, a_tmem + acol, desc_add(bd, (kk * 16 * 128) >> 4), idesc,
                (accumulate || kk > 0) ? 1u : 0u);
     }
 }
 
-// Load a 128 x D bf16 tile (rows row..row+127) as D/64 boxes.
+// Load a 128 x D bf16 tile (rows row..row+127) as 64 x 64 boxes: 64-column block cb,
+// 64-row block rb at byte cb * 16384 + rb * 8192, the layout of one 128-byte-swizzled
+// K-major operand of 128 rows.
 template <int D>
 __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int row,
                                           uint64_t policy) {
-    using C = BwdCfg<D>;
 #pragma unroll
-    for (int bx = 0; bx < C::kBoxes; ++bx) tma_load_2d_hint(dst + bx * C::kBoxBytes, map, bar, bx * 64, row, policy);
+    for (int cb = 0; cb < D / 64; ++cb)
+#pragma unroll
+        for (int rb = 0; rb < 2; ++rb)
+            tma_load_2d_hint(dst + cb * 16384 + rb * 8192, map, bar, cb * 64, row + rb * 64, policy);
 }
 
 // 64 fp32 TMEM columns of this thread's lane, in two 32-column loads.
@@ -241,26 +246,89 @@ __device__ __forceinline__ void store_acc(uint32_t taddr, float* dst) {
     }
 }
 
-// ------------------------------------------------------------------ dq kernel
-// Barriers: 0 q_full (Q, dO landed), 1 q_empty (item's MMAs done with Q, dO), 2 s_full
-// (S, dP in TMEM), 3 ds_full (256 compute threads wrote dS), 4 acc_done (item's dQ
-// complete), 5 acc_free (256 threads read dQ out), 6 drain (abort only), then kv_full
-// and kv_empty per stage (K and V of one key tile).
-struct DqBars {
-    uint64_t *q_full, *q_empty, *s_full, *ds_full, *acc_done, *acc_free, *drain, *kv_full, *kv_empty;
-    __device__ DqBars(uint64_t* b, int stages)
-        : q_full(b), q_empty(b + 1), s_full(b + 2), ds_full(b + 3), acc_done(b + 4), acc_free(b + 5),
-          drain(b + 6), kv_full(b + 16), kv_empty(b + 16 + stages) {}
+// Barriers shared by both kernels' layouts (slot rings A: 3, B: 2).
+struct Bars {
+    uint64_t *res_full, *res_empty;  // resident tiles landed / item's MMAs done with them
+    uint64_t *s_full, *dp_full;      // S (S^T) / dP (dP^T) in TMEM
+    uint64_t *s_free, *dp_free;      // 256 compute threads copied S / dP out of TMEM
+    uint64_t *ds_full;               // [2] dq: dS buffer written; dk/dv: [0] P^T, dS^T written
+    uint64_t *acc_done, *acc_free, *drain;
+    uint64_t *a_full, *a_empty, *b_full, *b_empty;
+    __device__ explicit Bars(uint64_t* b)
+        : res_full(b), res_empty(b + 1), s_full(b + 2), dp_full(b + 3), s_free(b + 4), dp_free(b + 5),
+          ds_full(b + 6), acc_done(b + 8), acc_free(b + 9), drain(b + 10), a_full(b + 16), a_empty(b + 19),
+          b_full(b + 22), b_empty(b + 24) {}
 };
 
+__device__ __forceinline__ void init_bars(const Bars& b) {
+    mbar_init(b.res_full, 1);
+    mbar_init(b.res_empty, 1);
+    mbar_init(b.s_full, 1);
+    mbar_init(b.dp_full, 1);
+    mbar_init(b.s_free, 256);
+    mbar_init(b.dp_free, 256);
+    mbar_init(&b.ds_full[0], 256);
+    mbar_init(&b.ds_full[1], 256);
+    mbar_init(b.acc_done, 1);
+    mbar_init(b.acc_free, 256);
+    mbar_init(b.drain, 1);
+    for (int s = 0; s < 3; ++s) {
+        mbar_init(&b.a_full[s], 1);
+        mbar_init(&b.a_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+        mbar_init(&b.b_full[s], 1);
+        mbar_init(&b.b_empty[s], 1);
+    }
+}
+
+// Wait (one poller warp per warpgroup, the rest in the group's named barrier).
+__device__ __forceinline__ bool group_wait(uint64_t* bar, uint32_t parity, int h, int wq, const WaitCtl& wc) {
+    bool ok = true;
+    if (wq == 0) ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
+    return group_bar_and(h, ok);
+}
+
+// Copy 64 fp32 TMEM columns of this lane into registers, then release them.
+__device__ __forceinline__ void tmem_take64(uint32_t taddr, float (&v)[64], uint64_t* free_bar) {
+    tmem_ld64(taddr, v);
+    tc_fence_before();
+    mbar_arrive(free_bar);
+}
+
+// Loader helper: wait for slot `i % n` of a ring to be empty and load one tile into it.
+template <int D>
+__device__ __forceinline__ bool ring_load(uint8_t* ring, uint64_t* full, uint64_t* empty, uint32_t i, int n,
+                                          const CUtensorMap* map, int row, uint64_t policy, const WaitCtl& wc) {
+    using C = BwdCfg<D>;
+    const uint32_t s = i % n;
+    if (!mbar_wait(&empty[s], ((i / n) & 1u) ^ 1u, wc, 32)) return false;
+    mbar_arrive_expect_tx(&full[s], C::kTileBytes);
+    load_tile<D>(ring + s * C::kTileBytes, map, &full[s], row, policy);
+    return true;
+}
+
+__device__ __forceinline__ bool ring_wait(uint64_t* full, uint32_t i, int n, const WaitCtl& wc) {
+    return mbar_wait(&full[i % n], (i / n) & 1u, wc);
+}
+
+// Let every copy issued into a ring land before the CTA's shared memory goes away.
+__device__ __forceinline__ void ring_drain(uint64_t* full, uint32_t issued, int n, uint64_t timeout_ns) {
+    for (uint32_t s = 0; s < (uint32_t)n && s < issued; ++s) {
+        const uint32_t last = issued - 1 - ((issued - 1 - s) % n);
+        drain_wait(&full[s], (last / n) & 1u, timeout_ns);
+    }
+}
+
+// ------------------------------------------------------------------ dq kernel
 template <int D>
 __device__ void dq_load(const AttnBwdParams& p, const CUtensorMap* tq, const CUtensorMap* tdo,
-                        const CUtensorMap* tk, const CUtensorMap* tv, uint8_t* smem, const DqBars& b,
+                        const CUtensorMap* tk, const CUtensorMap* tv, uint8_t* smem, const Bars& b,
                         const WaitCtl& wc) {
     using C = BwdCfg<D>;
     const Ring& R = p.ring;
     const uint64_t keep = make_policy_evict_last(), stream = make_policy_evict_first();
-    uint32_t kv_idx = 0, qit = 0;
+    uint32_t ka = 0, vb = 0, qit = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
         if (round * (int)gridDim.x >= p.n_items) break;
@@ -268,41 +336,39 @@ __device__ void dq_load(const AttnBwdParams& p, const CUtensorMap* tq, const CUt
         if (item >= p.n_items) continue;
         int hq, qp;
         dq_item(p, item, hq, qp);
-        if (!mbar_wait(b.q_empty, (qit & 1u) ^ 1u, wc, 32)) { ok = false; break; }
+        if (!mbar_wait(b.res_empty, (qit & 1u) ^ 1u, wc, 32)) { ok = false; break; }
         ++qit;
-        mbar_arrive_expect_tx(b.q_full, 2 * C::kTileBytes);
+        mbar_arrive_expect_tx(b.res_full, 2 * C::kTileBytes);
         const int qrow = row_of(p, hq, qp);
-        load_tile<D>(smem, tq, b.q_full, qrow, stream);
-        load_tile<D>(smem + C::kTileBytes, tdo, b.q_full, qrow, stream);
+        load_tile<D>(smem, tq, b.res_full, qrow, stream);
+        load_tile<D>(smem + C::kTileBytes, tdo, b.res_full, qrow, stream);
         const int hk = hq / R.g;
         for_each_key_tile(R, qp, [&](int t0) -> bool {
-            const uint32_t s = kv_idx % C::kStages;
-            if (!mbar_wait(&b.kv_empty[s], ((kv_idx / C::kStages) & 1u) ^ 1u, wc, 32)) { ok = false; return false; }
-            mbar_arrive_expect_tx(&b.kv_full[s], 2 * C::kTileBytes);
-            uint8_t* st = smem + C::kDqKVOff + s * C::kDqStageBytes;
             const int krow = row_of(p, hk, t0);
-            load_tile<D>(st, tk, &b.kv_full[s], krow, keep);
-            load_tile<D>(st + C::kTileBytes, tv, &b.kv_full[s], krow, keep);
-            ++kv_idx;
+            if (!ring_load<D>(smem + C::kAOff, b.a_full, b.a_empty, ka, C::kSlotsA, tk, krow, keep, wc) ||
+                !ring_load<D>(smem + C::kBOff, b.b_full, b.b_empty, vb, C::kSlotsB, tv, krow, keep, wc)) {
+                ok = false;
+                return false;
+            }
+            ++ka;
+            ++vb;
             return true;
         });
     }
     if (!ok) {
-        // let every copy already issued land before the CTA's shared memory goes away
-        for (uint32_t s = 0; s < (uint32_t)C::kStages && s < kv_idx; ++s) {
-            const uint32_t last = kv_idx - 1 - ((kv_idx - 1 - s) % C::kStages);
-            drain_wait(&b.kv_full[s], (last / C::kStages) & 1u, wc.timeout_ns);
-        }
-        if (qit > 0) drain_wait(b.q_full, (qit - 1) & 1u, wc.timeout_ns);
+        ring_drain(b.a_full, ka, C::kSlotsA, wc.timeout_ns);
+        ring_drain(b.b_full, vb, C::kSlotsB, wc.timeout_ns);
+        if (qit > 0) drain_wait(b.res_full, (qit - 1) & 1u, wc.timeout_ns);
     }
 }
 
 template <int D>
-__device__ void dq_mma(const AttnBwdParams& p, uint8_t* smem, const DqBars& b, uint32_t tmem, const WaitCtl& wc) {
+__device__ void dq_mma(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uint32_t tmem, const WaitCtl& wc) {
     using C = BwdCfg<D>;
     const Ring& R = p.ring;
-    const uint32_t sQ = smem_u32(smem), sdO = sQ + C::kTileBytes, sKV = sQ + C::kDqKVOff;
-    uint32_t kv_idx = 0, qit = 0, dsit = 0;
+    const uint32_t sQ = smem_u32(smem), sdO = sQ + C::kTileBytes;
+    const uint32_t sA = sQ + C::kAOff, sB = sQ + C::kBOff;
+    uint32_t idx = 0, qit = 0, sf = 0, dpf = 0, dsit[2] = {0, 0};
     bool ok = true;
     for (int round = 0; ok; ++round) {
         if (round * (int)gridDim.x >= p.n_items) break;
@@ -311,32 +377,51 @@ __device__ void dq_mma(const AttnBwdParams& p, uint8_t* smem, const DqBars& b, u
         int hq, qp;
         dq_item(p, item, hq, qp);
         const int nj = count_key_tiles(R, qp);
-        if (!mbar_wait(b.q_full, qit & 1u, wc)) { ok = false; break; }
-        uint32_t st = kv_idx % C::kStages;
-        if (!mbar_wait(&b.kv_full[st], (kv_idx / C::kStages) & 1u, wc)) { ok = false; break; }
+        const uint32_t i0 = idx;
+        if (!mbar_wait(b.res_full, qit & 1u, wc)) { ok = false; break; }
+        // S(0), dP(0)
+        if (!ring_wait(b.a_full, i0, C::kSlotsA, wc)) { ok = false; break; }
         tc_fence_after();
-        issue_kk<D>(tmem, sQ, sKV + st * C::kDqStageBytes);                            // S = Q K^T
-        issue_kk<D>(tmem + kTile, sdO, sKV + st * C::kDqStageBytes + C::kTileBytes);  // dP = dO V^T
+        issue_kk<D>(tmem, sQ, sA + (i0 % C::kSlotsA) * C::kTileBytes);
         mma_commit(b.s_full);
+        if (!ring_wait(b.b_full, i0, C::kSlotsB, wc)) { ok = false; break; }
+        tc_fence_after();
+        issue_kk<D>(tmem + kTile, sdO, sB + (i0 % C::kSlotsB) * C::kTileBytes);
+        mma_commit(b.dp_full);
+        mma_commit(&b.b_empty[i0 % C::kSlotsB]);  // V(0) is done once dP(0) is
         for (int j = 0; j < nj && ok; ++j) {
-            if (!mbar_wait(b.ds_full, dsit & 1u, wc)) { ok = false; break; }
-            ++dsit;
-            if (j == 0 && !mbar_wait(b.acc_free, (qit & 1u) ^ 1u, wc)) { ok = false; break; }
-            tc_fence_after();
-            issue_tm<D>(tmem + kAccCol, tmem, sKV + st * C::kDqStageBytes, j > 0);  // dQ += dS K
-            mma_commit(&b.kv_empty[st]);
-            ++kv_idx;
-            if (j + 1 < nj) {
-                st = kv_idx % C::kStages;
-                if (!mbar_wait(&b.kv_full[st], (kv_idx / C::kStages) & 1u, wc)) { ok = false; break; }
+            const uint32_t i = i0 + j;
+            const bool more = j + 1 < nj;
+            // the next S as soon as this tile's S is out of TMEM
+            if (!mbar_wait(b.s_free, sf & 1u, wc)) { ok = false; break; }
+            ++sf;
+            if (more) {
+                if (!ring_wait(b.a_full, i + 1, C::kSlotsA, wc)) { ok = false; break; }
                 tc_fence_after();
-                issue_kk<D>(tmem, sQ, sKV + st * C::kDqStageBytes);
-                issue_kk<D>(tmem + kTile, sdO, sKV + st * C::kDqStageBytes + C::kTileBytes);
+                issue_kk<D>(tmem, sQ, sA + ((i + 1) % C::kSlotsA) * C::kTileBytes);
                 mma_commit(b.s_full);
             }
+            if (!mbar_wait(b.dp_free, dpf & 1u, wc)) { ok = false; break; }
+            ++dpf;
+            if (more) {
+                if (!ring_wait(b.b_full, i + 1, C::kSlotsB, wc)) { ok = false; break; }
+                tc_fence_after();
+                issue_kk<D>(tmem + kTile, sdO, sB + ((i + 1) % C::kSlotsB) * C::kTileBytes);
+                mma_commit(b.dp_full);
+                mma_commit(&b.b_empty[(i + 1) % C::kSlotsB]);
+            }
+            const int bb = j & 1;
+            if (!mbar_wait(&b.ds_full[bb], dsit[bb] & 1u, wc)) { ok = false; break; }
+            ++dsit[bb];
+            if (j == 0 && !mbar_wait(b.acc_free, (qit & 1u) ^ 1u, wc)) { ok = false; break; }
+            tc_fence_after();
+            // dQ += dS K, dS from TMEM buffer j % 2, K from its ring slot as an MN-major B
+            issue_tm<D>(tmem + kAccCol, tmem + 384 + 64 * bb, 32, sA + (i % C::kSlotsA) * C::kTileBytes, j > 0);
+            mma_commit(&b.a_empty[i % C::kSlotsA]);
         }
         if (!ok) break;
-        mma_commit(b.q_empty);
+        idx = i0 + nj;
+        mma_commit(b.res_empty);
         mma_commit(b.acc_done);
         ++qit;
     }
@@ -348,7 +433,7 @@ __device__ void dq_mma(const AttnBwdParams& p, uint8_t* smem, const DqBars& b, u
 }
 
 template <int D>
-__device__ void dq_compute(const AttnBwdParams& p, const DqBars& b, uint32_t tmem, const WaitCtl& wc) {
+__device__ void dq_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem, const WaitCtl& wc) {
     const Ring& R = p.ring;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int h = warp / 4, wq = warp % 4;
@@ -357,7 +442,7 @@ __device__ void dq_compute(const AttnBwdParams& p, const DqBars& b, uint32_t tme
     const uint32_t s_tm = tmem + lane_off + h * 64;           // my 64 key columns of S
     const uint32_t dp_tm = tmem + lane_off + kTile + h * 64;  // and of dP
     const uint32_t acc_tm = tmem + lane_off + kAccCol + h * (D / 2);
-    uint32_t sit = 0, it = 0;
+    uint32_t sf = 0, dpf = 0, it = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
         if (round * (int)gridDim.x >= p.n_items) break;
@@ -369,41 +454,46 @@ __device__ void dq_compute(const AttnBwdParams& p, const DqBars& b, uint32_t tme
         const float nl = -__ldg(p.lse + grow) * kLog2e;
         const float dl = __ldg(p.delta + grow);
         const int qpos = qp + row;
+        uint32_t jj = 0;  // tile within the item
         for_each_key_tile(R, qp, [&](int t0) -> bool {
-            bool w_ok = true;
-            if (wq == 0) w_ok = __all_sync(0xffffffffu, mbar_wait(b.s_full, sit & 1u, wc));
-            w_ok = group_bar_and(h, w_ok);
-            ++sit;
-            if (!w_ok) { ok = false; return false; }
+            if (!group_wait(b.s_full, sf & 1u, h, wq, wc)) { ok = false; return false; }
+            ++sf;
             tc_fence_after();
-            float s[64], dp[64];
-            tmem_ld64(s_tm, s);
-            tmem_ld64(dp_tm, dp);
+            float x[64];
+            tmem_take64(s_tm, x, b.s_free);
             const int lim = qpos - (t0 + h * 64);  // my keys [0, lim] are visible
             const bool mask = R.causal && lim < 63;
-            uint32_t pk[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < 64; i += 2) {
                 float p0, p1;
-                ffma2(p0, p1, s[2 * i], s[2 * i + 1], kLog2e, kLog2e, nl, nl);
+                ffma2(p0, p1, x[i], x[i + 1], kLog2e, kLog2e, nl, nl);
                 p0 = ex2(p0);
                 p1 = ex2(p1);
                 if (mask) {
-                    p0 = (2 * i > lim) ? 0.f : p0;
-                    p1 = (2 * i + 1 > lim) ? 0.f : p1;
+                    p0 = (i > lim) ? 0.f : p0;
+                    p1 = (i + 1 > lim) ? 0.f : p1;
                 }
-                pk[i] = pack_bf16x2(p0 * (dp[2 * i] - dl), p1 * (dp[2 * i + 1] - dl));
+                x[i] = p0;
+                x[i + 1] = p1;
             }
-            tmem_st32(s_tm, pk);  // dS over the first 32 of my own S columns
+            if (!group_wait(b.dp_full, dpf & 1u, h, wq, wc)) { ok = false; return false; }
+            ++dpf;
+            tc_fence_after();
+            float dp[64];
+            tmem_take64(dp_tm, dp, b.dp_free);
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(x[2 * i] * (dp[2 * i] - dl), x[2 * i + 1] * (dp[2 * i + 1] - dl));
+            const int bb = jj & 1;  // dS buffer, as the MMA issuer counts it
+            tmem_st32(tmem + lane_off + 384 + 64 * bb + 32 * h, pk);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(b.ds_full);
+            mbar_arrive(&b.ds_full[bb]);
+            ++jj;
             return true;
         });
         if (!ok) break;
-        bool d_ok = true;
-        if (wq == 0) d_ok = __all_sync(0xffffffffu, mbar_wait(b.acc_done, it & 1u, wc));
-        if (!group_bar_and(h, d_ok)) { ok = false; break; }
+        if (!group_wait(b.acc_done, it & 1u, h, wq, wc)) { ok = false; break; }
         ++it;
         tc_fence_after();
         store_acc<D / 2>(acc_tm, p.dq + static_cast<size_t>(grow) * D + h * (D / 2));
@@ -412,83 +502,16 @@ __device__ void dq_compute(const AttnBwdParams& p, const DqBars& b, uint32_t tme
     }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
-    bwd_dq_kernel(const __grid_constant__ AttnBwdParams p, const __grid_constant__ CUtensorMap tq,
-                  const __grid_constant__ CUtensorMap tdo, const __grid_constant__ CUtensorMap tk,
-                  const __grid_constant__ CUtensorMap tv) {
-    using C = BwdCfg<D>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kDqBarOff);
-    const DqBars b(bars, C::kStages);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kDqBarOff + C::kNumBars * 8);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kDqBarOff + C::kNumBars * 8 + 4);
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    if (threadIdx.x == 0) {
-        mbar_init(b.q_full, 1);
-        mbar_init(b.q_empty, 1);
-        mbar_init(b.s_full, 1);
-        mbar_init(b.ds_full, 256);
-        mbar_init(b.acc_done, 1);
-        mbar_init(b.acc_free, 256);
-        mbar_init(b.drain, 1);
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(&b.kv_full[s], 1);
-            mbar_init(&b.kv_empty[s], 1);
-        }
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
-    if (warp == kMmaWarp) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
-    }
-    if (warp == kLoadWarp && lane == 0) {
-        tma_prefetch_desc(&tq);
-        tma_prefetch_desc(&tdo);
-        tma_prefetch_desc(&tk);
-        tma_prefetch_desc(&tv);
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const WaitCtl wc{abort_flag, p.err, p.timeout_ns};
-    if (warp < 8) {
-        dq_compute<D>(p, b, tmem, wc);
-    } else if (warp == kMmaWarp) {
-        if (lane == 0) dq_mma<D>(p, smem, b, tmem, wc);
-    } else if (warp == kLoadWarp) {
-        if (lane == 0) dq_load<D>(p, &tq, &tdo, &tk, &tv, smem, b, wc);
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
-}
-
 // ------------------------------------------------------------------ dk/dv kernel
-// Barriers: 0 kv_full (K, V landed), 1 kv_empty (item's MMAs done with K, V), 2 s_full
-// (S^T, dP^T in TMEM), 3 p_full (256 compute threads wrote P^T, dS^T), 4 acc_done,
-// 5 acc_free (256), 6 drain, then qd_full and qd_empty per stage (Q, dO, lse, D of one
-// query tile).
-struct KvBars {
-    uint64_t *kv_full, *kv_empty, *s_full, *p_full, *acc_done, *acc_free, *drain, *qd_full, *qd_empty;
-    __device__ KvBars(uint64_t* b, int stages)
-        : kv_full(b), kv_empty(b + 1), s_full(b + 2), p_full(b + 3), acc_done(b + 4), acc_free(b + 5),
-          drain(b + 6), qd_full(b + 16), qd_empty(b + 16 + stages) {}
-};
-
 template <int D>
 __device__ void kv_load(const AttnBwdParams& p, const CUtensorMap* tq, const CUtensorMap* tdo,
-                        const CUtensorMap* tk, const CUtensorMap* tv, uint8_t* smem, const KvBars& b,
+                        const CUtensorMap* tk, const CUtensorMap* tv, uint8_t* smem, const Bars& b,
                         const WaitCtl& wc) {
     using C = BwdCfg<D>;
     const Ring& R = p.ring;
-    // Q, dO tiles are re-read by every key tile of their KV group: keep them in L2
+    // Q, dO are re-read by every key tile of their KV group: keep them in L2
     const uint64_t keep = make_policy_evict_last(), stream = make_policy_evict_first();
-    uint32_t idx = 0, kit = 0;
+    uint32_t qa = 0, ob = 0, kit = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
         if (round * (int)gridDim.x >= p.n_items) break;
@@ -496,41 +519,38 @@ __device__ void kv_load(const AttnBwdParams& p, const CUtensorMap* tq, const CUt
         if (item >= p.n_items) continue;
         int hk, kp;
         kv_item(p, item, hk, kp);
-        if (!mbar_wait(b.kv_empty, (kit & 1u) ^ 1u, wc, 32)) { ok = false; break; }
+        if (!mbar_wait(b.res_empty, (kit & 1u) ^ 1u, wc, 32)) { ok = false; break; }
         ++kit;
-        mbar_arrive_expect_tx(b.kv_full, 2 * C::kTileBytes);
+        mbar_arrive_expect_tx(b.res_full, 2 * C::kTileBytes);
         const int krow = row_of(p, hk, kp);
-        load_tile<D>(smem, tk, b.kv_full, krow, stream);
-        load_tile<D>(smem + C::kTileBytes, tv, b.kv_full, krow, stream);
+        load_tile<D>(smem, tk, b.res_full, krow, stream);
+        load_tile<D>(smem + C::kTileBytes, tv, b.res_full, krow, stream);
         for_each_query_tile(R, hk, kp, [&](int hq, int t0) -> bool {
-            const uint32_t s = idx % C::kStages;
-            if (!mbar_wait(&b.qd_empty[s], ((idx / C::kStages) & 1u) ^ 1u, wc, 32)) { ok = false; return false; }
-            mbar_arrive_expect_tx(&b.qd_full[s], 2 * C::kTileBytes + 2 * kTile * 4);
-            uint8_t* st = smem + C::kKvQOff + s * C::kKvStageBytes;
             const int qrow = row_of(p, hq, t0);
-            load_tile<D>(st, tq, &b.qd_full[s], qrow, keep);
-            load_tile<D>(st + C::kTileBytes, tdo, &b.qd_full[s], qrow, keep);
-            bulk_load_1d(st + 2 * C::kTileBytes, p.lse + qrow, kTile * 4, &b.qd_full[s]);
-            bulk_load_1d(st + 2 * C::kTileBytes + kTile * 4, p.delta + qrow, kTile * 4, &b.qd_full[s]);
-            ++idx;
+            if (!ring_load<D>(smem + C::kAOff, b.a_full, b.a_empty, qa, C::kSlotsA, tq, qrow, keep, wc) ||
+                !ring_load<D>(smem + C::kBOff, b.b_full, b.b_empty, ob, C::kSlotsB, tdo, qrow, keep, wc)) {
+                ok = false;
+                return false;
+            }
+            ++qa;
+            ++ob;
             return true;
         });
     }
     if (!ok) {
-        for (uint32_t s = 0; s < (uint32_t)C::kStages && s < idx; ++s) {
-            const uint32_t last = idx - 1 - ((idx - 1 - s) % C::kStages);
-            drain_wait(&b.qd_full[s], (last / C::kStages) & 1u, wc.timeout_ns);
-        }
-        if (kit > 0) drain_wait(b.kv_full, (kit - 1) & 1u, wc.timeout_ns);
+        ring_drain(b.a_full, qa, C::kSlotsA, wc.timeout_ns);
+        ring_drain(b.b_full, ob, C::kSlotsB, wc.timeout_ns);
+        if (kit > 0) drain_wait(b.res_full, (kit - 1) & 1u, wc.timeout_ns);
     }
 }
 
 template <int D>
-__device__ void kv_mma(const AttnBwdParams& p, uint8_t* smem, const KvBars& b, uint32_t tmem, const WaitCtl& wc) {
+__device__ void kv_mma(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uint32_t tmem, const WaitCtl& wc) {
     using C = BwdCfg<D>;
     const Ring& R = p.ring;
-    const uint32_t sK = smem_u32(smem), sV = sK + C::kTileBytes, sQD = sK + C::kKvQOff;
-    uint32_t idx = 0, kit = 0, pit = 0;
+    const uint32_t sK = smem_u32(smem), sV = sK + C::kTileBytes;
+    const uint32_t sA = sK + C::kAOff, sB = sK + C::kBOff;
+    uint32_t idx = 0, kit = 0, sf = 0, pf = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
         if (round * (int)gridDim.x >= p.n_items) break;
@@ -539,34 +559,50 @@ __device__ void kv_mma(const AttnBwdParams& p, uint8_t* smem, const KvBars& b, u
         int hk, kp;
         kv_item(p, item, hk, kp);
         const int n = count_query_tiles(R, hk, kp);
-        if (!mbar_wait(b.kv_full, kit & 1u, wc)) { ok = false; break; }
-        uint32_t st = idx % C::kStages;
-        if (!mbar_wait(&b.qd_full[st], (idx / C::kStages) & 1u, wc)) { ok = false; break; }
+        const uint32_t i0 = idx;
+        if (!mbar_wait(b.res_full, kit & 1u, wc)) { ok = false; break; }
+        // S^T(0) = K Q(0)^T, dP^T(0) = V dO(0)^T
+        if (!ring_wait(b.a_full, i0, C::kSlotsA, wc)) { ok = false; break; }
         tc_fence_after();
-        issue_kk<D>(tmem, sK, sQD + st * C::kKvStageBytes);                           // S^T = K Q^T
-        issue_kk<D>(tmem + kTile, sV, sQD + st * C::kKvStageBytes + C::kTileBytes);  // dP^T = V dO^T
+        issue_kk<D>(tmem, sK, sA + (i0 % C::kSlotsA) * C::kTileBytes);
         mma_commit(b.s_full);
-        for (int i = 0; i < n && ok; ++i) {
-            if (!mbar_wait(b.p_full, pit & 1u, wc)) { ok = false; break; }
-            ++pit;
-            if (i == 0 && !mbar_wait(b.acc_free, (kit & 1u) ^ 1u, wc)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t sq = sQD + st * C::kKvStageBytes;
-            issue_tm<D>(tmem + kAccCol, tmem, sq + C::kTileBytes, i > 0);          // dV += P^T dO
-            issue_tm<D>(tmem + kAccCol + D, tmem + kTile, sq, i > 0);              // dK += dS^T Q
-            mma_commit(&b.qd_empty[st]);
-            ++idx;
-            if (i + 1 < n) {
-                st = idx % C::kStages;
-                if (!mbar_wait(&b.qd_full[st], (idx / C::kStages) & 1u, wc)) { ok = false; break; }
+        if (!ring_wait(b.b_full, i0, C::kSlotsB, wc)) { ok = false; break; }
+        tc_fence_after();
+        issue_kk<D>(tmem + kTile, sV, sB + (i0 % C::kSlotsB) * C::kTileBytes);
+        mma_commit(b.dp_full);
+        for (int t = 0; t < n && ok; ++t) {
+            const uint32_t i = i0 + t;
+            const bool more = t + 1 < n;
+            // the next S^T as soon as this tile's S^T is out of TMEM
+            if (!mbar_wait(b.s_free, sf & 1u, wc)) { ok = false; break; }
+            ++sf;
+            if (more) {
+                if (!ring_wait(b.a_full, i + 1, C::kSlotsA, wc)) { ok = false; break; }
                 tc_fence_after();
-                issue_kk<D>(tmem, sK, sQD + st * C::kKvStageBytes);
-                issue_kk<D>(tmem + kTile, sV, sQD + st * C::kKvStageBytes + C::kTileBytes);
+                issue_kk<D>(tmem, sK, sA + ((i + 1) % C::kSlotsA) * C::kTileBytes);
                 mma_commit(b.s_full);
+            }
+            if (!mbar_wait(&b.ds_full[0], pf & 1u, wc)) { ok = false; break; }
+            ++pf;
+            if (t == 0 && !mbar_wait(b.acc_free, (kit & 1u) ^ 1u, wc)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sq = sA + (i % C::kSlotsA) * C::kTileBytes;
+            const uint32_t sdo = sB + (i % C::kSlotsB) * C::kTileBytes;
+            issue_tm<D>(tmem + kAccCol, tmem + kTile, 64, sdo, t > 0);           // dV += P^T dO
+            mma_commit(&b.b_empty[i % C::kSlotsB]);
+            issue_tm<D>(tmem + kAccCol + D, tmem + kTile + 32, 64, sq, t > 0);   // dK += dS^T Q
+            mma_commit(&b.a_empty[i % C::kSlotsA]);
+            if (more) {
+                // dP^T(t+1) overwrites the P^T, dS^T columns the two products above read
+                if (!ring_wait(b.b_full, i + 1, C::kSlotsB, wc)) { ok = false; break; }
+                tc_fence_after();
+                issue_kk<D>(tmem + kTile, sV, sB + ((i + 1) % C::kSlotsB) * C::kTileBytes);
+                mma_commit(b.dp_full);
             }
         }
         if (!ok) break;
-        mma_commit(b.kv_empty);
+        idx = i0 + n;
+        mma_commit(b.res_empty);
         mma_commit(b.acc_done);
         ++kit;
     }
@@ -577,19 +613,17 @@ __device__ void kv_mma(const AttnBwdParams& p, uint8_t* smem, const KvBars& b, u
 }
 
 template <int D>
-__device__ void kv_compute(const AttnBwdParams& p, uint8_t* smem, const KvBars& b, uint32_t tmem,
-                           const WaitCtl& wc) {
-    using C = BwdCfg<D>;
+__device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem, const WaitCtl& wc) {
     const Ring& R = p.ring;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int h = warp / 4, wq = warp % 4;
     const int row = wq * 32 + lane;  // key row of the tile
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t s_tm = tmem + lane_off + h * 64;           // my 64 query columns of S^T
-    const uint32_t dp_tm = tmem + lane_off + kTile + h * 64;  // and of dP^T
+    const uint32_t dp_tm = tmem + lane_off + kTile + h * 64;  // and of dP^T (P^T, dS^T go here)
     const uint32_t dv_tm = tmem + lane_off + kAccCol + h * (D / 2);
     const uint32_t dk_tm = tmem + lane_off + kAccCol + D + h * (D / 2);
-    uint32_t idx = 0, sit = 0, it = 0;
+    uint32_t sf = 0, dpf = 0, it = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
         if (round * (int)gridDim.x >= p.n_items) break;
@@ -598,58 +632,63 @@ __device__ void kv_compute(const AttnBwdParams& p, uint8_t* smem, const KvBars& 
         int hk, kp;
         kv_item(p, item, hk, kp);
         const int kpos = kp + row;
-        for_each_query_tile(R, hk, kp, [&](int, int t0) -> bool {
-            const uint32_t st = idx % C::kStages;
-            bool w_ok = true;
-            if (wq == 0)
-                w_ok = __all_sync(0xffffffffu, mbar_wait(b.s_full, sit & 1u, wc) &&
-                                                   mbar_wait(&b.qd_full[st], (idx / C::kStages) & 1u, wc));
-            w_ok = group_bar_and(h, w_ok);
-            ++sit;
-            ++idx;
-            if (!w_ok) { ok = false; return false; }
+        for_each_query_tile(R, hk, kp, [&](int hq, int t0) -> bool {
+            const int qrow = row_of(p, hq, t0) + h * 64;  // my first query column's row in lse, delta
+            if (!group_wait(b.s_full, sf & 1u, h, wq, wc)) { ok = false; return false; }
+            ++sf;
             tc_fence_after();
-            float s[64], dp[64];
-            tmem_ld64(s_tm, s);
-            tmem_ld64(dp_tm, dp);
-            const float* sl = reinterpret_cast<const float*>(smem + C::kKvQOff + st * C::kKvStageBytes +
-                                                             2 * C::kTileBytes) + h * 64;
-            const float* sd = sl + kTile;
+            float x[64];
+            tmem_take64(s_tm, x, b.s_free);
             const int lo = kpos - (t0 + h * 64);  // my query columns [lo, 64) see my key
             const bool mask = R.causal && lo > 0;
+            const float4* l4 = reinterpret_cast<const float4*>(p.lse + qrow);
+#pragma unroll
+            for (int i4 = 0; i4 < 16; ++i4) {
+                const float4 lv = __ldg(l4 + i4);
+                float p0, p1, p2, p3;
+                ffma2(p0, p1, x[4 * i4], x[4 * i4 + 1], kLog2e, kLog2e, -lv.x * kLog2e, -lv.y * kLog2e);
+                ffma2(p2, p3, x[4 * i4 + 2], x[4 * i4 + 3], kLog2e, kLog2e, -lv.z * kLog2e, -lv.w * kLog2e);
+                p0 = ex2(p0);
+                p1 = ex2(p1);
+                p2 = ex2(p2);
+                p3 = ex2(p3);
+                if (mask) {
+                    const int i = 4 * i4;
+                    p0 = (i < lo) ? 0.f : p0;
+                    p1 = (i + 1 < lo) ? 0.f : p1;
+                    p2 = (i + 2 < lo) ? 0.f : p2;
+                    p3 = (i + 3 < lo) ? 0.f : p3;
+                }
+                x[4 * i4] = p0;
+                x[4 * i4 + 1] = p1;
+                x[4 * i4 + 2] = p2;
+                x[4 * i4 + 3] = p3;
+            }
+            if (!group_wait(b.dp_full, dpf & 1u, h, wq, wc)) { ok = false; return false; }
+            ++dpf;
+            tc_fence_after();
+            float dp[64];
+            tmem_ld64(dp_tm, dp);
+            const float4* d4 = reinterpret_cast<const float4*>(p.delta + qrow);
             uint32_t pp[32], pd[32];
 #pragma unroll
             for (int i4 = 0; i4 < 16; ++i4) {
-                const float4 l4 = reinterpret_cast<const float4*>(sl)[i4];
-                const float4 d4 = reinterpret_cast<const float4*>(sd)[i4];
-                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-                for (int e = 0; e < 4; e += 2) {
-                    const int i = i4 * 4 + e;
-                    float p0, p1;
-                    ffma2(p0, p1, s[i], s[i + 1], kLog2e, kLog2e, -lv[e] * kLog2e, -lv[e + 1] * kLog2e);
-                    p0 = ex2(p0);
-                    p1 = ex2(p1);
-                    if (mask) {
-                        p0 = (i < lo) ? 0.f : p0;
-                        p1 = (i + 1 < lo) ? 0.f : p1;
-                    }
-                    pp[i / 2] = pack_bf16x2(p0, p1);
-                    pd[i / 2] = pack_bf16x2(p0 * (dp[i] - dv[e]), p1 * (dp[i + 1] - dv[e + 1]));
-                }
+                const float4 dv = __ldg(d4 + i4);
+                const int i = 4 * i4;
+                pp[2 * i4] = pack_bf16x2(x[i], x[i + 1]);
+                pp[2 * i4 + 1] = pack_bf16x2(x[i + 2], x[i + 3]);
+                pd[2 * i4] = pack_bf16x2(x[i] * (dp[i] - dv.x), x[i + 1] * (dp[i + 1] - dv.y));
+                pd[2 * i4 + 1] = pack_bf16x2(x[i + 2] * (dp[i + 2] - dv.z), x[i + 3] * (dp[i + 3] - dv.w));
             }
-            tmem_st32(s_tm, pp);   // P^T over the first 32 of my own S^T columns
-            tmem_st32(dp_tm, pd);  // dS^T over the first 32 of my own dP^T columns
+            tmem_st32(dp_tm, pp);       // P^T over the first 32 of my own dP^T columns
+            tmem_st32(dp_tm + 32, pd);  // dS^T over the other 32
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(b.p_full);
+            mbar_arrive(&b.ds_full[0]);
             return true;
         });
         if (!ok) break;
-        bool d_ok = true;
-        if (wq == 0) d_ok = __all_sync(0xffffffffu, mbar_wait(b.acc_done, it & 1u, wc));
-        if (!group_bar_and(h, d_ok)) { ok = false; break; }
+        if (!group_wait(b.acc_done, it & 1u, h, wq, wc)) { ok = false; break; }
         ++it;
         tc_fence_after();
         const size_t grow = static_cast<size_t>(row_of(p, hk, kp) + row);
@@ -660,31 +699,22 @@ __device__ void kv_compute(const AttnBwdParams& p, uint8_t* smem, const KvBars& 
     }
 }
 
-template <int D>
+// ------------------------------------------------------------------ kernels
+template <int D, bool DQ>
 __global__ void __launch_bounds__(kThreads, 1)
-    bwd_dkdv_kernel(const __grid_constant__ AttnBwdParams p, const __grid_constant__ CUtensorMap tq,
-                    const __grid_constant__ CUtensorMap tdo, const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv) {
+    bwd_kernel(const __grid_constant__ AttnBwdParams p, const __grid_constant__ CUtensorMap tq,
+               const __grid_constant__ CUtensorMap tdo, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kKvBarOff);
-    const KvBars b(bars, C::kStages);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kKvBarOff + C::kNumBars * 8);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kKvBarOff + C::kNumBars * 8 + 4);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+    const Bars b(bars);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kBarOff + C::kNumBars * 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kBarOff + C::kNumBars * 8 + 4);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
-        mbar_init(b.kv_full, 1);
-        mbar_init(b.kv_empty, 1);
-        mbar_init(b.s_full, 1);
-        mbar_init(b.p_full, 256);
-        mbar_init(b.acc_done, 1);
-        mbar_init(b.acc_free, 256);
-        mbar_init(b.drain, 1);
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(&b.qd_full[s], 1);
-            mbar_init(&b.qd_empty[s], 1);
-        }
+        init_bars(b);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -704,11 +734,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const WaitCtl wc{abort_flag, p.err, p.timeout_ns};
     if (warp < 8) {
-        kv_compute<D>(p, smem, b, tmem, wc);
+        if constexpr (DQ) dq_compute<D>(p, b, tmem, wc);
+        else kv_compute<D>(p, b, tmem, wc);
     } else if (warp == kMmaWarp) {
-        if (lane == 0) kv_mma<D>(p, smem, b, tmem, wc);
+        if (lane == 0) {
+            if constexpr (DQ) dq_mma<D>(p, smem, b, tmem, wc);
+            else kv_mma<D>(p, smem, b, tmem, wc);
+        }
     } else if (warp == kLoadWarp) {
-        if (lane == 0) kv_load<D>(p, &tq, &tdo, &tk, &tv, smem, b, wc);
+        if (lane == 0) {
+            if constexpr (DQ) dq_load<D>(p, &tq, &tdo, &tk, &tv, smem, b, wc);
+            else kv_load<D>(p, &tq, &tdo, &tk, &tv, smem, b, wc);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -759,16 +796,15 @@ int launch_bwd_d(const AttnBwdParams& p0, const float* out, const void* dout, co
 
     AttnBwdParams p = p0;
     p.n_items = R.Hq * p.n_tiles;
-    auto kq = bwd_dq_kernel<D>;
-    if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDqSmem) != cudaSuccess) return -4;
-    kq<<<p.n_items < sms ? p.n_items : sms, kThreads, C::kDqSmem, stream>>>(p, tq, tdo, tk, tv);
+    auto kq = bwd_kernel<D, true>;
+    if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess) return -4;
+    kq<<<p.n_items < sms ? p.n_items : sms, kThreads, C::kSmem, stream>>>(p, tq, tdo, tk, tv);
     if (cudaGetLastError() != cudaSuccess) return -4;
 
     p.n_items = R.Hkv * p.n_tiles;
-    auto kkv = bwd_dkdv_kernel<D>;
-    if (cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kKvSmem) != cudaSuccess)
-        return -4;
-    kkv<<<p.n_items < sms ? p.n_items : sms, kThreads, C::kKvSmem, stream>>>(p, tq, tdo, tk, tv);
+    auto kkv = bwd_kernel<D, false>;
+    if (cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess) return -4;
+    kkv<<<p.n_items < sms ? p.n_items : sms, kThreads, C::kSmem, stream>>>(p, tq, tdo, tk, tv);
     return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
