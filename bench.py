@@ -524,18 +524,19 @@ def main():
     # end to end through the C-ABI call on host buffers (ringattn_fwd_host): H2D of Q/K/V
     # from pinned memory, the attention, D2H of out and lse, every step inside the timed
     # region; the library overlaps the copies with the attention by KV-head groups
-    e2e_steps = max(1, min(args.steps, 5))
+    e2e_steps = max(1, min(args.steps, 10))
     ws = torch.empty(ra.host_workspace_bytes(S, w.bhq, w.bhkv, w.d), dtype=torch.uint8, device=dev)
-    ra.fwd_host(q_h, k_h, v_h, out_h, lse_h, ws, **kw)   # first call creates the copy streams
-    torch.cuda.synchronize()
-    s0 = torch.cuda.Event(enable_timing=True)
-    s1 = torch.cuda.Event(enable_timing=True)
-    s0.record(stream)
-    for _ in range(e2e_steps):
+    for _ in range(2):   # the first call creates the copy streams; both touch every host page
         ra.fwd_host(q_h, k_h, v_h, out_h, lse_h, ws, **kw)
-    s1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = s0.elapsed_time(s1) / e2e_steps
+    e2e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
+    e2e_ev[0].record(stream)
+    for i in range(e2e_steps):
+        ra.fwd_host(q_h, k_h, v_h, out_h, lse_h, ws, **kw)
+        e2e_ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e2e_ev[0].elapsed_time(e2e_ev[-1]) / e2e_steps
+    e2e_each = [e2e_ev[i].elapsed_time(e2e_ev[i + 1]) for i in range(e2e_steps)]
     del ws
     if ra.sync_status() != ra.RA_OK:
         raise SystemExit("device wait timed out in the end-to-end region")
@@ -581,6 +582,8 @@ def main():
         extra = [attention_only(ra, WORKLOADS[name], dev, stream, 5, peaks()[0])
                  for name in ("causal_gqa_S131072_h32x8_d128_c16_zigzag", "docmask_gqa_S32768_h64x8_d128_c8_zigzag")]
         extra.append(ulysses_only(ra, w, dev, stream, 5, peaks()[0], peaks()[2]))
+        torch.cuda.empty_cache()
+        extra.append(backward_only(ra, w, dev, stream, 3, peaks()[0]))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -617,6 +620,7 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "steps": e2e_steps,
+                    "ms_per_step_min": min(e2e_each), "ms_per_step_median": float(np.median(e2e_each)),
                     "call": "ringattn_fwd_host (natural order; copies overlapped with attention by KV-head groups)"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,

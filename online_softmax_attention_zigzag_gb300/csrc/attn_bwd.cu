@@ -59,7 +59,9 @@ struct BwdCfg {
     static constexpr int kBOff = kAOff + kSlotsA * kTileBytes;
     static constexpr int kBarOff = kBOff + kSlotsB * kTileBytes;
     static constexpr int kNumBars = 32;
-    static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;  // + slack to align the base
+    // dk/dv: lse and D of the current query tile, per compute warpgroup (64 + 64 floats)
+    static constexpr int kLdOff = kBarOff + kNumBars * 8 + 16;
+    static constexpr int kSmem = kLdOff + 2 * 128 * 4 + 1024;  // + slack to align the base
 };
 
 // Rank-major (or natural) row of natural position pos of head `head`.
@@ -612,8 +614,13 @@ __device__ void kv_mma(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uin
     }
 }
 
+// Named barrier over one compute warpgroup, no predicate.
+__device__ __forceinline__ void group_sync(int h) {
+    asm volatile("bar.sync %0, 128;" ::"r"(3 + h) : "memory");
+}
+
 template <int D>
-__device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem, const WaitCtl& wc) {
+__device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem, float* sld, const WaitCtl& wc) {
     const Ring& R = p.ring;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int h = warp / 4, wq = warp % 4;
@@ -634,17 +641,22 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
         const int kpos = kp + row;
         for_each_query_tile(R, hk, kp, [&](int hq, int t0) -> bool {
             const int qrow = row_of(p, hq, t0) + h * 64;  // my first query column's row in lse, delta
+            // each thread fetches one of the warpgroup's 64 lse and 64 D values now, so the
+            // load's latency hides behind the wait for S^T
+            const float mine = __ldg((row < 64 ? p.lse : p.delta) + qrow + (row & 63));
             if (!group_wait(b.s_full, sf & 1u, h, wq, wc)) { ok = false; return false; }
             ++sf;
+            sld[row] = mine;  // every thread of the group is past its reads of the last tile
+            group_sync(h);
             tc_fence_after();
             float x[64];
             tmem_take64(s_tm, x, b.s_free);
             const int lo = kpos - (t0 + h * 64);  // my query columns [lo, 64) see my key
             const bool mask = R.causal && lo > 0;
-            const float4* l4 = reinterpret_cast<const float4*>(p.lse + qrow);
+            const float4* l4 = reinterpret_cast<const float4*>(sld);
 #pragma unroll
             for (int i4 = 0; i4 < 16; ++i4) {
-                const float4 lv = __ldg(l4 + i4);
+                const float4 lv = l4[i4];
                 float p0, p1, p2, p3;
                 ffma2(p0, p1, x[4 * i4], x[4 * i4 + 1], kLog2e, kLog2e, -lv.x * kLog2e, -lv.y * kLog2e);
                 ffma2(p2, p3, x[4 * i4 + 2], x[4 * i4 + 3], kLog2e, kLog2e, -lv.z * kLog2e, -lv.w * kLog2e);
@@ -669,11 +681,11 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
             tc_fence_after();
             float dp[64];
             tmem_ld64(dp_tm, dp);
-            const float4* d4 = reinterpret_cast<const float4*>(p.delta + qrow);
+            const float4* d4 = reinterpret_cast<const float4*>(sld + 64);
             uint32_t pp[32], pd[32];
 #pragma unroll
             for (int i4 = 0; i4 < 16; ++i4) {
-                const float4 dv = __ldg(d4 + i4);
+                const float4 dv = d4[i4];
                 const int i = 4 * i4;
                 pp[2 * i4] = pack_bf16x2(x[i], x[i + 1]);
                 pp[2 * i4 + 1] = pack_bf16x2(x[i + 2], x[i + 3]);
@@ -735,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const WaitCtl wc{abort_flag, p.err, p.timeout_ns};
     if (warp < 8) {
         if constexpr (DQ) dq_compute<D>(p, b, tmem, wc);
-        else kv_compute<D>(p, b, tmem, wc);
+        else kv_compute<D>(p, b, tmem, reinterpret_cast<float*>(smem + C::kLdOff) + (warp / 4) * 128, wc);
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
             if constexpr (DQ) dq_mma<D>(p, smem, b, tmem, wc);

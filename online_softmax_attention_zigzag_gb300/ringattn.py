@@ -355,3 +355,31 @@ def attention(q, k, v, *, c, causal, layout, kv_block, stream=None):
     permute(o_r, out, c=c, layout=layout, inverse=1, stream=stream)
     permute(l_r, lse, c=c, layout=layout, inverse=1, stream=stream)
     return out, lse
+
+
+def attention_backward(q, k, v, out, lse, dout, *, c, causal, layout, kv_block, stream=None):
+    """Natural-order convenience call for the backward pass: permute the inputs to
+    rank-major, run ringattn_bwd, permute the gradients back.  ``out`` and ``lse`` are
+    :func:`attention`'s results for q, k, v.  Returns (dq, dk, dv), fp32, natural order."""
+    Hq, S, d = q.shape
+    Hkv = k.shape[0]
+    dev = q.device
+
+    def rm(x):
+        y = torch.empty_like(x)
+        permute(x, y, c=c, layout=layout, inverse=0, stream=stream)
+        return y
+
+    qr, kr, vr, o_r, l_r, do_r = (rm(x) for x in (q, k, v, out, lse, dout))
+    dq_r = torch.empty((Hq, S, d), dtype=torch.float32, device=dev)
+    dk_r = torch.empty((Hkv, S, d), dtype=torch.float32, device=dev)
+    dv_r = torch.empty_like(dk_r)
+    delta = torch.empty((Hq, S), dtype=torch.float32, device=dev)
+    bwd(qr, kr, vr, o_r, l_r, do_r, dq_r, dk_r, dv_r, delta, c=c, causal=causal, layout=layout,
+        kv_block=kv_block, stream=stream)
+    res = []
+    for x in (dq_r, dk_r, dv_r):
+        y = torch.empty_like(x)
+        permute(x, y, c=c, layout=layout, inverse=1, stream=stream)
+        res.append(y)
+    return tuple(res)

@@ -50,9 +50,14 @@ def _probs(qh, kh, causal):
     return e / L, (M + np.log(L))[:, 0]
 
 
-def attention_grad(q, k, v, dout, causal: bool):
-    """q, dout [Hq, S, d]; k, v [Hkv, S, d] -> dq [Hq, S, d], dk, dv [Hkv, S, d]."""
+def attention_grad(q, k, v, dout, causal: bool, out=None):
+    """q, dout [Hq, S, d]; k, v [Hkv, S, d] -> dq [Hq, S, d], dk, dv [Hkv, S, d].
+
+    out: the forward output the backward pass is given (D_i = dout_i . out_i is formed
+    from it, as a backward pass does); None takes the exact forward output, which makes
+    this the exact gradient."""
     q, k, v, dout = (_f64(x) for x in (q, k, v, dout))
+    out_given = None if out is None else _f64(out)
     Hq, S, d = q.shape
     Hkv = k.shape[0]
     g = Hq // Hkv
@@ -62,7 +67,7 @@ def attention_grad(q, k, v, dout, causal: bool):
     for h in range(Hq):
         hk = h // g
         P, _ = _probs(q[h], k[hk], causal)
-        out = P @ v[hk]
+        out = P @ v[hk] if out_given is None else out_given[h]
         dP = dout[h] @ v[hk].T
         D = np.einsum("sd,sd->s", dout[h], out)
         dS = P * (dP - D[:, None])
@@ -72,11 +77,12 @@ def attention_grad(q, k, v, dout, causal: bool):
     return dq, dk, dv
 
 
-def grad_abs_sums(q, k, v, dout, causal: bool):
+def grad_abs_sums(q, k, v, dout, causal: bool, out=None):
     """Per entry of dq, dk, dv, the sum of the absolute values of the terms it adds up
     (sum_j |dS_ij| |k_j|, sum_i |dS_ij| |q_i|, sum_i P_ij |dout_i|): the scale against
-    which rounding of the summed factors is measured."""
+    which rounding of the summed factors is measured.  out: as for attention_grad."""
     q, k, v, dout = (_f64(x) for x in (q, k, v, dout))
+    out_given = None if out is None else _f64(out)
     Hq, S, d = q.shape
     Hkv = k.shape[0]
     g = Hq // Hkv
@@ -86,7 +92,7 @@ def grad_abs_sums(q, k, v, dout, causal: bool):
     for h in range(Hq):
         hk = h // g
         P, _ = _probs(q[h], k[hk], causal)
-        out = P @ v[hk]
+        out = P @ v[hk] if out_given is None else out_given[h]
         dP = dout[h] @ v[hk].T
         D = np.einsum("sd,sd->s", dout[h], out)
         adS = np.abs(P * (dP - D[:, None]))

@@ -132,3 +132,22 @@ def test_backward_32k_sampled_dq_and_dv_column_sums(ra):
     want_sum = dout.double().reshape(w.bhkv, g, S, w.d).sum(dim=(1, 2))  # [Hkv, d]
     amass = dout.double().abs().reshape(w.bhkv, g, S, w.d).sum(dim=(1, 2))
     assert ((dsum - want_sum).abs() <= REL * amass).all()
+
+
+def test_natural_order_helpers_forward_and_backward(ra):
+    """ringattn.attention then ringattn.attention_backward (permute, ringattn_fwd /
+    ringattn_bwd, permute back) on natural-order tensors, against the oracle."""
+    Hq, Hkv, S, d = 4, 2, 1024, 64
+    q, k, v = _randn((Hq, S, d), 231, 0.125), _randn((Hkv, S, d), 232), _randn((Hkv, S, d), 233)
+    dout = _randn((Hq, S, d), 234)
+    kw = dict(c=4, causal=1, layout=1, kv_block=128)
+    out, lse = ra.attention(q.to(dev()), k.to(dev()), v.to(dev()), **kw)
+    grads = ra.attention_backward(q.to(dev()), k.to(dev()), v.to(dev()), out, lse, dout.to(dev()), **kw)
+    assert ra.sync_status() == ra.RA_OK
+    # D = dout . out comes from the forward's output on both sides
+    args = [f64(x) for x in (q, k, v, dout)]
+    o64 = f64(out)
+    for name, g, w, a in zip(("dq", "dk", "dv"), grads, obwd.attention_grad(*args, True, out=o64),
+                             obwd.grad_abs_sums(*args, True, out=o64)):
+        excess = np.abs(g.cpu().double().numpy() - w) - REL * a
+        assert excess.max() <= 1e-6 * a.max(), name

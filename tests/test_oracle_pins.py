@@ -166,3 +166,23 @@ def test_backward_dq_rows_match_whole():
         aq, _, _ = backward.grad_abs_sums(q, k, v, do, causal)
         _, ra_ = backward.dq_rows(q, k, v, do, heads, posn, causal, with_abs=True)
         assert np.abs(ra_ - aq[heads, posn]).max() < 1e-12
+
+
+def test_backward_given_out():
+    """Given the exact forward output, D is the same and so is the gradient; given a
+    perturbed one, only dq and dk move, and by exactly -P_ij (dout_i . delta_i) terms."""
+    from oracle import attention, backward
+    rng = np.random.default_rng(11)
+    q, k, v, do = (rng.standard_normal(s) for s in ((2, 12, 3), (1, 12, 3), (1, 12, 3), (2, 12, 3)))
+    o, _ = attention.full_attention(q, k, v, True)
+    for a, b in zip(backward.attention_grad(q, k, v, do, True), backward.attention_grad(q, k, v, do, True, out=o)):
+        assert np.abs(a - b).max() < 1e-12
+    dlt = rng.standard_normal(o.shape) * 1e-3
+    g0 = backward.attention_grad(q, k, v, do, True)
+    g1 = backward.attention_grad(q, k, v, do, True, out=o + dlt)
+    assert np.abs(g1[2] - g0[2]).max() < 1e-14                       # dv does not use D
+    dD = np.einsum("hsd,hsd->hs", do, dlt)                           # change of D per row
+    P = np.exp(np.where(np.triu(np.ones((12, 12)), 1) > 0, -np.inf, q @ k[0].T)
+               - attention.full_attention(q, k, v, True)[1][..., None])
+    want_dq = g0[0] - np.einsum("hij,hi,jd->hid", P, dD, k[0])
+    assert np.abs(g1[0] - want_dq).max() < 1e-12
