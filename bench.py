@@ -36,6 +36,7 @@ from online_softmax_attention_zigzag_gb300.configs import (  # noqa: E402
 from online_softmax_attention_zigzag_gb300.inputs import doc_ids, make_qkv, sample_rows  # noqa: E402
 
 METRIC = "causal-adjusted attention TFLOP/s and % of GB300 bf16 tensor peak, 1 GPU"
+NOMINAL_BF16_TFLOPS = 2250.0  # GB300 dense bf16 tensor rate, vendor figure (without 2:4 sparsity)
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
@@ -605,7 +606,8 @@ def main():
                          "frac": achieved / bf16_peak, "traffic": traffic,
                          "kernel": "attn_bf16_kernel<%d, false>" % w.d, "kernel_ms": attn_ms,
                          "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
-                         "frac_of_sustained": (achieved / bf16_sust) if bf16_sust else None},
+                         "frac_of_sustained": (achieved / bf16_sust) if bf16_sust else None,
+                         "nominal_peak": NOMINAL_BF16_TFLOPS, "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS},
             "natural_step": {"ms_per_step": nat_ms, "value": flop / (nat_ms * 1e-3) / 1e12, "unit": UNIT,
                              "what": "ringattn_fwd_natural: chunk map in TMA addressing, no permutation passes"},
             "also_measured": extra,
