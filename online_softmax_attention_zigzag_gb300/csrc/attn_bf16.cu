@@ -552,9 +552,9 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, int h, const Bars& 
             const float nmu = (m == -INFINITY) ? 0.f : -m;
             float se[4] = {0.f, 0.f, 0.f, 0.f};
             float sr[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[32];
 #pragma unroll
             for (int hh = 0; hh < 4; ++hh) {
-                uint32_t pk[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     float t0, t1;
@@ -562,11 +562,11 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, int h, const Bars& 
                     const float a = ex2(t0), c2 = ex2(t1);
                     const int q2 = 2 * (i & 1);
                     fadd2(se[q2], se[q2 + 1], se[q2], se[q2 + 1], a, c2);
-                    pk[i] = pack_bf16x2(a, c2);
-                    add_bf16x2_f32(sr[q2], sr[q2 + 1], pk[i]);
+                    pk[hh * 8 + i] = pack_bf16x2(a, c2);
+                    add_bf16x2_f32(sr[q2], sr[q2 + 1], pk[hh * 8 + i]);
                 }
-                tmem_st8(p_tmem + hh * 8, pk);
             }
+            tmem_st32(p_tmem, pk);
             // O is stable here: the commit that signalled this S also covered the
             // previous P V, and the next P V waits for this tile's arrivals.
             if (__any_sync(0xffffffffu, need)) {
