@@ -679,18 +679,26 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
             if (!group_wait(b.dp_full, dpf & 1u, h, wq, wc)) { ok = false; return false; }
             ++dpf;
             tc_fence_after();
-            float dp[64];
-            tmem_ld64(dp_tm, dp);
             const float4* d4 = reinterpret_cast<const float4*>(sld + 64);
             uint32_t pp[32], pd[32];
+            // dP^T in two 32-column chunks, each packed as soon as it is used, so that P, dP^T
+            // and the packed words are never all live at once
 #pragma unroll
-            for (int i4 = 0; i4 < 16; ++i4) {
-                const float4 dv = d4[i4];
-                const int i = 4 * i4;
-                pp[2 * i4] = pack_bf16x2(x[i], x[i + 1]);
-                pp[2 * i4 + 1] = pack_bf16x2(x[i + 2], x[i + 3]);
-                pd[2 * i4] = pack_bf16x2(x[i] * (dp[i] - dv.x), x[i + 1] * (dp[i + 1] - dv.y));
-                pd[2 * i4 + 1] = pack_bf16x2(x[i + 2] * (dp[i + 2] - dv.z), x[i + 3] * (dp[i + 3] - dv.w));
+            for (int c = 0; c < 2; ++c) {
+                uint32_t r[32];
+                tmem_ld32(dp_tm + 32 * c, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i4 = 0; i4 < 8; ++i4) {
+                    const float4 dv = d4[8 * c + i4];
+                    const int i = 32 * c + 4 * i4, k = 16 * c + 2 * i4;
+                    pp[k] = pack_bf16x2(x[i], x[i + 1]);
+                    pp[k + 1] = pack_bf16x2(x[i + 2], x[i + 3]);
+                    pd[k] = pack_bf16x2(x[i] * (__uint_as_float(r[4 * i4]) - dv.x),
+                                        x[i + 1] * (__uint_as_float(r[4 * i4 + 1]) - dv.y));
+                    pd[k + 1] = pack_bf16x2(x[i + 2] * (__uint_as_float(r[4 * i4 + 2]) - dv.z),
+                                            x[i + 3] * (__uint_as_float(r[4 * i4 + 3]) - dv.w));
+                }
             }
             tmem_st32(dp_tm, pp);       // P^T over the first 32 of my own dP^T columns
             tmem_st32(dp_tm + 32, pd);  // dS^T over the other 32
