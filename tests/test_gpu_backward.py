@@ -63,6 +63,8 @@ CASES = [
     (2, 2, 512, 64, 2, 0, 1, 1.0),             # MHA d = 64, contiguous, unscaled scores
     (3, 1, 768, 128, 3, 1, 0, 128 ** -0.5),    # g = 3, non-causal
     (8, 2, 2048, 128, 4, 1, 1, 128 ** -0.5),   # the 4-rank zigzag GQA shape
+    (4, 1, 512, 128, 1, 0, 1, 128 ** -0.5),    # one rank (no ring), one KV head for all queries
+    (2, 2, 256, 64, 1, 1, 1, 0.125),           # smallest zigzag: one 128-row tile per chunk
 ]
 
 
