@@ -249,6 +249,16 @@ int ringattn_bwd(const void* q, const void* k, const void* v, const float* out, 
                  int Hkv, int d, int c, int causal, int layout, int kv_block, ra_stream_t stream);
 
 /*
+ * ringattn_bwd_natural -- as ringattn_bwd with every tensor (q, k, v, out, lse, dout, dq, dk,
+ * dv, delta) in NATURAL sequence order: the chunk map is applied in the kernels' tile
+ * addressing, as in ringattn_fwd_natural.  Same result, same requirements.
+ */
+int ringattn_bwd_natural(const void* q, const void* k, const void* v, const float* out,
+                         const float* lse, const void* dout, float* dq, float* dk, float* dv,
+                         float* delta, int S, int Hq, int Hkv, int d, int c, int causal, int layout,
+                         int kv_block, ra_stream_t stream);
+
+/*
  * ringattn_fwd_natural -- as ringattn_fwd, but q, k, v, out and lse are in NATURAL
  * sequence order: the zigzag/contiguous chunk map is applied in the kernel's tile
  * addressing, so no permutation pass is needed.  Same result, same requirements.

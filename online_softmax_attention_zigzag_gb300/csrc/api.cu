@@ -486,9 +486,13 @@ int ringattn_ulysses_fwd(const void* q_seq, const void* k_seq, const void* v_seq
     return RA_OK;
 }
 
-int ringattn_bwd(const void* q, const void* k, const void* v, const float* out, const float* lse, const void* dout,
-                 float* dq, float* dk, float* dv, float* delta, int S, int Hq, int Hkv, int d, int c, int causal,
-                 int layout, int kv_block, ra_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int bwd_bf16(const void* q, const void* k, const void* v, const float* out, const float* lse, const void* dout,
+             float* dq, float* dk, float* dv, float* delta, int S, int Hq, int Hkv, int d, int c, int causal,
+             int layout, int kv_block, int natural, cudaStream_t stream) {
     if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !delta) return RA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) || !aligned16(dout) ||
         !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(delta))
@@ -503,7 +507,7 @@ int ringattn_bwd(const void* q, const void* k, const void* v, const float* out, 
     if ((st = get_encoder()) != RA_OK) return st;
     ra::AttnBwdParams p;
     p.ring = R;
-    p.natural = 0;
+    p.natural = natural;
     p.n_tiles = S / 128;
     p.n_items = 0;
     p.lse = lse;
@@ -520,9 +524,25 @@ int ringattn_bwd(const void* q, const void* k, const void* v, const float* out, 
         encode_bf16_map(&tv, v, static_cast<long long>(Hkv) * S, d, 64) != RA_OK ||
         encode_bf16_map(&tdo, dout, static_cast<long long>(Hq) * S, d, 64) != RA_OK)
         return RA_ERR_CUDA;
-    return ra::launch_attn_bwd(p, out, dout, tq, tk, tv, tdo, dev->sms, reinterpret_cast<cudaStream_t>(stream)) == 0
-               ? RA_OK
-               : RA_ERR_CUDA;
+    return ra::launch_attn_bwd(p, out, dout, tq, tk, tv, tdo, dev->sms, stream) == 0 ? RA_OK : RA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ringattn_bwd(const void* q, const void* k, const void* v, const float* out, const float* lse, const void* dout,
+                 float* dq, float* dk, float* dv, float* delta, int S, int Hq, int Hkv, int d, int c, int causal,
+                 int layout, int kv_block, ra_stream_t stream) {
+    return bwd_bf16(q, k, v, out, lse, dout, dq, dk, dv, delta, S, Hq, Hkv, d, c, causal, layout, kv_block, 0,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ringattn_bwd_natural(const void* q, const void* k, const void* v, const float* out, const float* lse,
+                         const void* dout, float* dq, float* dk, float* dv, float* delta, int S, int Hq, int Hkv,
+                         int d, int c, int causal, int layout, int kv_block, ra_stream_t stream) {
+    return bwd_bf16(q, k, v, out, lse, dout, dq, dk, dv, delta, S, Hq, Hkv, d, c, causal, layout, kv_block, 1,
+                    reinterpret_cast<cudaStream_t>(stream));
 }
 
 int ringattn_fwd_natural(const void* q, const void* k, const void* v, float* out, float* lse, int S, int Hq,

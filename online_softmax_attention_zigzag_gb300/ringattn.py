@@ -31,7 +31,7 @@ EXPORTS = (
     "ringattn_sync_status", "ringattn_selftest_timeout", "ringattn_strerror", "ringattn_last_timeout",
     "ringattn_fwd_rank", "ringattn_fwd_docmask", "ringattn_fwd_docmask_noalloc",
     "ringattn_fwd_host", "ringattn_host_workspace_bytes", "ringattn_relayout", "ringattn_ulysses_fwd",
-    "ringattn_bwd",
+    "ringattn_bwd", "ringattn_bwd_natural",
 )
 
 # Longest sequence ringattn_fwd_docmask_noalloc takes (its static scratch, int32 [S]).
@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
             "ringattn_host_workspace_bytes": [_I, _I, _I, _I, _P],
             "ringattn_relayout": [_P, _P, _I, _I, _I, _I, _I, _I, _P],
             "ringattn_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P],
+            "ringattn_bwd_natural": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P],
             "ringattn_ulysses_fwd": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _LL, _P],
             "ringattn_fwd_f32": _ATTN + [_P],
             "ringattn_fwd_hop": _ATTN + [_I, _I, _P],
@@ -245,10 +246,12 @@ def ulysses_fwd(q_seq, k_seq, v_seq, out_seq, lse_seq, workspace, *, c, causal, 
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
-def bwd(q, k, v, out, lse, dout, dq, dk, dv, delta, *, c, causal, layout, kv_block, stream=None) -> None:
-    """ringattn_bwd: gradients of :func:`fwd` (rank-major tensors).  q, dout [Hq, S, d] and
-    k, v [Hkv, S, d] bf16; out [Hq, S, d], lse [Hq, S] fp32 from the forward; dq, dk, dv
-    fp32 like q, k, v; delta [Hq, S] fp32 scratch."""
+def bwd(q, k, v, out, lse, dout, dq, dk, dv, delta, *, c, causal, layout, kv_block, stream=None,
+        natural=False) -> None:
+    """ringattn_bwd (rank-major tensors) or, with natural=True, ringattn_bwd_natural
+    (natural order): gradients of the forward.  q, dout [Hq, S, d] and k, v [Hkv, S, d] bf16;
+    out [Hq, S, d], lse [Hq, S] fp32 from the forward; dq, dk, dv fp32 like q, k, v; delta
+    [Hq, S] fp32 scratch."""
     ptrs, S, Hq, Hkv, d = _attn_args(q, k, v, out, lse, torch.bfloat16)
     if tuple(dout.shape) != (Hq, S, d) or tuple(dq.shape) != (Hq, S, d):
         raise ValueError("dout and dq must be [Hq, S, d]")
@@ -256,7 +259,8 @@ def bwd(q, k, v, out, lse, dout, dq, dk, dv, delta, *, c, causal, layout, kv_blo
         raise ValueError("dk, dv must be [Hkv, S, d] and delta [Hq, S]")
     ptrs += [_dev(dout, "dout", torch.bfloat16), _dev(dq, "dq", torch.float32), _dev(dk, "dk", torch.float32),
              _dev(dv, "dv", torch.float32), _dev(delta, "delta", torch.float32)]
-    _check("ringattn_bwd", lib().ringattn_bwd(*ptrs, S, Hq, Hkv, d, c, causal, layout, kv_block, _stream(stream)))
+    name = "ringattn_bwd_natural" if natural else "ringattn_bwd"
+    _check(name, getattr(lib(), name)(*ptrs, S, Hq, Hkv, d, c, causal, layout, kv_block, _stream(stream)))
 
 
 def fwd_natural(q, k, v, out, lse, *, c, causal, layout, kv_block, stream=None) -> None:
@@ -358,28 +362,16 @@ def attention(q, k, v, *, c, causal, layout, kv_block, stream=None):
 
 
 def attention_backward(q, k, v, out, lse, dout, *, c, causal, layout, kv_block, stream=None):
-    """Natural-order convenience call for the backward pass: permute the inputs to
-    rank-major, run ringattn_bwd, permute the gradients back.  ``out`` and ``lse`` are
+    """Natural-order convenience call for the backward pass (ringattn_bwd_natural: the
+    chunk map is applied in the kernels' addressing).  ``out`` and ``lse`` are
     :func:`attention`'s results for q, k, v.  Returns (dq, dk, dv), fp32, natural order."""
     Hq, S, d = q.shape
     Hkv = k.shape[0]
     dev = q.device
-
-    def rm(x):
-        y = torch.empty_like(x)
-        permute(x, y, c=c, layout=layout, inverse=0, stream=stream)
-        return y
-
-    qr, kr, vr, o_r, l_r, do_r = (rm(x) for x in (q, k, v, out, lse, dout))
-    dq_r = torch.empty((Hq, S, d), dtype=torch.float32, device=dev)
-    dk_r = torch.empty((Hkv, S, d), dtype=torch.float32, device=dev)
-    dv_r = torch.empty_like(dk_r)
+    dq = torch.empty((Hq, S, d), dtype=torch.float32, device=dev)
+    dk = torch.empty((Hkv, S, d), dtype=torch.float32, device=dev)
+    dv = torch.empty_like(dk)
     delta = torch.empty((Hq, S), dtype=torch.float32, device=dev)
-    bwd(qr, kr, vr, o_r, l_r, do_r, dq_r, dk_r, dv_r, delta, c=c, causal=causal, layout=layout,
-        kv_block=kv_block, stream=stream)
-    res = []
-    for x in (dq_r, dk_r, dv_r):
-        y = torch.empty_like(x)
-        permute(x, y, c=c, layout=layout, inverse=1, stream=stream)
-        res.append(y)
-    return tuple(res)
+    bwd(q, k, v, out, lse, dout, dq, dk, dv, delta, c=c, causal=causal, layout=layout, kv_block=kv_block,
+        stream=stream, natural=True)
+    return dq, dk, dv

@@ -153,3 +153,25 @@ def test_natural_order_helpers_forward_and_backward(ra):
                              obwd.grad_abs_sums(*args, True, out=o64)):
         excess = np.abs(g.cpu().double().numpy() - w) - REL * a
         assert excess.max() <= 1e-6 * a.max(), name
+
+
+def test_natural_order_backward_equals_rank_major(ra):
+    """ringattn_bwd_natural (chunk map in the kernels' addressing) gives bitwise the
+    gradients of ringattn_bwd on rank-major tensors, for both layouts."""
+    Hq, Hkv, S, d, c = 8, 2, 2048, 128, 4
+    q, k, v = _randn((Hq, S, d), 241, 128 ** -0.5), _randn((Hkv, S, d), 242), _randn((Hkv, S, d), 243)
+    dout = _randn((Hq, S, d), 244)
+    out, lse = _forward_oracle(q, k, v, 1)
+    for layout in (0, 1):
+        kvb = S // (c * (2 if layout else 1))
+        want = _gpu_bwd(ra, q, k, v, dout, out, lse, c, layout, 1, kvb)
+        dq = torch.empty((Hq, S, d), dtype=torch.float32, device=dev())
+        dk = torch.empty((Hkv, S, d), dtype=torch.float32, device=dev())
+        dv = torch.empty_like(dk)
+        delta = torch.empty((Hq, S), dtype=torch.float32, device=dev())
+        ra.bwd(q.to(dev()), k.to(dev()), v.to(dev()), out.to(torch.float32).to(dev()),
+               lse.to(torch.float32).to(dev()), dout.to(dev()), dq, dk, dv, delta, c=c, causal=1,
+               layout=layout, kv_block=kvb, natural=True)
+        assert ra.sync_status() == ra.RA_OK
+        for g, w in zip((dq, dk, dv), want):
+            assert torch.equal(g.cpu(), w)
