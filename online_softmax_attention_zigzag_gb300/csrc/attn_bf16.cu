@@ -230,21 +230,6 @@ __device__ __forceinline__ int count_kv_tiles(const AttnBf16Params& p, const Ite
     }
 }
 
-// Snake order over persistent CTAs: items are sorted by decreasing work, so
-// alternating the direction each round evens out the totals.
-__device__ __forceinline__ int item_of_round(int round) {
-    const int b = (round & 1) ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;
-    return round * gridDim.x + b;
-}
-
-// Bounded wait that ignores the abort flag (used to drain in-flight work on abort).
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > timeout_ns) return;
-    }
-}
-
 // ------------------------------------------------------------------ TMA producer
 template <int D, bool DOC>
 __device__ void load_role(const AttnBf16Params& p, const CUtensorMap* tq, const CUtensorMap* tk,
@@ -301,14 +286,6 @@ __device__ void load_role(const AttnBf16Params& p, const CUtensorMap* tq, const 
 }
 
 // ------------------------------------------------------------------ MMA issuer
-// desc + off computed where it is used: an opaque add keeps the compiler from hoisting
-// every (descriptor, K-slice) pair out of the loops into registers.
-__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t off16) {
-    uint64_t r;
-    asm volatile("add.s64 %0, %1, %2;" : "=l"(r) : "l"(desc), "l"(static_cast<uint64_t>(off16)));
-    return r;
-}
-
 template <int D>
 __device__ __forceinline__ void issue_s(uint32_t tmem, int x, uint32_t q_base, uint32_t k_base) {
     using C = Cfg<D>;
@@ -423,16 +400,7 @@ __device__ void mma_role(const AttnBf16Params& p, uint8_t* sQ, uint8_t* sKV, con
 // ------------------------------------------------------------------ softmax warpgroups
 // Named barrier over the two warpgroups (256 threads) that share query tile x; returns
 // the AND of every thread's `ok`, so that both halves leave together on an abort.
-__device__ __forceinline__ bool unit_bar_and(int x, bool ok) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.and.pred po, %2, 256, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"(ok ? 1u : 0u), "r"(1 + x)
-        : "memory");
-    return r != 0;
-}
+__device__ __forceinline__ bool unit_bar_and(int x, bool ok) { return named_bar_and(1 + x, 256, ok); }
 
 // One warpgroup owns column half h (keys [64h, 64h+64) of every key tile) of query tile
 // x; thread t of the warpgroup owns row t.  The two halves of a tile exchange their

@@ -144,35 +144,8 @@ __device__ __forceinline__ int count_query_tiles(const Ring& R, int hk, int kp) 
     return n;
 }
 
-__device__ __forceinline__ int item_of_round(int round) {
-    const int b = (round & 1) ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;
-    return round * gridDim.x + b;
-}
-
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > timeout_ns) return;
-    }
-}
-
 // Named barrier over one compute warpgroup (128 threads); returns the AND of `ok`.
-__device__ __forceinline__ bool group_bar_and(int h, bool ok) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.and.pred po, %2, 128, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"(ok ? 1u : 0u), "r"(1 + h)
-        : "memory");
-    return r != 0;
-}
-
-__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t off16) {
-    uint64_t r;
-    asm volatile("add.s64 %0, %1, %2;" : "=l"(r) : "l"(desc), "l"(static_cast<uint64_t>(off16)));
-    return r;
-}
+__device__ __forceinline__ bool group_bar_and(int h, bool ok) { return named_bar_and(1 + h, 128, ok); }
 
 // D[tmem] = A B^T with A (128 x D) and B (128 x D) both K-major in shared memory (128-byte
 // swizzle, 64-column boxes): the 128 x 128 tile products S, dP, S^T, dP^T.

@@ -89,6 +89,34 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     }
 }
 
+// Bounded wait that ignores the abort flag (used to drain in-flight work on abort).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > timeout_ns) return;
+    }
+}
+
+// Named barrier `id` over `nthreads` threads (a multiple of 32); returns the AND of every
+// participating thread's `ok`, so that a failed wait reaches the whole group.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.and.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(ok ? 1u : 0u), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
+// Persistent CTAs take work items in snake order: round k of CTA b is item k * grid + b,
+// reversed on odd rounds, so items sorted by decreasing work even out across CTAs.
+__device__ __forceinline__ int item_of_round(int round) {
+    const int b = (round & 1) ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;
+    return round * gridDim.x + b;
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x,
                                             int y) {
@@ -195,6 +223,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) 
            | (static_cast<uint32_t>(b_mn_major) << 16)  // B major-ness
            | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+// desc + off computed where it is used: an opaque add keeps the compiler from hoisting
+// every (descriptor, K-slice) pair out of the loops into registers.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t off16) {
+    uint64_t r;
+    asm volatile("add.s64 %0, %1, %2;" : "=l"(r) : "l"(desc), "l"(static_cast<uint64_t>(off16)));
+    return r;
 }
 
 // Shared-memory matrix descriptor with 128-byte swizzle.
