@@ -128,6 +128,55 @@ __global__ void __launch_bounds__(256) merge_kernel(float* __restrict__ o_run, f
     }
 }
 
+// d = 128 (one float4 of each row per lane): a warp takes R consecutive rows per iteration
+// and issues every load of them before any arithmetic, so 2R independent 16-byte loads per
+// lane are in flight (one row at a time left the merge latency-bound at ~71% of HBM).
+template <int R>
+__global__ void __launch_bounds__(256) merge_kernel_d128(float4* __restrict__ o_run, float* __restrict__ lse_run,
+                                                         const float4* __restrict__ o_part,
+                                                         const float* __restrict__ lse_part, long long rows) {
+    const int lane = threadIdx.x & 31;
+    const long long warp = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
+    for (long long r0 = warp * R; r0 < rows; r0 += warps * R) {
+        float4 x[R], y[R];
+        float a[R], b[R];
+#pragma unroll
+        for (int k = 0; k < R; ++k) {
+            const long long row = r0 + k;
+            if (row < rows) {
+                a[k] = lse_run[row];
+                b[k] = lse_part[row];
+                x[k] = o_run[row * 32 + lane];
+                y[k] = o_part[row * 32 + lane];
+            }
+        }
+        float lse_new = 0.f;  // lane k keeps row r0 + k's result
+#pragma unroll
+        for (int k = 0; k < R; ++k) {
+            const long long row = r0 + k;
+            if (row >= rows) break;
+            const float M = fmaxf(a[k], b[k]);
+            float wa = 0.f, wb = 0.f, lse = -INFINITY;
+            if (M != -INFINITY) {  // else neither partial saw a key
+                const float ea = expf(a[k] - M), eb = expf(b[k] - M);  // exp(-inf) = 0: weight 0
+                const float tot = ea + eb;
+                wa = ea / tot;
+                wb = eb / tot;
+                lse = M + logf(tot);
+            }
+            // a side with no key contributes exactly nothing, whatever its o holds
+            const bool ua = a[k] != -INFINITY, ub = b[k] != -INFINITY;
+            o_run[row * 32 + lane] = make_float4(mix(x[k].x, wa, ua, y[k].x, wb, ub), mix(x[k].y, wa, ua, y[k].y, wb, ub),
+                                                 mix(x[k].z, wa, ua, y[k].z, wb, ub), mix(x[k].w, wa, ua, y[k].w, wb, ub));
+            if (lane == k) lse_new = lse;
+        }
+        // every lane has read the R lse values above before any lane writes one back
+        __syncwarp();
+        if (lane < R && r0 + lane < rows) lse_run[r0 + lane] = lse_new;
+    }
+}
+
 // ------------------------------------------------------------------ bounded-wait self test
 __global__ void selftest_timeout_kernel(int* err, unsigned long long timeout_ns) {
     __shared__ __align__(8) uint64_t bar;
@@ -171,7 +220,13 @@ int launch_merge(float* o_run, float* lse_run, const float* o_part, const float*
     const long long cap = static_cast<long long>(sms) * 8;
     if (blocks > cap) blocks = cap;
     const bool vec = (d % 4 == 0) && ((reinterpret_cast<uintptr_t>(o_run) | reinterpret_cast<uintptr_t>(o_part)) & 15) == 0;
-    if (vec)
+    if (vec && d == 128) {
+        constexpr int kRows = 4;
+        long long b4 = (rows + 8 * kRows - 1) / (8 * kRows);
+        if (b4 > cap) b4 = cap;
+        merge_kernel_d128<kRows><<<static_cast<unsigned>(b4), 256, 0, stream>>>(
+            reinterpret_cast<float4*>(o_run), lse_run, reinterpret_cast<const float4*>(o_part), lse_part, rows);
+    } else if (vec)
         merge_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o_run, lse_run, o_part, lse_part, rows, d);
     else
         merge_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o_run, lse_run, o_part, lse_part, rows, d);
