@@ -13,48 +13,48 @@ namespace ra {
 namespace {
 
 // ------------------------------------------------------------------ permutation
-// The tensor is H * nchunks slabs of `slab` bytes.  Work item = one vector of width
-// sizeof(V) inside one destination slab; four independent vectors per thread per
-// iteration keep enough loads in flight to approach the copy bandwidth.
+// The tensor is H * nchunks slabs of `slab` bytes; a chunk moves whole, so the copy is one
+// contiguous slab-to-slab copy per destination slab.  Grid: y (and z) = destination slab,
+// x = blocks sharing it; four independent vectors per thread per iteration keep enough
+// loads in flight to approach the copy bandwidth.
 template <typename V>
-__global__ void __launch_bounds__(256) permute_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+__global__ void __launch_bounds__(256) permute_kernel(const V* __restrict__ src, V* __restrict__ dst,
                                                       long long slab_vecs, int nchunks, int c, int layout,
-                                                      int inverse, long long total_vecs) {
+                                                      int inverse, long long nslabs) {
     constexpr int kUnroll = 4;
+    const long long slab = static_cast<long long>(blockIdx.z) * gridDim.y + blockIdx.y;
+    if (slab >= nslabs) return;
+    const long long h = slab / nchunks;
+    const int dslab = static_cast<int>(slab - h * nchunks);
+    // natural chunk <-> rank-major chunk
+    int sslab;
+    if (layout == 1) {
+        if (!inverse) {  // dst is rank-major: rank-major chunk j = 2r + slot
+            const int r = dslab >> 1, slot = dslab & 1;
+            sslab = slot ? 2 * c - 1 - r : r;
+        } else {         // dst is natural chunk k
+            const int k = dslab;
+            sslab = (k < c) ? 2 * k : 2 * (2 * c - 1 - k) + 1;
+        }
+    } else {
+        sslab = dslab;
+    }
+    const V* sp = src + (h * nchunks + sslab) * slab_vecs;
+    V* dp = dst + slab * slab_vecs;
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-    for (long long base = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; base < total_vecs;
+    for (long long base = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; base < slab_vecs;
          base += stride * kUnroll) {
         V vals[kUnroll];
-        long long dsto[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            const long long i = base + u * stride;  // vector index in the destination
-            dsto[u] = -1;
-            if (i < total_vecs) {
-                const long long slab = i / slab_vecs;
-                const long long off = i - slab * slab_vecs;
-                const long long h = slab / nchunks;
-                const int dslab = static_cast<int>(slab - h * nchunks);
-                // natural chunk <-> rank-major chunk
-                int sslab;
-                if (layout == 1) {
-                    if (!inverse) {  // dst is rank-major: rank-major chunk j = 2r + slot
-                        const int r = dslab >> 1, slot = dslab & 1;
-                        sslab = slot ? 2 * c - 1 - r : r;
-                    } else {         // dst is natural chunk k
-                        const int k = dslab;
-                        sslab = (k < c) ? 2 * k : 2 * (2 * c - 1 - k) + 1;
-                    }
-                } else {
-                    sslab = dslab;
-                }
-                vals[u] = reinterpret_cast<const V*>(src)[(h * nchunks + sslab) * slab_vecs + off];
-                dsto[u] = i;
-            }
+            const long long i = base + u * stride;
+            if (i < slab_vecs) vals[u] = sp[i];
         }
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-            if (dsto[u] >= 0) reinterpret_cast<V*>(dst)[dsto[u]] = vals[u];
+        for (int u = 0; u < kUnroll; ++u) {
+            const long long i = base + u * stride;
+            if (i < slab_vecs) dp[i] = vals[u];
+        }
     }
 }
 
@@ -62,18 +62,23 @@ template <typename V>
 int launch_permute_v(const void* src, void* dst, long long slab_bytes, int H, int nchunks, int c, int layout,
                      int inverse, cudaStream_t stream) {
     const long long slab_vecs = slab_bytes / static_cast<long long>(sizeof(V));
-    const long long total = slab_vecs * H * nchunks;
-    if (total == 0) return 0;
+    const long long nslabs = static_cast<long long>(H) * nchunks;
+    if (slab_vecs == 0 || nslabs == 0) return 0;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // about 8 CTAs of 256 threads per SM in total, but no more than a slab needs
     const long long per_block = 256LL * 4;
-    long long blocks = (total + per_block - 1) / per_block;
-    const long long cap = static_cast<long long>(sms) * 8;  // 8 CTAs of 256 threads per SM
-    if (blocks > cap) blocks = cap;
-    permute_kernel<V><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), slab_vecs, nchunks, c, layout, inverse,
-        total);
+    long long bx = (static_cast<long long>(sms) * 8 + nslabs - 1) / nslabs;
+    const long long need = (slab_vecs + per_block - 1) / per_block;
+    if (bx > need) bx = need;
+    if (bx < 1) bx = 1;
+    const long long gy = nslabs < 65535 ? nslabs : 65535;
+    const long long gz = (nslabs + gy - 1) / gy;
+    if (gz > 65535) return -2;
+    dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(gy), static_cast<unsigned>(gz));
+    permute_kernel<V><<<grid, 256, 0, stream>>>(static_cast<const V*>(src), static_cast<V*>(dst), slab_vecs, nchunks,
+                                               c, layout, inverse, nslabs);
     return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
