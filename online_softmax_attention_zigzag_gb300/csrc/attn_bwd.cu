@@ -747,31 +747,62 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ D = dout . out
-// One warp per row; lane l holds elements [l*E, l*E + E) of the row (E = D / 32).
-template <int D>
+// Lane l holds elements [l*E, l*E + E) of a row (E = D / 32); a warp takes R consecutive rows
+// per iteration and issues all their loads before reducing, so 2R independent loads per lane
+// are in flight (one row at a time leaves an HBM-bound kernel latency-bound).
+template <int D, int R>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* __restrict__ dout,
                                                         const float* __restrict__ out, float* __restrict__ delta,
                                                         long long rows) {
     constexpr int E = D / 32;
     const int lane = threadIdx.x & 31;
+    const long long warp = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
     const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
-    for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; r < rows;
-         r += warps) {
-        const size_t base = static_cast<size_t>(r) * D + lane * E;
-        float acc = 0.f;
+    for (long long r0 = warp * R; r0 < rows; r0 += warps * R) {
+        float acc[R];
         if constexpr (E == 4) {
-            const float4 o = *reinterpret_cast<const float4*>(out + base);
-            const uint2 g = *reinterpret_cast<const uint2*>(dout + base);
-            acc = o.x * __uint_as_float(g.x << 16) + o.y * __uint_as_float(g.x & 0xffff0000u) +
-                  o.z * __uint_as_float(g.y << 16) + o.w * __uint_as_float(g.y & 0xffff0000u);
+            float4 o[R];
+            uint2 g[R];
+#pragma unroll
+            for (int k = 0; k < R; ++k) {
+                if (r0 + k < rows) {
+                    const size_t base = static_cast<size_t>(r0 + k) * D + lane * E;
+                    o[k] = *reinterpret_cast<const float4*>(out + base);
+                    g[k] = *reinterpret_cast<const uint2*>(dout + base);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < R; ++k)
+                acc[k] = (r0 + k < rows)
+                             ? o[k].x * __uint_as_float(g[k].x << 16) + o[k].y * __uint_as_float(g[k].x & 0xffff0000u) +
+                                   o[k].z * __uint_as_float(g[k].y << 16) + o[k].w * __uint_as_float(g[k].y & 0xffff0000u)
+                             : 0.f;
         } else {
-            const float2 o = *reinterpret_cast<const float2*>(out + base);
-            const uint32_t g = *reinterpret_cast<const uint32_t*>(dout + base);
-            acc = o.x * __uint_as_float(g << 16) + o.y * __uint_as_float(g & 0xffff0000u);
+            float2 o[R];
+            uint32_t g[R];
+#pragma unroll
+            for (int k = 0; k < R; ++k) {
+                if (r0 + k < rows) {
+                    const size_t base = static_cast<size_t>(r0 + k) * D + lane * E;
+                    o[k] = *reinterpret_cast<const float2*>(out + base);
+                    g[k] = *reinterpret_cast<const uint32_t*>(dout + base);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < R; ++k)
+                acc[k] = (r0 + k < rows) ? o[k].x * __uint_as_float(g[k] << 16) + o[k].y * __uint_as_float(g[k] & 0xffff0000u)
+                                         : 0.f;
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) delta[r] = acc;
+        for (int k = 0; k < R; ++k)
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], off);
+        if (lane < R && r0 + lane < rows) {
+            float v = acc[0];
+#pragma unroll
+            for (int k = 1; k < R; ++k) v = (lane == k) ? acc[k] : v;
+            delta[r0 + lane] = v;
+        }
     }
 }
 
@@ -781,9 +812,10 @@ int launch_bwd_d(const AttnBwdParams& p0, const float* out, const void* dout, co
     using C = BwdCfg<D>;
     const Ring& R = p0.ring;
     const long long rows = static_cast<long long>(R.Hq) * R.S;
-    long long blocks = (rows + 7) / 8;
-    if (blocks > static_cast<long long>(sms) * 16) blocks = static_cast<long long>(sms) * 16;
-    bwd_delta_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+    constexpr int kRows = 4;
+    long long blocks = (rows + 8 * kRows - 1) / (8 * kRows);
+    if (blocks > static_cast<long long>(sms) * 8) blocks = static_cast<long long>(sms) * 8;
+    bwd_delta_kernel<D, kRows><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
         static_cast<const uint16_t*>(dout), out, const_cast<float*>(p0.delta), rows);
     if (cudaGetLastError() != cudaSuccess) return -4;
 
