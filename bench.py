@@ -624,6 +624,10 @@ def main():
                     "ms_per_step": e2e_ms, "steps": e2e_steps,
                     "ms_per_step_min": min(e2e_each), "ms_per_step_median": float(np.median(e2e_each)),
                     "call": "ringattn_fwd_host (natural order; copies overlapped with attention by KV-head groups)"},
+            "context": {"overlap_condition_tokens_per_block": {
+                "pages_H100_989TFLOPs_over_450GBs_NVLink": 2198,
+                "GB300_nominal_2250TFLOPs_over_900GBs_NVLink5": 2500,
+                "GB300_at_this_kernel_rate": round(achieved * 1e12 / 900e9)}},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
         }
