@@ -22,7 +22,8 @@
 //     head; items are ordered KV-head-major, then by decreasing causal work;
 //   * warp 17 (one thread) streams Q tiles and, in visiting order, K and V tiles into
 //     shared memory with TMA (128-byte swizzle), through a ring of stages guarded by
-//     mbarriers;
+//     mbarriers; a stage pairs the V tile of one key tile with the K tile of the next,
+//     which is what the MMA issuer consumes together (one wait, one release per tile);
 //   * warp 16 (one thread) issues tcgen05.mma: S_x = Q_x K^T into TMEM, and after
 //     softmax O_x += P_x V with P_x read from TMEM;
 //   * warps 0-15 are four softmax warpgroups, two per unit, each owning 64 of the 128
@@ -58,10 +59,12 @@ struct Cfg {
     static constexpr int kTileBytes = kTile * D * 2;   // one 128 x D bf16 tile
     static constexpr int kBoxBytes = kTile * 64 * 2;   // one 128 x 64 TMA box (16 KB)
     static constexpr int kBoxes = D / 64;
-    static constexpr int kStages = (D == 128) ? 4 : 8;  // K/V tiles in flight (128 KB)
+    // A stage holds the V tile of one key tile and the K tile of the next (128 KB in all).
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kStages = (D == 128) ? 2 : 4;
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = 2 * kTileBytes;
-    static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+    static constexpr int kBarOff = kKVOff + kStages * kStageBytes;
     static constexpr int kNumBars = 13 + 2 * kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kXchgOff = kMiscOff + 16;              // softmax exchange: 2 x 8 x 128 floats
@@ -231,15 +234,30 @@ __device__ __forceinline__ int count_kv_tiles(const AttnBf16Params& p, const Ite
 }
 
 // ------------------------------------------------------------------ TMA producer
+// Stage sequence of an item with n key tiles: K(0); then V(j-1) with K(j) for j = 1..n-1;
+// then V(n-1).  V sits at the stage base, K one tile above it.
 template <int D, bool DOC>
 __device__ void load_role(const AttnBf16Params& p, const CUtensorMap* tq, const CUtensorMap* tk,
                           const CUtensorMap* tv, uint8_t* sQ, uint8_t* sKV, const Bars& b, const WaitCtl& wc) {
     using C = Cfg<D>;
-    uint32_t kv_idx = 0, qit[2] = {0, 0};
+    uint32_t st_idx = 0, qit[2] = {0, 0};
     bool ok = true;
     // K/V tiles are re-read by every query tile of their head group: keep them in L2;
     // Q tiles are read once: let them go first
     const uint64_t keep = make_policy_evict_last(), stream = make_policy_evict_first();
+    // wait for the next stage to be empty and announce the bytes it will receive
+    auto claim = [&](uint32_t bytes, uint32_t& s) -> bool {
+        s = st_idx % C::kStages;
+        if (!mbar_wait(&b.kv_empty[s], ((st_idx / C::kStages) & 1u) ^ 1u, wc, 32)) return false;
+        mbar_arrive_expect_tx(&b.kv_full[s], bytes);
+        ++st_idx;
+        return true;
+    };
+    auto load_tile = [&](uint32_t s, int off, const CUtensorMap* map, int row) {
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_2d_hint(sKV + s * C::kStageBytes + off + bx * C::kBoxBytes, map, &b.kv_full[s], bx * 64, row,
+                             keep);
+    };
     for (int round = 0; ok; ++round) {
         if (round * (int)gridDim.x >= p.n_items) break;
         const int item = item_of_round(round);
@@ -260,24 +278,24 @@ __device__ void load_role(const AttnBf16Params& p, const CUtensorMap* tq, const 
                 tma_load_2d_hint(sQ + x * C::kTileBytes + bx * C::kBoxBytes, tq, &b.q_full[x], bx * 64, qrow, stream);
         }
         if (!ok) break;
+        int prev = -1;  // row of the previous tile, whose V goes with this tile's K
         for_each_kv_tile<DOC>(p, it, [&](int row, int) -> bool {
-            for (int kv = 0; kv < 2; ++kv) {
-                const uint32_t s = kv_idx % C::kStages;
-                if (!mbar_wait(&b.kv_empty[s], ((kv_idx / C::kStages) & 1u) ^ 1u, wc, 32)) { ok = false; return false; }
-                mbar_arrive_expect_tx(&b.kv_full[s], C::kTileBytes);
-                const CUtensorMap* map = kv ? tv : tk;
-                for (int bx = 0; bx < C::kBoxes; ++bx)
-                    tma_load_2d_hint(sKV + s * C::kTileBytes + bx * C::kBoxBytes, map, &b.kv_full[s], bx * 64, row,
-                                     keep);
-                ++kv_idx;
-            }
+            uint32_t s;
+            if (!claim(prev < 0 ? C::kTileBytes : C::kStageBytes, s)) { ok = false; return false; }
+            if (prev >= 0) load_tile(s, 0, tv, prev);
+            load_tile(s, C::kTileBytes, tk, row);
+            prev = row;
             return true;
         });
+        if (!ok) break;
+        uint32_t s;
+        if (!claim(C::kTileBytes, s)) { ok = false; break; }
+        load_tile(s, 0, tv, prev);
     }
     if (!ok) {
         // let every copy already issued land before the CTA's shared memory goes away
-        for (uint32_t s = 0; s < (uint32_t)C::kStages && s < kv_idx; ++s) {
-            const uint32_t last = kv_idx - 1 - ((kv_idx - 1 - s) % C::kStages);
+        for (uint32_t s = 0; s < (uint32_t)C::kStages && s < st_idx; ++s) {
+            const uint32_t last = st_idx - 1 - ((st_idx - 1 - s) % C::kStages);
             drain_wait(&b.kv_full[s], (last / C::kStages) & 1u, wc.timeout_ns);
         }
         for (int x = 0; x < 2; ++x)
@@ -286,18 +304,46 @@ __device__ void load_role(const AttnBf16Params& p, const CUtensorMap* tq, const 
 }
 
 // ------------------------------------------------------------------ MMA issuer
+// The two halves of a 128-byte-swizzle descriptor: the low word carries (address >> 4)
+// and the leading byte offset, the high word the stride, version and swizzle, which are
+// the same for every operand here.
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t smem_addr, uint32_t lbo) {
+    return ((smem_addr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+constexpr uint32_t kSdescHi = (1024u >> 4) | (1u << 14) | (2u << 29);  // sbo 1024 B, version 1, 128 B swizzle
+
+// Eight MMAs along K into one accumulator, descriptors stepped in their low words.
+__device__ __forceinline__ void mma_ss8(uint32_t d_tmem, uint32_t alo, uint32_t blo, uint32_t idesc, uint32_t acc,
+                                        uint32_t step_lo4, uint32_t step_box) {
+    // K slice kk sits at byte offset (kk / 4) * box + (kk % 4) * 32
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk / 4) * step_box + (kk % 4) * step_lo4;
+        asm volatile(
+            "{\n\t.reg .b64 da, db;\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "mov.b64 da, {%1, %5};\n\tmov.b64 db, {%2, %5};\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+            "r"(alo + off), "r"(blo + off), "r"(idesc), "r"(kk > 0 ? 1u : acc), "r"(kSdescHi)
+            : "memory");
+    }
+}
+
 template <int D>
 __device__ __forceinline__ void issue_s(uint32_t tmem, int x, uint32_t q_base, uint32_t k_base) {
     using C = Cfg<D>;
+    static_assert(D == 128 || D == 64, "head dimension");
     constexpr uint32_t idesc = idesc_bf16(kTile, kTile, 0);
     const uint32_t d_tmem = tmem + x * kTile;
-    // the start-address field holds (address >> 4): step it in place per K slice
-    const uint64_t qd = sdesc_sw128(q_base, 16, 1024);
-    const uint64_t kd = sdesc_sw128(k_base, 16, 1024);
+    const uint32_t qlo = sdesc_lo(q_base, 16), klo = sdesc_lo(k_base, 16);
+    if constexpr (D == 128) {
+        mma_ss8(d_tmem, qlo, klo, idesc, 0u, 32 >> 4, C::kBoxBytes >> 4);
+    } else {
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = ((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4;
-        mma_ss(d_tmem, desc_add(qd, off), desc_add(kd, off), idesc, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t off = (kk * 32) >> 4;
+            mma_ss(d_tmem, (static_cast<uint64_t>(kSdescHi) << 32) | (qlo + off),
+                   (static_cast<uint64_t>(kSdescHi) << 32) | (klo + off), idesc, kk > 0 ? 1u : 0u);
+        }
     }
 }
 
@@ -307,11 +353,17 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, int x, uint32_t v_base, 
     constexpr uint32_t idesc = idesc_bf16(kTile, D, 1);
     const uint32_t d_tmem = tmem + C::kOCol + x * D;
     const uint32_t a_tmem = tmem + x * kTile + 64;
-    const uint64_t vd = sdesc_sw128(v_base, C::kBoxBytes, 1024);
+    const uint32_t vlo = sdesc_lo(v_base, C::kBoxBytes);
+    const uint32_t acc = accumulate ? 1u : 0u;
 #pragma unroll
     for (int kk = 0; kk < kTile / 16; ++kk) {
-        mma_ts(d_tmem, a_tmem + kk * 8, desc_add(vd, (kk * 16 * 128) >> 4), idesc,
-               (accumulate || kk > 0) ? 1u : 0u);
+        asm volatile(
+            "{\n\t.reg .b64 db;\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "mov.b64 db, {%2, %5};\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
+            "r"(a_tmem + kk * 8), "r"(vlo + ((kk * 16 * 128) >> 4)), "r"(idesc), "r"(kk > 0 ? 1u : acc),
+            "r"(kSdescHi)
+            : "memory");
     }
 }
 
@@ -320,8 +372,16 @@ __device__ void mma_role(const AttnBf16Params& p, uint8_t* sQ, uint8_t* sKV, con
                          const WaitCtl& wc) {
     using C = Cfg<D>;
     const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
-    uint32_t kv_idx = 0, qit[2] = {0, 0}, pit[2] = {0, 0};
+    uint32_t st_idx = 0, qit[2] = {0, 0}, pit[2] = {0, 0};
     bool ok = true;
+    // wait for the next stage to be loaded; base = its shared-memory address
+    auto wait_stage = [&](uint32_t& s, uint32_t& base) -> bool {
+        s = st_idx % C::kStages;
+        base = sKVa + s * C::kStageBytes;
+        const bool r = mbar_wait(&b.kv_full[s], (st_idx / C::kStages) & 1u, wc);
+        ++st_idx;
+        return r;
+    };
     for (int round = 0; ok; ++round) {
         if (round * (int)gridDim.x >= p.n_items) break;
         const int item = item_of_round(round);
@@ -335,29 +395,25 @@ __device__ void mma_role(const AttnBf16Params& p, uint8_t* sQ, uint8_t* sKV, con
         for (int x = 0; x < 2; ++x)
             if (x < nx && ok && !mbar_wait(&b.q_full[x], qit[x] & 1u, wc)) ok = false;
         if (!ok) break;
-        // S(0)
-        uint32_t ks = kv_idx % C::kStages;
-        if (!mbar_wait(&b.kv_full[ks], (kv_idx / C::kStages) & 1u, wc)) { ok = false; break; }
-        ++kv_idx;
+        // S(0) from the stage holding K(0) alone
+        uint32_t s, base;
+        if (!wait_stage(s, base)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
             if (x >= nx) break;
-            issue_s<D>(tmem, x, sQa + x * C::kTileBytes, sKVa + ks * C::kTileBytes);
+            issue_s<D>(tmem, x, sQa + x * C::kTileBytes, base + C::kTileBytes);
             mma_commit(&b.s_full[x]);
         }
-        mma_commit(&b.kv_empty[ks]);
+        mma_commit(&b.kv_empty[s]);
         if (nj == 1)
 #pragma unroll
             for (int x = 0; x < 2; ++x)
                 if (x < nx) mma_commit(&b.q_empty[x]);
         for (int j = 0; j < nj && ok; ++j) {
-            const uint32_t vs = kv_idx % C::kStages;
-            if (!mbar_wait(&b.kv_full[vs], (kv_idx / C::kStages) & 1u, wc)) { ok = false; break; }
-            ++kv_idx;
+            // this stage holds V(j) and, unless j is the last tile, K(j+1)
+            if (!wait_stage(s, base)) { ok = false; break; }
             const bool more = (j + 1 < nj);
-            const uint32_t ks2 = kv_idx % C::kStages;
-            const uint32_t ks2_par = (kv_idx / C::kStages) & 1u;
 #pragma unroll
             for (int x = 0; x < 2; ++x) {
                 if (x >= nx) break;
@@ -365,27 +421,20 @@ __device__ void mma_role(const AttnBf16Params& p, uint8_t* sQ, uint8_t* sKV, con
                 ++pit[x];
                 if (j == 0 && !mbar_wait(&b.o_free[x], (qit[x] & 1u) ^ 1u, wc)) { ok = false; break; }
                 tc_fence_after();
-                issue_pv<D>(tmem, x, sKVa + vs * C::kTileBytes, j > 0);
-                if (!more) mma_commit(&b.o_done[x]);
+                issue_pv<D>(tmem, x, base, j > 0);
                 if (more) {
-                    if (x == 0) {
-                        if (!mbar_wait(&b.kv_full[ks2], ks2_par, wc)) { ok = false; break; }
-                        tc_fence_after();
-                    }
-                    issue_s<D>(tmem, x, sQa + x * C::kTileBytes, sKVa + ks2 * C::kTileBytes);
+                    issue_s<D>(tmem, x, sQa + x * C::kTileBytes, base + C::kTileBytes);
                     mma_commit(&b.s_full[x]);
+                } else {
+                    mma_commit(&b.o_done[x]);
                 }
             }
             if (!ok) break;
-            mma_commit(&b.kv_empty[vs]);
-            if (more) {
-                ++kv_idx;
-                mma_commit(&b.kv_empty[ks2]);
-                if (j + 2 == nj)
+            mma_commit(&b.kv_empty[s]);
+            if (j + 2 == nj)
 #pragma unroll
-                    for (int x = 0; x < 2; ++x)
-                        if (x < nx) mma_commit(&b.q_empty[x]);
-            }
+                for (int x = 0; x < 2; ++x)
+                    if (x < nx) mma_commit(&b.q_empty[x]);
         }
         qit[0] += 1;
         qit[1] += (nx > 1) ? 1u : 0u;
