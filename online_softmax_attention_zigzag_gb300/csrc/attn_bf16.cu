@@ -16,22 +16,24 @@
 // touches, and a key is visible to a row when it lies between the start of the row's
 // document and the row itself.
 //
-// Design (one CTA per SM, persistent, 576 threads):
+// Design (one CTA per SM, persistent, 352 threads):
 //   * a work item is two 128-row query tiles (units) that share every K/V tile: two
 //     query heads of one KV group at the same positions, or two adjacent tiles of one
 //     head; items are ordered KV-head-major, then by decreasing causal work;
-//   * warp 17 (one thread) streams Q tiles and, in visiting order, K and V tiles into
+//   * warp 10 (one thread) streams Q tiles and, in visiting order, K and V tiles into
 //     shared memory with TMA (128-byte swizzle), through a ring of stages guarded by
 //     mbarriers; a stage pairs the V tile of one key tile with the K tile of the next,
-//     which is what the MMA issuer consumes together (one wait, one release per tile);
-//   * warp 16 (one thread) issues tcgen05.mma: S_x = Q_x K^T into TMEM, and after
-//     softmax O_x += P_x V with P_x read from TMEM;
-//   * warps 0-15 are four softmax warpgroups, two per unit, each owning 64 of the 128
-//     key columns of its unit's score tile (thread = row).  They read S from TMEM,
-//     mask, exchange partial row maxima through shared memory, update the running max
-//     and sums with exp2, write P (bf16) back to TMEM, rescale O in TMEM when the
-//     running max rose by more than 2^8, and at the end write out = O / (sum of the
-//     bf16 P) and lse = m + ln(sum of the exact p).
+//     which is what the MMA issuers consume together (one wait, one release per tile);
+//   * warps 8 and 9 (one thread each) issue tcgen05.mma for units 0 and 1: S_x = Q_x K^T
+//     into TMEM, and after softmax O_x += P_x V with P_x read from TMEM.  They take
+//     turns batch by batch through a counter in shared memory, so the tensor pipe sees
+//     each unit's batch whole while one issuer's waits and commits overlap the other's
+//     batch;
+//   * warps 0-7 are two softmax warpgroups, one per unit; thread t owns row t of its
+//     unit and all 128 key columns of every score tile.  They read S from TMEM, mask,
+//     update the running max and sums with exp2, write P (bf16) back to TMEM, rescale O
+//     in TMEM when the running max rose by more than 2^8, and at the end write
+//     out = O / (sum of the bf16 P) and lse = m + ln(sum of the exact p).
 //   One unit's softmax overlaps the other unit's MMAs.
 //
 // TMEM (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256) -- P_x is stored
@@ -46,8 +48,8 @@ namespace ra {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kThreads = 576;  // 4 softmax warpgroups + MMA warp + TMA warp
-constexpr int kMmaWarp = 16, kLoadWarp = 17;
+constexpr int kThreads = 352;  // 2 softmax warpgroups + two MMA warps + TMA warp
+constexpr int kMmaWarp = 8, kLoadWarp = 10;  // warp 8 + x issues the MMAs of unit x
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
 // The running max used for P is only moved when the true max exceeds it by more
@@ -65,10 +67,9 @@ struct Cfg {
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = 2 * kTileBytes;
     static constexpr int kBarOff = kKVOff + kStages * kStageBytes;
-    static constexpr int kNumBars = 13 + 2 * kStages;
+    static constexpr int kNumBars = 14 + 2 * kStages;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr int kXchgOff = kMiscOff + 16;              // softmax exchange: 2 x 8 x 128 floats
-    static constexpr int kSmemBytes = kXchgOff + 2 * 8 * kTile * 4 + 1024;  // + slack to align the base
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kOCol = 256;
 };
@@ -367,14 +368,37 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, int x, uint32_t v_base, 
     }
 }
 
+// Wait until `turn` reaches `mine` (bounded: gives up on abort or after the timeout).
+__device__ __forceinline__ bool wait_turn(volatile uint32_t* turn, uint32_t mine, const WaitCtl& wc) {
+    if (*turn == mine) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (*turn == mine) return true;
+        if ((i & 255u) == 0u) {
+            if (*wc.abort_flag) return false;
+            if (globaltimer_ns() - t0 > wc.timeout_ns) {
+                raise_abort(wc, reinterpret_cast<uint64_t*>(const_cast<uint32_t*>(turn)));
+                return false;
+            }
+        }
+    }
+}
+
+// One issuer thread per unit x.  The two issuers take turns batch by batch (a batch is
+// the MMAs one unit issues between two softmax hand-offs), so the tensor pipe sees the
+// units' batches whole and in the order of the single-issuer schedule, while each
+// issuer's waits and commits overlap the other's batch.  `turn` counts the batches
+// issued so far; both issuers derive every batch's number from the item sequence.
+// Each K/V stage is released once per issuer (the barrier counts two): by a commit after
+// the unit's last MMA on it, or, in an item without a unit 1, by issuer 1's plain
+// arrival once the stage is loaded, which keeps both within one phase of every stage.
 template <int D, bool DOC>
-__device__ void mma_role(const AttnBf16Params& p, uint8_t* sQ, uint8_t* sKV, const Bars& b, uint32_t tmem,
-                         const WaitCtl& wc) {
+__device__ void mma_role(const AttnBf16Params& p, int x, uint8_t* sQ, uint8_t* sKV, const Bars& b, uint32_t tmem,
+                         volatile uint32_t* turn, const WaitCtl& wc) {
     using C = Cfg<D>;
-    const uint32_t sQa = smem_u32(sQ), sKVa = smem_u32(sKV);
-    uint32_t st_idx = 0, qit[2] = {0, 0}, pit[2] = {0, 0};
+    const uint32_t sQa = smem_u32(sQ) + x * C::kTileBytes, sKVa = smem_u32(sKV);
+    uint32_t st_idx = 0, qit = 0, pit = 0, seq = 0;
     bool ok = true;
-    // wait for the next stage to be loaded; base = its shared-memory address
     auto wait_stage = [&](uint32_t& s, uint32_t& base) -> bool {
         s = st_idx % C::kStages;
         base = sKVa + s * C::kStageBytes;
@@ -391,88 +415,72 @@ __device__ void mma_role(const AttnBf16Params& p, uint8_t* sQ, uint8_t* sKV, con
         const int nj = count_kv_tiles<DOC>(p, it);
         if (nj == 0) continue;
         const int nx = (it.hq[1] >= 0) ? 2 : 1;
-#pragma unroll
-        for (int x = 0; x < 2; ++x)
-            if (x < nx && ok && !mbar_wait(&b.q_full[x], qit[x] & 1u, wc)) ok = false;
-        if (!ok) break;
-        // S(0) from the stage holding K(0) alone
+        if (x >= nx) {  // no unit 1: pass every stage of the item
+            for (int i = 0; i <= nj && ok; ++i) {
+                uint32_t s, base;
+                if (!wait_stage(s, base)) { ok = false; break; }
+                mbar_arrive(&b.kv_empty[s]);
+            }
+            seq += 1 + nj;
+            continue;
+        }
+        // batch numbers: S(0) of unit x is seq + x, tile j of unit x is seq + nx (j + 1) + x
+        if (!mbar_wait(&b.q_full[x], qit & 1u, wc)) { ok = false; break; }
         uint32_t s, base;
         if (!wait_stage(s, base)) { ok = false; break; }
+        if (!wait_turn(turn, seq + x, wc)) { ok = false; break; }
         tc_fence_after();
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-            if (x >= nx) break;
-            issue_s<D>(tmem, x, sQa + x * C::kTileBytes, base + C::kTileBytes);
-            mma_commit(&b.s_full[x]);
-        }
+        issue_s<D>(tmem, x, sQa, base + C::kTileBytes);
+        mma_commit(&b.s_full[x]);
+        *turn = seq + x + 1;
         mma_commit(&b.kv_empty[s]);
-        if (nj == 1)
-#pragma unroll
-            for (int x = 0; x < 2; ++x)
-                if (x < nx) mma_commit(&b.q_empty[x]);
+        if (nj == 1) mma_commit(&b.q_empty[x]);
         for (int j = 0; j < nj && ok; ++j) {
             // this stage holds V(j) and, unless j is the last tile, K(j+1)
             if (!wait_stage(s, base)) { ok = false; break; }
-            const bool more = (j + 1 < nj);
-#pragma unroll
-            for (int x = 0; x < 2; ++x) {
-                if (x >= nx) break;
-                if (!mbar_wait(&b.p_full[x], pit[x] & 1u, wc)) { ok = false; break; }
-                ++pit[x];
-                if (j == 0 && !mbar_wait(&b.o_free[x], (qit[x] & 1u) ^ 1u, wc)) { ok = false; break; }
-                tc_fence_after();
-                issue_pv<D>(tmem, x, base, j > 0);
-                if (more) {
-                    issue_s<D>(tmem, x, sQa + x * C::kTileBytes, base + C::kTileBytes);
-                    mma_commit(&b.s_full[x]);
-                } else {
-                    mma_commit(&b.o_done[x]);
-                }
+            if (!mbar_wait(&b.p_full[x], pit & 1u, wc)) { ok = false; break; }
+            ++pit;
+            if (j == 0 && !mbar_wait(&b.o_free[x], (qit & 1u) ^ 1u, wc)) { ok = false; break; }
+            const uint32_t mine = seq + nx * (j + 1) + x;
+            if (!wait_turn(turn, mine, wc)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv<D>(tmem, x, base, j > 0);
+            if (j + 1 < nj) {
+                issue_s<D>(tmem, x, sQa, base + C::kTileBytes);
+                mma_commit(&b.s_full[x]);
+            } else {
+                mma_commit(&b.o_done[x]);
             }
-            if (!ok) break;
+            *turn = mine + 1;
             mma_commit(&b.kv_empty[s]);
-            if (j + 2 == nj)
-#pragma unroll
-                for (int x = 0; x < 2; ++x)
-                    if (x < nx) mma_commit(&b.q_empty[x]);
+            if (j + 2 == nj) mma_commit(&b.q_empty[x]);
         }
-        qit[0] += 1;
-        qit[1] += (nx > 1) ? 1u : 0u;
+        seq += nx * (nj + 1);
+        ++qit;
     }
     if (!ok) {
-        // every MMA issued so far must finish before TMEM is released
-        mma_commit(b.drain);
-        drain_wait(b.drain, 0, wc.timeout_ns);
+        // every MMA this thread issued must finish before TMEM is released
+        mma_commit(&b.drain[x]);
+        drain_wait(&b.drain[x], 0, wc.timeout_ns);
     }
 }
 
 // ------------------------------------------------------------------ softmax warpgroups
-// Named barrier over the two warpgroups (256 threads) that share query tile x; returns
-// the AND of every thread's `ok`, so that both halves leave together on an abort.
-__device__ __forceinline__ bool unit_bar_and(int x, bool ok) { return named_bar_and(1 + x, 256, ok); }
-
-// One warpgroup owns column half h (keys [64h, 64h+64) of every key tile) of query tile
-// x; thread t of the warpgroup owns row t.  The two halves of a tile exchange their
-// partial row maxima through shared memory once per key tile, so both compute P against
-// the same reference max; row sums stay per half until the epilogue.
+// Warpgroup x owns query tile x; thread t owns row t (TMEM lane t) and all 128 key
+// columns of every score tile, so a row's max and sums never leave its thread.  Each
+// warp waits on the tile's barriers by itself: the warps of a warpgroup share nothing
+// but the arrival that hands P to the MMA issuer.
 template <int D, bool DOC>
-__device__ void softmax_role(const AttnBf16Params& p, int x, int h, const Bars& b, uint32_t tmem, float* xchg,
-                             const WaitCtl& wc) {
+__device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint32_t tmem, const WaitCtl& wc) {
     using C = Cfg<D>;
-    constexpr int kHalf = kTile / 2;   // key columns per warpgroup
-    constexpr int kOHalf = D / 2;      // output columns per warpgroup
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t s_tmem = tmem + lane_off + x * kTile + h * kHalf;   // my 64 score columns
-    const uint32_t p_tmem = tmem + lane_off + x * kTile + 64 + h * 32;  // my 32 packed P columns
-    const uint32_t o_tmem = tmem + lane_off + C::kOCol + x * D + h * kOHalf;
-    // exchange slots per tile x: max [tile parity][half][row], sums [half][l | lr][row]
-    float* xm = xchg + x * (8 * kTile);
-    float* xs = xm + 4 * kTile;
+    const uint32_t s_tmem = tmem + lane_off + x * kTile;       // 128 score columns
+    const uint32_t p_tmem = s_tmem + 64;                        // 64 packed P columns over S's upper half
+    const uint32_t o_tmem = tmem + lane_off + C::kOCol + x * D;
     const bool causal = p.ring.causal != 0;
-    const bool poller = h == 0 && wq == 0;  // the warp that waits on the tile's barriers
     uint32_t sit = 0, iit = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
@@ -485,12 +493,12 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, int h, const Bars& 
         if (my_hq < 0) continue;
         const int nj = count_kv_tiles<DOC>(p, it);
         const size_t grow = static_cast<size_t>((x ? it.qrow[1] : it.qrow[0]) + row);
-        float* orow = p.out + grow * D + h * kOHalf;
+        float* orow = p.out + grow * D;
         if (nj == 0) {  // a message with no visible key for this tile
             float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int i = 0; i < kOHalf / 4; ++i) reinterpret_cast<float4*>(orow)[i] = z;
-            if (h == 0) p.lse[grow] = -INFINITY;
+            for (int i = 0; i < D / 4; ++i) reinterpret_cast<float4*>(orow)[i] = z;
+            p.lse[grow] = -INFINITY;
             continue;
         }
         const int tpos = x ? it.pos[1] : it.pos[0];
@@ -502,58 +510,48 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, int h, const Bars& 
         float m = -INFINITY, l = 0.f, lr = 0.f;
         int j = 0;
         for_each_kv_tile<DOC>(p, it, [&](int, int kpos) -> bool {
-            // One warp of the tile polls; the other seven wait in the named barrier, which
-            // costs no issue slots (spinning warps would steal them from the ones computing).
-            bool w_ok = true;
-            if (poller) w_ok = __all_sync(0xffffffffu, mbar_wait(&b.s_full[x], sit & 1u, wc));
-            w_ok = unit_bar_and(x, w_ok);
-            const uint32_t par = sit & 1u;
+            if (!__all_sync(0xffffffffu, mbar_wait(&b.s_full[x], sit & 1u, wc))) { ok = false; return false; }
             ++sit;
             tc_fence_after();
-            float s[kHalf];
-            if (w_ok) {
-                uint32_t r0[32], r1[32];
+            float s[kTile];
+            {
+                uint32_t r0[32], r1[32], r2[32], r3[32];
                 tmem_ld32(s_tmem + 0, r0);
                 tmem_ld32(s_tmem + 32, r1);
+                tmem_ld32(s_tmem + 64, r2);
+                tmem_ld32(s_tmem + 96, r3);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     s[i] = __uint_as_float(r0[i]);
                     s[32 + i] = __uint_as_float(r1[i]);
+                    s[64 + i] = __uint_as_float(r2[i]);
+                    s[96 + i] = __uint_as_float(r3[i]);
                 }
-            } else {
-#pragma unroll
-                for (int i = 0; i < kHalf; ++i) s[i] = 0.f;
             }
-            const int kcol = kpos + h * kHalf;  // natural position of my first key column
             if constexpr (DOC) {
                 // my keys [lo, hi] are visible: my document's start up to my own position
-                const int hi = qpos - kcol, lo = doc_lo - kcol;
-                if (lo > 0 || hi < kHalf - 1) {
+                const int hi = qpos - kpos, lo = doc_lo - kpos;
+                if (lo > 0 || hi < kTile - 1) {
 #pragma unroll
-                    for (int i = 0; i < kHalf; ++i) s[i] = (i > hi || i < lo) ? -INFINITY : s[i];
+                    for (int i = 0; i < kTile; ++i) s[i] = (i > hi || i < lo) ? -INFINITY : s[i];
                 }
-            } else if (causal && kcol + kHalf - 1 > qpos - row) {  // my half may cross the diagonal
-                const int lim = qpos - kcol;                // my keys [0, lim] are visible
+            } else if (causal && kpos + kTile - 1 > tpos) {  // the tile may cross the diagonal
+                const int lim = qpos - kpos;                  // my keys [0, lim] are visible
 #pragma unroll
-                for (int i = 0; i < kHalf; ++i) s[i] = (i > lim) ? -INFINITY : s[i];
+                for (int i = 0; i < kTile; ++i) s[i] = (i > lim) ? -INFINITY : s[i];
             }
             float mx;
             {
-                float c[4];
+                float c[8];
 #pragma unroll
-                for (int a = 0; a < 4; ++a) c[a] = fmaxf(s[2 * a], s[2 * a + 1]);
+                for (int a = 0; a < 8; ++a) c[a] = fmaxf(s[2 * a], s[2 * a + 1]);
 #pragma unroll
-                for (int i = 8; i < kHalf; i += 8)
+                for (int i = 16; i < kTile; i += 16)
 #pragma unroll
-                    for (int a = 0; a < 4; ++a) c[a] = fmax3(c[a], s[i + 2 * a], s[i + 2 * a + 1]);
-                mx = fmaxf(fmax3(c[0], c[1], c[2]), c[3]);
+                    for (int a = 0; a < 8; ++a) c[a] = fmax3(c[a], s[i + 2 * a], s[i + 2 * a + 1]);
+                mx = fmaxf(fmax3(c[0], c[1], c[2]), fmax3(c[3], c[4], fmax3(c[5], c[6], c[7])));
             }
-            // both halves have read their scores (the P stores below overwrite the upper
-            // half of S) and published their partial max
-            xm[(par * 2 + h) * kTile + row] = mx;
-            if (!unit_bar_and(x, w_ok)) { ok = false; return false; }
-            mx = fmaxf(mx, xm[(par * 2 + (h ^ 1)) * kTile + row]);
             const float m_new = fmaxf(m, mx * kLog2e);
             float f = 1.f;
             bool need = false;
@@ -569,26 +567,27 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, int h, const Bars& 
             const float nmu = (m == -INFINITY) ? 0.f : -m;
             float se[4] = {0.f, 0.f, 0.f, 0.f};
             float sr[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t pk[32];
 #pragma unroll
-            for (int hh = 0; hh < 4; ++hh) {
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t pk[32];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < 32; ++i) {
                     float t0, t1;
-                    ffma2(t0, t1, s[hh * 16 + 2 * i], s[hh * 16 + 2 * i + 1], kLog2e, kLog2e, nmu, nmu);
+                    ffma2(t0, t1, s[hh * 64 + 2 * i], s[hh * 64 + 2 * i + 1], kLog2e, kLog2e, nmu, nmu);
                     const float a = ex2(t0), c2 = ex2(t1);
                     const int q2 = 2 * (i & 1);
                     fadd2(se[q2], se[q2 + 1], se[q2], se[q2 + 1], a, c2);
-                    pk[hh * 8 + i] = pack_bf16x2(a, c2);
-                    add_bf16x2_f32(sr[q2], sr[q2 + 1], pk[hh * 8 + i]);
+                    pk[i] = pack_bf16x2(a, c2);
+                    add_bf16x2_f32(sr[q2], sr[q2 + 1], pk[i]);
                 }
+                // every score is in registers: P may overwrite S's upper half
+                tmem_st32(p_tmem + hh * 32, pk);
             }
-            tmem_st32(p_tmem, pk);
             // O is stable here: the commit that signalled this S also covered the
             // previous P V, and the next P V waits for this tile's arrivals.
             if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-                for (int cc = 0; cc < kOHalf; cc += 32) {
+                for (int cc = 0; cc < D; cc += 32) {
                     uint32_t o0[32];
                     tmem_ld32(o_tmem + cc, o0);
                     tmem_wait_ld();
@@ -606,20 +605,14 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, int h, const Bars& 
             return true;
         });
         if (!ok) break;
-        // epilogue: combine the two halves' sums, then each half writes its output columns
-        xs[(h * 2 + 0) * kTile + row] = l;
-        xs[(h * 2 + 1) * kTile + row] = lr;
-        bool d_ok = true;
-        if (poller) d_ok = __all_sync(0xffffffffu, mbar_wait(&b.o_done[x], iit & 1u, wc));
+        // epilogue: out = O / lr, lse = m + log2(l), both in natural-log units
+        if (!__all_sync(0xffffffffu, mbar_wait(&b.o_done[x], iit & 1u, wc))) { ok = false; break; }
         ++iit;
-        if (!unit_bar_and(x, d_ok)) { ok = false; break; }
-        const float l_all = l + xs[((h ^ 1) * 2 + 0) * kTile + row];
-        const float lr_all = lr + xs[((h ^ 1) * 2 + 1) * kTile + row];
         tc_fence_after();
-        const float inv = (lr_all > 0.f) ? 1.f / lr_all : 0.f;
+        const float inv = (lr > 0.f) ? 1.f / lr : 0.f;
         const uint64_t out_policy = make_policy_evict_first();  // written once, read by the host
 #pragma unroll
-        for (int cc = 0; cc < kOHalf; cc += 32) {
+        for (int cc = 0; cc < D; cc += 32) {
             uint32_t o0[32];
             tmem_ld32(o_tmem + cc, o0);
             tmem_wait_ld();
@@ -633,9 +626,7 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, int h, const Bars& 
         }
         tc_fence_before();
         mbar_arrive(&b.o_free[x]);
-        if (h == 0) p.lse[grow] = (l_all > 0.f) ? (m + log2f(l_all)) * kLn2 : -INFINITY;
-        // the sum slots are rewritten only at the next item's epilogue, after both halves
-        // have passed at least one more exchange barrier
+        p.lse[grow] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
     }
 }
 
@@ -657,10 +648,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     b.o_done = bars + 8;
     b.o_free = bars + 10;
     b.drain = bars + 12;
-    b.kv_full = bars + 13;
-    b.kv_empty = bars + 13 + C::kStages;
+    b.kv_full = bars + 14;
+    b.kv_empty = bars + 14 + C::kStages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
+    volatile uint32_t* turn = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 8);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
@@ -668,16 +660,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&b.q_full[x], 1);
             mbar_init(&b.q_empty[x], 1);
             mbar_init(&b.s_full[x], 1);
-            mbar_init(&b.p_full[x], 256);
+            mbar_init(&b.p_full[x], 128);
             mbar_init(&b.o_done[x], 1);
-            mbar_init(&b.o_free[x], 256);
+            mbar_init(&b.o_free[x], 128);
         }
-        mbar_init(b.drain, 1);
+        mbar_init(&b.drain[0], 1);
+        mbar_init(&b.drain[1], 1);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&b.kv_full[s], 1);
-            mbar_init(&b.kv_empty[s], 1);
+            mbar_init(&b.kv_empty[s], 2);  // released once by each unit's issuer
         }
         *abort_flag = 0;
+        *turn = 0;
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -696,10 +690,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const WaitCtl wc{abort_flag, p.err, p.timeout_ns};
 
     // warps 0-15: softmax, warpgroup g = warp / 4 owns tile g / 2, key half g % 2
-    if (warp < 16) {
-        softmax_role<D, DOC>(p, warp / 8, (warp / 4) & 1, b, tmem, reinterpret_cast<float*>(smem + C::kXchgOff), wc);
-    } else if (warp == kMmaWarp) {
-        if (lane == 0) mma_role<D, DOC>(p, sQ, sKV, b, tmem, wc);
+    if (warp < 8) {
+        softmax_role<D, DOC>(p, warp / 4, b, tmem, wc);
+    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+        if (lane == 0) mma_role<D, DOC>(p, warp - kMmaWarp, sQ, sKV, b, tmem, turn, wc);
     } else if (warp == kLoadWarp) {
         if (lane == 0) load_role<D, DOC>(p, &tq, &tk, &tv, sQ, sKV, b, wc);
     }
