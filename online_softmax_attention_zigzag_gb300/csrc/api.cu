@@ -19,6 +19,12 @@ namespace {
 // static device variable, so the library allocates nothing; host code reaches it
 // through the address cudaGetSymbolAddress returns for the current device.
 __device__ int g_err_word[4];  // status, record set, barrier address, (block << 10 | thread)
+// Work-item counters of the fused kernel, one pair per launch slot.  A launch takes the
+// next slot in turn; its last CTA zeroes the pair again, so a slot is clean for the launch
+// that takes it kSchedSlots launches later.  (Two launches in flight at once that held the
+// same slot would share counters: that needs kSchedSlots launches in flight together.)
+constexpr int kSchedSlots = 256;
+__device__ unsigned int g_sched[2 * kSchedSlots];
 
 constexpr int kMaxDevices = 64;
 
@@ -27,6 +33,8 @@ struct DeviceInfo {
     int status = RA_OK;  // RA_ERR_ARCH when the device is not sm_103
     int sms = 0;
     int* err = nullptr;
+    unsigned int* sched = nullptr;  // g_sched on this device
+    unsigned int next_slot = 0;     // guarded by g_mu
 };
 
 std::mutex g_mu;
@@ -53,6 +61,8 @@ int device_info(DeviceInfo** out) {
             void* p = nullptr;
             if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return RA_ERR_CUDA;
             d.err = static_cast<int*>(p);
+            if (cudaGetSymbolAddress(&p, g_sched) != cudaSuccess) return RA_ERR_CUDA;
+            d.sched = static_cast<unsigned int*>(p);
             d.status = RA_OK;
         }
         d.ready = true;
@@ -171,6 +181,25 @@ int fwd_bf16(const void* q, const void* k, const void* v, float* out, float* lse
     } else {
         p.pair_mode = ra::kSingles;
         p.n_items = p.n_tiles * Hq;
+    }
+    // Order work items by groups of KV heads whose K and V take a third of L2 at most:
+    // within a group the items go by decreasing work across the group's heads; across
+    // groups, one group's K/V is live at a time, so K and V come from DRAM once.  The
+    // CTAs draw items from this list as they finish (a counter in global memory), which
+    // evens out their work whatever the list's shape.
+    {
+        constexpr double kBudget = 40e6;
+        const double kv_head_bytes = static_cast<double>(S) * d * 4.0;  // K and V of one head, bf16
+        p.kv_group = 1;
+        for (int gsz = Hkv; gsz >= 1; --gsz)
+            if (Hkv % gsz == 0 && gsz * kv_head_bytes <= kBudget) {
+                p.kv_group = gsz;
+                break;
+            }
+    }
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        p.sched = dev->sched + 2 * (dev->next_slot++ % kSchedSlots);
     }
     p.out = out;
     p.lse = lse;

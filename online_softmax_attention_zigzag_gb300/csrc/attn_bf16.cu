@@ -19,7 +19,8 @@
 // Design (one CTA per SM, persistent, 352 threads):
 //   * a work item is two 128-row query tiles (units) that share every K/V tile: two
 //     query heads of one KV group at the same positions, or two adjacent tiles of one
-//     head; items are ordered KV-head-major, then by decreasing causal work;
+//     head; items are listed by groups of KV heads, then by decreasing causal work, and
+//     each CTA's loader draws the next one from a global counter when it needs it;
 //   * warp 10 (one thread) streams Q tiles and, in visiting order, K and V tiles into
 //     shared memory with TMA (128-byte swizzle), through a ring of stages guarded by
 //     mbarriers; a stage pairs the V tile of one key tile with the K tile of the next,
@@ -51,6 +52,10 @@ constexpr int kTile = 128;
 constexpr int kThreads = 352;  // 2 softmax warpgroups + two MMA warps + TMA warp
 constexpr int kMmaWarp = 8, kLoadWarp = 10;  // warp 8 + x issues the MMAs of unit x
 constexpr float kLog2e = 1.4426950408889634f;
+// Work items are taken dynamically: the loader draws the next item index from a counter in
+// global memory and passes it to the other roles through a ring of this many entries.
+constexpr int kItemRing = 4;
+constexpr uint32_t kItemTakers = 10;  // 2 MMA issuers + 8 softmax warps
 constexpr float kLn2 = 0.69314718055994531f;
 // The running max used for P is only moved when the true max exceeds it by more
 // than this (log2 units): P then stays below 2^8 and O needs no rescale otherwise.
@@ -67,9 +72,10 @@ struct Cfg {
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = 2 * kTileBytes;
     static constexpr int kBarOff = kKVOff + kStages * kStageBytes;
-    static constexpr int kNumBars = 14 + 2 * kStages;
+    static constexpr int kNumBars = 14 + 2 * kStages + 2 * kItemRing;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack to align the base
+    static constexpr int kRingOff = kMiscOff + 16;  // item ids handed from the loader to the other roles
+    static constexpr int kSmemBytes = kRingOff + 4 * kItemRing + 1024;  // + slack to align the base
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kOCol = 256;
 };
@@ -84,7 +90,22 @@ struct Bars {
     uint64_t* drain;     // [1] mma, on abort only
     uint64_t* kv_full;   // [stages]
     uint64_t* kv_empty;  // [stages]
+    uint64_t* item_full;   // [kItemRing] loader -> issuers, softmax warps (item id written)
+    uint64_t* item_empty;  // [kItemRing] issuers, softmax warps (one arrival each) -> loader
 };
+
+// Entry k of the item sequence as the loader published it: an item index, -1 at the end,
+// -2 on abort.  Every taker takes every entry, in order; one arrival per taker (`leader`
+// is lane 0 of a softmax warp, or an issuer thread) frees the ring slot.
+__device__ __forceinline__ int take_item(const Bars& b, const volatile int* ring, uint32_t k, bool leader,
+                                         const WaitCtl& wc) {
+    const uint32_t slot = k % kItemRing;
+    if (!mbar_wait(&b.item_full[slot], (k / kItemRing) & 1u, wc)) return -2;
+    const int item = ring[slot];
+    __syncwarp(__activemask());
+    if (leader) mbar_arrive(&b.item_empty[slot]);
+    return item;
+}
 
 // A work item: up to two query tiles (units) of one rank that share a KV head.
 struct Item {
@@ -114,26 +135,27 @@ template <bool DOC>
 __device__ __forceinline__ void decode_item(const AttnBf16Params& p, int item, Item& it) {
     const Ring& R = p.ring;
     int t0, t1;
+    // Items are grouped by KV heads (p.kv_group heads per group, chosen by the host so
+    // that a group's K and V stay in L2); within a group, by decreasing causal work
+    // (last query tiles first), then by head.  upk: items per (KV head, tile position).
+    const int upk = (p.pair_mode == kPairHeads) ? R.g / 2 : (p.pair_mode == kPairPositions ? 1 : R.g);
+    const int n_pi = (p.pair_mode == kPairPositions) ? p.n_tiles / 2 : p.n_tiles;
+    const int per_pi = upk * p.kv_group;
+    const int grp = item / (n_pi * per_pi), rem = item - grp * (n_pi * per_pi);
+    const int pi = rem / per_pi, r2 = rem - pi * per_pi;
+    it.hk = grp * p.kv_group + r2 / upk;
+    const int u = r2 - (r2 / upk) * upk;
     if (p.pair_mode == kPairHeads) {
-        const int gh = R.g / 2, per_kv = p.n_tiles * gh;
-        it.hk = item / per_kv;
-        const int rem = item - it.hk * per_kv;
-        const int pi = rem / gh;
         t0 = t1 = p.n_tiles - 1 - pi;
-        it.hq[0] = it.hk * R.g + 2 * (rem - pi * gh);
+        it.hq[0] = it.hk * R.g + 2 * u;
         it.hq[1] = it.hq[0] + 1;
     } else if (p.pair_mode == kPairPositions) {
-        const int per_h = p.n_tiles / 2;
-        const int h = item / per_h, pi = item - h * per_h;
         t1 = p.n_tiles - 1 - 2 * pi;
         t0 = t1 - 1;
-        it.hk = h / R.g;
-        it.hq[0] = it.hq[1] = h;
+        it.hq[0] = it.hq[1] = it.hk;  // one query head per KV head
     } else {
-        const int h = item / p.n_tiles, pi = item - h * p.n_tiles;
         t0 = t1 = p.n_tiles - 1 - pi;
-        it.hk = h / R.g;
-        it.hq[0] = h;
+        it.hq[0] = it.hk * R.g + u;
         it.hq[1] = -1;
     }
     if (p.rank_sel >= 0) {  // tile indices count one rank's local tiles: map them to natural tiles
@@ -239,7 +261,8 @@ __device__ __forceinline__ int count_kv_tiles(const AttnBf16Params& p, const Ite
 // then V(n-1).  V sits at the stage base, K one tile above it.
 template <int D, bool DOC>
 __device__ void load_role(const AttnBf16Params& p, const CUtensorMap* tq, const CUtensorMap* tk,
-                          const CUtensorMap* tv, uint8_t* sQ, uint8_t* sKV, const Bars& b, const WaitCtl& wc) {
+                          const CUtensorMap* tv, uint8_t* sQ, uint8_t* sKV, const Bars& b, volatile int* ring,
+                          const WaitCtl& wc) {
     using C = Cfg<D>;
     uint32_t st_idx = 0, qit[2] = {0, 0};
     bool ok = true;
@@ -259,10 +282,15 @@ __device__ void load_role(const AttnBf16Params& p, const CUtensorMap* tq, const 
             tma_load_2d_hint(sKV + s * C::kStageBytes + off + bx * C::kBoxBytes, map, &b.kv_full[s], bx * 64, row,
                              keep);
     };
-    for (int round = 0; ok; ++round) {
-        if (round * (int)gridDim.x >= p.n_items) break;
-        const int item = item_of_round(round);
-        if (item >= p.n_items) continue;
+    for (uint32_t k = 0; ok; ++k) {
+        // draw the next item and publish it (or the end of the sequence)
+        const uint32_t slot = k % kItemRing;
+        if (!mbar_wait(&b.item_empty[slot], ((k / kItemRing) & 1u) ^ 1u, wc, 32)) { ok = false; break; }
+        int item = static_cast<int>(atomicAdd(p.sched, 1u));
+        if (item >= p.n_items) item = -1;
+        ring[slot] = item;
+        mbar_arrive(&b.item_full[slot]);
+        if (item < 0) break;
         Item it;
         decode_item<DOC>(p, item, it);
         if (count_kv_tiles<DOC>(p, it) == 0) continue;
@@ -394,7 +422,7 @@ __device__ __forceinline__ bool wait_turn(volatile uint32_t* turn, uint32_t mine
 // arrival once the stage is loaded, which keeps both within one phase of every stage.
 template <int D, bool DOC>
 __device__ void mma_role(const AttnBf16Params& p, int x, uint8_t* sQ, uint8_t* sKV, const Bars& b, uint32_t tmem,
-                         volatile uint32_t* turn, const WaitCtl& wc) {
+                         volatile uint32_t* turn, const volatile int* ring, const WaitCtl& wc) {
     using C = Cfg<D>;
     const uint32_t sQa = smem_u32(sQ) + x * C::kTileBytes, sKVa = smem_u32(sKV);
     uint32_t st_idx = 0, qit = 0, pit = 0, seq = 0;
@@ -406,10 +434,10 @@ __device__ void mma_role(const AttnBf16Params& p, int x, uint8_t* sQ, uint8_t* s
         ++st_idx;
         return r;
     };
-    for (int round = 0; ok; ++round) {
-        if (round * (int)gridDim.x >= p.n_items) break;
-        const int item = item_of_round(round);
-        if (item >= p.n_items) continue;
+    for (uint32_t k = 0; ok; ++k) {
+        const int item = take_item(b, ring, k, true, wc);
+        if (item == -2) { ok = false; break; }
+        if (item < 0) break;
         Item it;
         decode_item<DOC>(p, item, it);
         const int nj = count_kv_tiles<DOC>(p, it);
@@ -471,7 +499,8 @@ __device__ void mma_role(const AttnBf16Params& p, int x, uint8_t* sQ, uint8_t* s
 // warp waits on the tile's barriers by itself: the warps of a warpgroup share nothing
 // but the arrival that hands P to the MMA issuer.
 template <int D, bool DOC>
-__device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint32_t tmem, const WaitCtl& wc) {
+__device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint32_t tmem, const volatile int* ring,
+                             const WaitCtl& wc) {
     using C = Cfg<D>;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int wq = warp & 3;
@@ -483,10 +512,10 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
     const bool causal = p.ring.causal != 0;
     uint32_t sit = 0, iit = 0;
     bool ok = true;
-    for (int round = 0; ok; ++round) {
-        if (round * (int)gridDim.x >= p.n_items) break;
-        const int item = item_of_round(round);
-        if (item >= p.n_items) continue;
+    for (uint32_t k = 0; ok; ++k) {
+        const int item = take_item(b, ring, k, lane == 0, wc);
+        if (item == -2) { ok = false; break; }
+        if (item < 0) break;
         Item it;
         decode_item<DOC>(p, item, it);
         const int my_hq = x ? it.hq[1] : it.hq[0];
@@ -650,6 +679,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     b.drain = bars + 12;
     b.kv_full = bars + 14;
     b.kv_empty = bars + 14 + C::kStages;
+    b.item_full = bars + 14 + 2 * C::kStages;
+    b.item_empty = bars + 14 + 2 * C::kStages + kItemRing;
+    volatile int* ring = reinterpret_cast<volatile int*>(smem + C::kRingOff);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
     volatile uint32_t* turn = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff + 8);
@@ -669,6 +701,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&b.kv_full[s], 1);
             mbar_init(&b.kv_empty[s], 2);  // released once by each unit's issuer
+        }
+        for (int s = 0; s < kItemRing; ++s) {
+            mbar_init(&b.item_full[s], 1);
+            mbar_init(&b.item_empty[s], kItemTakers);
         }
         *abort_flag = 0;
         *turn = 0;
@@ -691,17 +727,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // warps 0-15: softmax, warpgroup g = warp / 4 owns tile g / 2, key half g % 2
     if (warp < 8) {
-        softmax_role<D, DOC>(p, warp / 4, b, tmem, wc);
+        softmax_role<D, DOC>(p, warp / 4, b, tmem, ring, wc);
     } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-        if (lane == 0) mma_role<D, DOC>(p, warp - kMmaWarp, sQ, sKV, b, tmem, turn, wc);
+        if (lane == 0) mma_role<D, DOC>(p, warp - kMmaWarp, sQ, sKV, b, tmem, turn, ring, wc);
     } else if (warp == kLoadWarp) {
-        if (lane == 0) load_role<D, DOC>(p, &tq, &tk, &tv, sQ, sKV, b, wc);
+        if (lane == 0) load_role<D, DOC>(p, &tq, &tk, &tv, sQ, sKV, b, ring, wc);
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
+    // the last CTA to finish re-zeroes the item counter for the next launch that uses it
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+            p.sched[0] = 0u;
+            p.sched[1] = 0u;
+            __threadfence();
+        }
+    }
 }
 
 template <int D, bool DOC>

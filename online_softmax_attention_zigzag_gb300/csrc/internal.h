@@ -33,6 +33,10 @@ struct AttnBf16Params {
     int rank_sel;   // -1: every rank's query rows; r >= 0: only virtual rank r's rows
     int n_tiles;    // 128-row query tiles per head (S / 128, or S / (128 c) for one rank)
     int n_items;
+    int kv_group;   // KV heads per ordering group of work items (divides Hkv)
+    // [2] item counter and finished-CTA counter in global memory: zero at launch; the
+    // last CTA of the launch zeroes them again
+    unsigned int* sched;
     float* out;
     float* lse;
     // document mask over all-gathered K/V: first natural position of the document of
