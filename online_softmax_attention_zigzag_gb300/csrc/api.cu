@@ -72,6 +72,18 @@ int device_info(DeviceInfo** out) {
     return RA_OK;
 }
 
+// n consecutive counter slots (pairs of words) of the device's ring, taken in turn.
+unsigned int* sched_slots(DeviceInfo* dev, int n) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    unsigned int i = dev->next_slot % kSchedSlots;
+    if (i + n > static_cast<unsigned int>(kSchedSlots)) {  // keep the n slots contiguous
+        dev->next_slot += kSchedSlots - i;
+        i = 0;
+    }
+    dev->next_slot += n;
+    return dev->sched + 2 * i;
+}
+
 int get_encoder() {
     std::lock_guard<std::mutex> lock(g_mu);
     if (g_encode) return RA_OK;
@@ -197,10 +209,7 @@ int fwd_bf16(const void* q, const void* k, const void* v, float* out, float* lse
                 break;
             }
     }
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        p.sched = dev->sched + 2 * (dev->next_slot++ % kSchedSlots);
-    }
+    p.sched = sched_slots(dev, 1);
     p.out = out;
     p.lse = lse;
     p.doc_start = doc_start;
@@ -546,6 +555,7 @@ int bwd_bf16(const void* q, const void* k, const void* v, const float* out, cons
     p.dv = dv;
     p.err = dev->err;
     p.timeout_ns = wait_timeout_ns();
+    p.sched = sched_slots(dev, 2);
     CUtensorMap tq, tk, tv, tdo;
     // the backward kernels move 64-row boxes (half tiles are their streaming unit)
     if (encode_bf16_map(&tq, q, static_cast<long long>(Hq) * S, d, 64) != RA_OK ||

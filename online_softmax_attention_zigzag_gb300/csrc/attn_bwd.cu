@@ -21,7 +21,11 @@
 // Splitting dq from dk/dv recomputes S and dP once more (7 tile products instead of 5)
 // but needs no atomics and gives a deterministic result.
 //
-// Each CTA is persistent: warps 0-7 compute (warpgroup h handles columns [64h, 64h+64)
+// Each CTA is persistent and draws its work items (query tiles for dq, key tiles for
+// dk/dv, listed by KV head and decreasing work) from a counter in global memory as it
+// finishes the previous one; its loader hands the index to the other roles through a ring
+// in shared memory.  (Dealing the 2048 key tiles of the 32k GQA dk/dv launch out
+// statically in snake order left the CTAs ~20% apart.)  Warps 0-7 compute (warpgroup h handles columns [64h, 64h+64)
 // of the 128 x 128 tile product, thread = TMEM lane = row), warp 8 issues the MMAs (one
 // thread), warp 9 the TMA loads (one thread).  The compute warps copy S (S^T) and dP
 // (dP^T) from TMEM into registers and release those columns at once, so the next tile's
@@ -47,6 +51,10 @@ constexpr int kMmaWarp = 8, kLoadWarp = 9;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 256;
+// Work items are drawn dynamically: the loader takes the next index from a counter in
+// global memory and hands it to the MMA issuer and the 8 compute warps through a ring.
+constexpr int kItemRing = 4;
+constexpr uint32_t kItemTakers = 9;
 
 // Shared memory of both kernels: two resident tiles (Q, dO or K, V), then ring A (three
 // slots: K for dq, Q for dk/dv) and ring B (two slots: V for dq, dO for dk/dv).
@@ -58,9 +66,10 @@ struct BwdCfg {
     static constexpr int kAOff = 2 * kTileBytes;
     static constexpr int kBOff = kAOff + kSlotsA * kTileBytes;
     static constexpr int kBarOff = kBOff + kSlotsB * kTileBytes;
-    static constexpr int kNumBars = 32;
+    static constexpr int kNumBars = 40;
+    static constexpr int kRingOff = kBarOff + kNumBars * 8 + 16;  // item ids, loader -> other roles
     // dk/dv: lse and D of the current query tile, per compute warpgroup (64 + 64 floats)
-    static constexpr int kLdOff = kBarOff + kNumBars * 8 + 16;
+    static constexpr int kLdOff = kRingOff + 16;
     static constexpr int kSmem = kLdOff + 2 * 128 * 4 + 1024;  // + slack to align the base
 };
 
@@ -229,10 +238,11 @@ struct Bars {
     uint64_t *ds_full;               // [2] dq: dS buffer written; dk/dv: [0] P^T, dS^T written
     uint64_t *acc_done, *acc_free, *drain;
     uint64_t *a_full, *a_empty, *b_full, *b_empty;
+    uint64_t *item_full, *item_empty;  // [kItemRing] each: item ids handed from the loader
     __device__ explicit Bars(uint64_t* b)
         : res_full(b), res_empty(b + 1), s_full(b + 2), dp_full(b + 3), s_free(b + 4), dp_free(b + 5),
           ds_full(b + 6), acc_done(b + 8), acc_free(b + 9), drain(b + 10), a_full(b + 16), a_empty(b + 19),
-          b_full(b + 22), b_empty(b + 24) {}
+          b_full(b + 22), b_empty(b + 24), item_full(b + 26), item_empty(b + 30) {}
 };
 
 __device__ __forceinline__ void init_bars(const Bars& b) {
@@ -255,6 +265,34 @@ __device__ __forceinline__ void init_bars(const Bars& b) {
         mbar_init(&b.b_full[s], 1);
         mbar_init(&b.b_empty[s], 1);
     }
+    for (int s = 0; s < kItemRing; ++s) {
+        mbar_init(&b.item_full[s], 1);
+        mbar_init(&b.item_empty[s], kItemTakers);
+    }
+}
+
+// The loader draws entry k of the item sequence from the launch's counter and publishes it
+// (-1 past the last item); -2 on abort.
+__device__ __forceinline__ int publish_item(const AttnBwdParams& p, const Bars& b, volatile int* ring, uint32_t k,
+                                            const WaitCtl& wc) {
+    const uint32_t slot = k % kItemRing;
+    if (!mbar_wait(&b.item_empty[slot], ((k / kItemRing) & 1u) ^ 1u, wc, 32)) return -2;
+    int item = static_cast<int>(atomicAdd(p.sched, 1u));
+    if (item >= p.n_items) item = -1;
+    ring[slot] = item;
+    mbar_arrive(&b.item_full[slot]);
+    return item;
+}
+
+// Every other role takes every entry, in order; one arrival per taker frees the slot.
+__device__ __forceinline__ int take_item(const Bars& b, const volatile int* ring, uint32_t k, bool leader,
+                                         const WaitCtl& wc) {
+    const uint32_t slot = k % kItemRing;
+    if (!mbar_wait(&b.item_full[slot], (k / kItemRing) & 1u, wc)) return -2;
+    const int item = ring[slot];
+    __syncwarp(__activemask());
+    if (leader) mbar_arrive(&b.item_empty[slot]);
+    return item;
 }
 
 // Wait (one poller warp per warpgroup, the rest in the group's named barrier).
@@ -299,16 +337,16 @@ __device__ __forceinline__ void ring_drain(uint64_t* full, uint32_t issued, int 
 template <int D>
 __device__ void dq_load(const AttnBwdParams& p, const CUtensorMap* tq, const CUtensorMap* tdo,
                         const CUtensorMap* tk, const CUtensorMap* tv, uint8_t* smem, const Bars& b,
-                        const WaitCtl& wc) {
+                        volatile int* ring, const WaitCtl& wc) {
     using C = BwdCfg<D>;
     const Ring& R = p.ring;
     const uint64_t keep = make_policy_evict_last(), stream = make_policy_evict_first();
     uint32_t ka = 0, vb = 0, qit = 0;
     bool ok = true;
-    for (int round = 0; ok; ++round) {
-        if (round * (int)gridDim.x >= p.n_items) break;
-        const int item = item_of_round(round);
-        if (item >= p.n_items) continue;
+    for (uint32_t n_it = 0; ok; ++n_it) {
+        const int item = publish_item(p, b, ring, n_it, wc);
+        if (item == -2) { ok = false; break; }
+        if (item < 0) break;
         int hq, qp;
         dq_item(p, item, hq, qp);
         if (!mbar_wait(b.res_empty, (qit & 1u) ^ 1u, wc, 32)) { ok = false; break; }
@@ -338,17 +376,17 @@ __device__ void dq_load(const AttnBwdParams& p, const CUtensorMap* tq, const CUt
 }
 
 template <int D>
-__device__ void dq_mma(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uint32_t tmem, const WaitCtl& wc) {
+__device__ void dq_mma(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uint32_t tmem, volatile int* ring, const WaitCtl& wc) {
     using C = BwdCfg<D>;
     const Ring& R = p.ring;
     const uint32_t sQ = smem_u32(smem), sdO = sQ + C::kTileBytes;
     const uint32_t sA = sQ + C::kAOff, sB = sQ + C::kBOff;
     uint32_t idx = 0, qit = 0, sf = 0, dpf = 0, dsit[2] = {0, 0};
     bool ok = true;
-    for (int round = 0; ok; ++round) {
-        if (round * (int)gridDim.x >= p.n_items) break;
-        const int item = item_of_round(round);
-        if (item >= p.n_items) continue;
+    for (uint32_t n_it = 0; ok; ++n_it) {
+        const int item = take_item(b, ring, n_it, true, wc);
+        if (item == -2) { ok = false; break; }
+        if (item < 0) break;
         int hq, qp;
         dq_item(p, item, hq, qp);
         const int nj = count_key_tiles(R, qp);
@@ -408,7 +446,7 @@ __device__ void dq_mma(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uin
 }
 
 template <int D>
-__device__ void dq_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem, const WaitCtl& wc) {
+__device__ void dq_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem, volatile int* ring, const WaitCtl& wc) {
     const Ring& R = p.ring;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int h = warp / 4, wq = warp % 4;
@@ -419,10 +457,10 @@ __device__ void dq_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
     const uint32_t acc_tm = tmem + lane_off + kAccCol + h * (D / 2);
     uint32_t sf = 0, dpf = 0, it = 0;
     bool ok = true;
-    for (int round = 0; ok; ++round) {
-        if (round * (int)gridDim.x >= p.n_items) break;
-        const int item = item_of_round(round);
-        if (item >= p.n_items) continue;
+    for (uint32_t n_it = 0; ok; ++n_it) {
+        const int item = take_item(b, ring, n_it, lane == 0, wc);
+        if (item == -2) { ok = false; break; }
+        if (item < 0) break;
         int hq, qp;
         dq_item(p, item, hq, qp);
         const int grow = row_of(p, hq, qp) + row;
@@ -481,17 +519,17 @@ __device__ void dq_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
 template <int D>
 __device__ void kv_load(const AttnBwdParams& p, const CUtensorMap* tq, const CUtensorMap* tdo,
                         const CUtensorMap* tk, const CUtensorMap* tv, uint8_t* smem, const Bars& b,
-                        const WaitCtl& wc) {
+                        volatile int* ring, const WaitCtl& wc) {
     using C = BwdCfg<D>;
     const Ring& R = p.ring;
     // Q, dO are re-read by every key tile of their KV group: keep them in L2
     const uint64_t keep = make_policy_evict_last(), stream = make_policy_evict_first();
     uint32_t qa = 0, ob = 0, kit = 0;
     bool ok = true;
-    for (int round = 0; ok; ++round) {
-        if (round * (int)gridDim.x >= p.n_items) break;
-        const int item = item_of_round(round);
-        if (item >= p.n_items) continue;
+    for (uint32_t n_it = 0; ok; ++n_it) {
+        const int item = publish_item(p, b, ring, n_it, wc);
+        if (item == -2) { ok = false; break; }
+        if (item < 0) break;
         int hk, kp;
         kv_item(p, item, hk, kp);
         if (!mbar_wait(b.res_empty, (kit & 1u) ^ 1u, wc, 32)) { ok = false; break; }
@@ -520,17 +558,17 @@ __device__ void kv_load(const AttnBwdParams& p, const CUtensorMap* tq, const CUt
 }
 
 template <int D>
-__device__ void kv_mma(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uint32_t tmem, const WaitCtl& wc) {
+__device__ void kv_mma(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uint32_t tmem, volatile int* ring, const WaitCtl& wc) {
     using C = BwdCfg<D>;
     const Ring& R = p.ring;
     const uint32_t sK = smem_u32(smem), sV = sK + C::kTileBytes;
     const uint32_t sA = sK + C::kAOff, sB = sK + C::kBOff;
     uint32_t idx = 0, kit = 0, sf = 0, pf = 0;
     bool ok = true;
-    for (int round = 0; ok; ++round) {
-        if (round * (int)gridDim.x >= p.n_items) break;
-        const int item = item_of_round(round);
-        if (item >= p.n_items) continue;
+    for (uint32_t n_it = 0; ok; ++n_it) {
+        const int item = take_item(b, ring, n_it, true, wc);
+        if (item == -2) { ok = false; break; }
+        if (item < 0) break;
         int hk, kp;
         kv_item(p, item, hk, kp);
         const int n = count_query_tiles(R, hk, kp);
@@ -593,7 +631,7 @@ __device__ __forceinline__ void group_sync(int h) {
 }
 
 template <int D>
-__device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem, float* sld, const WaitCtl& wc) {
+__device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem, float* sld, volatile int* ring, const WaitCtl& wc) {
     const Ring& R = p.ring;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int h = warp / 4, wq = warp % 4;
@@ -605,10 +643,10 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
     const uint32_t dk_tm = tmem + lane_off + kAccCol + D + h * (D / 2);
     uint32_t sf = 0, dpf = 0, it = 0;
     bool ok = true;
-    for (int round = 0; ok; ++round) {
-        if (round * (int)gridDim.x >= p.n_items) break;
-        const int item = item_of_round(round);
-        if (item >= p.n_items) continue;
+    for (uint32_t n_it = 0; ok; ++n_it) {
+        const int item = take_item(b, ring, n_it, lane == 0, wc);
+        if (item == -2) { ok = false; break; }
+        if (item < 0) break;
         int hk, kp;
         kv_item(p, item, hk, kp);
         const int kpos = kp + row;
@@ -726,24 +764,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const WaitCtl wc{abort_flag, p.err, p.timeout_ns};
+    volatile int* ring = reinterpret_cast<volatile int*>(smem + C::kRingOff);
     if (warp < 8) {
-        if constexpr (DQ) dq_compute<D>(p, b, tmem, wc);
-        else kv_compute<D>(p, b, tmem, reinterpret_cast<float*>(smem + C::kLdOff) + (warp / 4) * 128, wc);
+        if constexpr (DQ) dq_compute<D>(p, b, tmem, ring, wc);
+        else kv_compute<D>(p, b, tmem, reinterpret_cast<float*>(smem + C::kLdOff) + (warp / 4) * 128, ring, wc);
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
-            if constexpr (DQ) dq_mma<D>(p, smem, b, tmem, wc);
-            else kv_mma<D>(p, smem, b, tmem, wc);
+            if constexpr (DQ) dq_mma<D>(p, smem, b, tmem, ring, wc);
+            else kv_mma<D>(p, smem, b, tmem, ring, wc);
         }
     } else if (warp == kLoadWarp) {
         if (lane == 0) {
-            if constexpr (DQ) dq_load<D>(p, &tq, &tdo, &tk, &tv, smem, b, wc);
-            else kv_load<D>(p, &tq, &tdo, &tk, &tv, smem, b, wc);
+            if constexpr (DQ) dq_load<D>(p, &tq, &tdo, &tk, &tv, smem, b, ring, wc);
+            else kv_load<D>(p, &tq, &tdo, &tk, &tv, smem, b, ring, wc);
         }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+    // the last CTA to finish re-zeroes the item counter for the next launch that uses it
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+            p.sched[0] = 0u;
+            p.sched[1] = 0u;
+            __threadfence();
+        }
+    }
 }
 
 // ------------------------------------------------------------------ D = dout . out
@@ -827,6 +875,7 @@ int launch_bwd_d(const AttnBwdParams& p0, const float* out, const void* dout, co
     if (cudaGetLastError() != cudaSuccess) return -4;
 
     p.n_items = R.Hkv * p.n_tiles;
+    p.sched = p0.sched + 2;  // the dk/dv launch's own counter pair
     auto kkv = bwd_kernel<D, false>;
     if (cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess) return -4;
     kkv<<<p.n_items < sms ? p.n_items : sms, kThreads, C::kSmem, stream>>>(p, tq, tdo, tk, tv);

@@ -54,6 +54,9 @@ struct AttnBwdParams {
     int n_items;       // dq kernel: Hq * n_tiles; dk/dv kernel: Hkv * n_tiles
     const float* lse;  // [Hq, S] natural log, from the forward
     const float* delta;  // [Hq, S] dout . out per row (bwd_delta_kernel)
+    // [4] item counter and finished-CTA counter of the dq launch, then of the dk/dv launch
+    // (global memory, zero at launch; the last CTA of each launch zeroes its pair again)
+    unsigned int* sched;
     float* dq;
     float* dk;
     float* dv;
