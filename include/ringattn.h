@@ -44,6 +44,11 @@
  *    crosses the ABI and there is no CPU fallback.
  *  - The library allocates no device memory per call; scratch it needs is passed in,
  *    except for ringattn_fwd_docmask_noalloc, which uses a static device array.
+ *  - The fused bf16 kernels (ringattn_fwd*, ringattn_bwd*) hand out their work items
+ *    from counters in a static device array of 256 slots: a launch takes the next slot
+ *    in turn (the backward takes two) and its last block zeroes it again.  Launches in
+ *    flight at the same time on any streams use different slots unless 256 or more of
+ *    them are in flight together.
  */
 #ifndef RINGATTN_H
 #define RINGATTN_H
