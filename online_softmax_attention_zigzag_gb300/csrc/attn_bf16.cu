@@ -640,21 +640,34 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
         tc_fence_after();
         const float inv = (lr > 0.f) ? 1.f / lr : 0.f;
         const uint64_t out_policy = make_policy_evict_first();  // written once, read by the host
+        // read all of O, hand its columns back, then store: 32-byte stores when `out` allows
+        float o[D];
 #pragma unroll
         for (int cc = 0; cc < D; cc += 32) {
-            uint32_t o0[32];
-            tmem_ld32(o_tmem + cc, o0);
-            tmem_wait_ld();
-            float4* dst = reinterpret_cast<float4*>(orow + cc);
+            uint32_t r[32];
+            tmem_ld32(o_tmem + cc, r);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                st_stream_f4(dst + i,
-                             make_float4(__uint_as_float(o0[4 * i]) * inv, __uint_as_float(o0[4 * i + 1]) * inv,
-                                         __uint_as_float(o0[4 * i + 2]) * inv, __uint_as_float(o0[4 * i + 3]) * inv),
-                             out_policy);
+            for (int i = 0; i < 32; ++i) o[cc + i] = __uint_as_float(r[i]);
         }
+        tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&b.o_free[x]);
+#pragma unroll
+        for (int i = 0; i < D; ++i) o[i] *= inv;
+        if ((reinterpret_cast<uintptr_t>(p.out) & 31u) == 0u) {
+#pragma unroll
+            for (int i = 0; i < D; i += 8) {
+                float w8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) w8[e] = o[i + e];
+                st_stream_f8(orow + i, w8, out_policy);
+            }
+        } else {
+            float4* dst = reinterpret_cast<float4*>(orow);
+#pragma unroll
+            for (int i = 0; i < D / 4; ++i)
+                st_stream_f4(dst + i, make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]), out_policy);
+        }
         p.lse[grow] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
     }
 }

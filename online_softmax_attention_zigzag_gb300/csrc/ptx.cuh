@@ -158,6 +158,13 @@ __device__ __forceinline__ void st_stream_f4(float4* dst, float4 v, uint64_t pol
                  "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "l"(policy)
                  : "memory");
 }
+// 32-byte streaming store (dst 32-byte aligned)
+__device__ __forceinline__ void st_stream_f8(float* dst, const float (&v)[8], uint64_t policy) {
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(
+                     dst),
+                 "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "l"(policy)
+                 : "memory");
+}
 // 1-D bulk copy global -> shared that completes `bytes` on `bar`; both addresses
 // 16-byte aligned and bytes a multiple of 16.
 __device__ __forceinline__ void bulk_load_1d(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
