@@ -52,10 +52,7 @@ constexpr int kTile = 128;
 constexpr int kThreads = 352;  // 2 softmax warpgroups + two MMA warps + TMA warp
 constexpr int kMmaWarp = 8, kLoadWarp = 10;  // warp 8 + x issues the MMAs of unit x
 constexpr float kLog2e = 1.4426950408889634f;
-// Work items are taken dynamically: the loader draws the next item index from a counter in
-// global memory and passes it to the other roles through a ring of this many entries.
-constexpr int kItemRing = 4;
-constexpr uint32_t kItemTakers = 10;  // 2 MMA issuers + 8 softmax warps
+constexpr uint32_t kItemTakers = 10;  // work-item takers: 2 MMA issuers + 8 softmax warps
 constexpr float kLn2 = 0.69314718055994531f;
 // The running max used for P is only moved when the true max exceeds it by more
 // than this (log2 units): P then stays below 2^8 and O needs no rescale otherwise.
@@ -93,19 +90,6 @@ struct Bars {
     uint64_t* item_full;   // [kItemRing] loader -> issuers, softmax warps (item id written)
     uint64_t* item_empty;  // [kItemRing] issuers, softmax warps (one arrival each) -> loader
 };
-
-// Entry k of the item sequence as the loader published it: an item index, -1 at the end,
-// -2 on abort.  Every taker takes every entry, in order; one arrival per taker (`leader`
-// is lane 0 of a softmax warp, or an issuer thread) frees the ring slot.
-__device__ __forceinline__ int take_item(const Bars& b, const volatile int* ring, uint32_t k, bool leader,
-                                         const WaitCtl& wc) {
-    const uint32_t slot = k % kItemRing;
-    if (!mbar_wait(&b.item_full[slot], (k / kItemRing) & 1u, wc)) return -2;
-    const int item = ring[slot];
-    __syncwarp(__activemask());
-    if (leader) mbar_arrive(&b.item_empty[slot]);
-    return item;
-}
 
 // A work item: up to two query tiles (units) of one rank that share a KV head.
 struct Item {
@@ -284,12 +268,8 @@ __device__ void load_role(const AttnBf16Params& p, const CUtensorMap* tq, const 
     };
     for (uint32_t k = 0; ok; ++k) {
         // draw the next item and publish it (or the end of the sequence)
-        const uint32_t slot = k % kItemRing;
-        if (!mbar_wait(&b.item_empty[slot], ((k / kItemRing) & 1u) ^ 1u, wc, 32)) { ok = false; break; }
-        int item = static_cast<int>(atomicAdd(p.sched, 1u));
-        if (item >= p.n_items) item = -1;
-        ring[slot] = item;
-        mbar_arrive(&b.item_full[slot]);
+        const int item = publish_item(p.sched, p.n_items, b.item_full, b.item_empty, ring, k, wc);
+        if (item == -2) { ok = false; break; }
         if (item < 0) break;
         Item it;
         decode_item<DOC>(p, item, it);
@@ -435,7 +415,7 @@ __device__ void mma_role(const AttnBf16Params& p, int x, uint8_t* sQ, uint8_t* s
         return r;
     };
     for (uint32_t k = 0; ok; ++k) {
-        const int item = take_item(b, ring, k, true, wc);
+        const int item = take_item(b.item_full, b.item_empty, ring, k, true, wc);
         if (item == -2) { ok = false; break; }
         if (item < 0) break;
         Item it;
@@ -513,7 +493,7 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
     uint32_t sit = 0, iit = 0;
     bool ok = true;
     for (uint32_t k = 0; ok; ++k) {
-        const int item = take_item(b, ring, k, lane == 0, wc);
+        const int item = take_item(b.item_full, b.item_empty, ring, k, lane == 0, wc);
         if (item == -2) { ok = false; break; }
         if (item < 0) break;
         Item it;
@@ -751,15 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
-    // the last CTA to finish re-zeroes the item counter for the next launch that uses it
-    if (threadIdx.x == 0) {
-        __threadfence();
-        if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
-            p.sched[0] = 0u;
-            p.sched[1] = 0u;
-            __threadfence();
-        }
-    }
+    if (threadIdx.x == 0) finish_items(p.sched);
 }
 
 template <int D, bool DOC>

@@ -51,10 +51,7 @@ constexpr int kMmaWarp = 8, kLoadWarp = 9;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 256;
-// Work items are drawn dynamically: the loader takes the next index from a counter in
-// global memory and hands it to the MMA issuer and the 8 compute warps through a ring.
-constexpr int kItemRing = 4;
-constexpr uint32_t kItemTakers = 9;
+constexpr uint32_t kItemTakers = 9;  // work-item takers: the MMA issuer + 8 compute warps
 
 // Shared memory of both kernels: two resident tiles (Q, dO or K, V), then ring A (three
 // slots: K for dq, Q for dk/dv) and ring B (two slots: V for dq, dO for dk/dv).
@@ -271,35 +268,16 @@ __device__ __forceinline__ void init_bars(const Bars& b) {
     }
 }
 
-// The loader draws entry k of the item sequence from the launch's counter and publishes it
-// (-1 past the last item); -2 on abort.
-__device__ __forceinline__ int publish_item(const AttnBwdParams& p, const Bars& b, volatile int* ring, uint32_t k,
-                                            const WaitCtl& wc) {
-    const uint32_t slot = k % kItemRing;
-    if (!mbar_wait(&b.item_empty[slot], ((k / kItemRing) & 1u) ^ 1u, wc, 32)) return -2;
-    int item = static_cast<int>(atomicAdd(p.sched, 1u));
-    if (item >= p.n_items) item = -1;
-    ring[slot] = item;
-    mbar_arrive(&b.item_full[slot]);
-    return item;
-}
-
-// Every other role takes every entry, in order; one arrival per taker frees the slot.
-__device__ __forceinline__ int take_item(const Bars& b, const volatile int* ring, uint32_t k, bool leader,
-                                         const WaitCtl& wc) {
-    const uint32_t slot = k % kItemRing;
-    if (!mbar_wait(&b.item_full[slot], (k / kItemRing) & 1u, wc)) return -2;
-    const int item = ring[slot];
-    __syncwarp(__activemask());
-    if (leader) mbar_arrive(&b.item_empty[slot]);
-    return item;
-}
-
 // Wait (one poller warp per warpgroup, the rest in the group's named barrier).
 __device__ __forceinline__ bool group_wait(uint64_t* bar, uint32_t parity, int h, int wq, const WaitCtl& wc) {
     bool ok = true;
     if (wq == 0) ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
     return group_bar_and(h, ok);
+}
+
+// Wait with every lane of the warp polling (no named barrier).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& wc) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
 }
 
 // Copy 64 fp32 TMEM columns of this lane into registers, then release them.
@@ -344,7 +322,7 @@ __device__ void dq_load(const AttnBwdParams& p, const CUtensorMap* tq, const CUt
     uint32_t ka = 0, vb = 0, qit = 0;
     bool ok = true;
     for (uint32_t n_it = 0; ok; ++n_it) {
-        const int item = publish_item(p, b, ring, n_it, wc);
+        const int item = publish_item(p.sched, p.n_items, b.item_full, b.item_empty, ring, n_it, wc);
         if (item == -2) { ok = false; break; }
         if (item < 0) break;
         int hq, qp;
@@ -384,7 +362,7 @@ __device__ void dq_mma(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uin
     uint32_t idx = 0, qit = 0, sf = 0, dpf = 0, dsit[2] = {0, 0};
     bool ok = true;
     for (uint32_t n_it = 0; ok; ++n_it) {
-        const int item = take_item(b, ring, n_it, true, wc);
+        const int item = take_item(b.item_full, b.item_empty, ring, n_it, true, wc);
         if (item == -2) { ok = false; break; }
         if (item < 0) break;
         int hq, qp;
@@ -458,7 +436,7 @@ __device__ void dq_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
     uint32_t sf = 0, dpf = 0, it = 0;
     bool ok = true;
     for (uint32_t n_it = 0; ok; ++n_it) {
-        const int item = take_item(b, ring, n_it, lane == 0, wc);
+        const int item = take_item(b.item_full, b.item_empty, ring, n_it, lane == 0, wc);
         if (item == -2) { ok = false; break; }
         if (item < 0) break;
         int hq, qp;
@@ -469,7 +447,7 @@ __device__ void dq_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
         const int qpos = qp + row;
         uint32_t jj = 0;  // tile within the item
         for_each_key_tile(R, qp, [&](int t0) -> bool {
-            if (!group_wait(b.s_full, sf & 1u, h, wq, wc)) { ok = false; return false; }
+            if (!warp_wait(b.s_full, sf & 1u, wc)) { ok = false; return false; }
             ++sf;
             tc_fence_after();
             float x[64];
@@ -489,7 +467,7 @@ __device__ void dq_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
                 x[i] = p0;
                 x[i + 1] = p1;
             }
-            if (!group_wait(b.dp_full, dpf & 1u, h, wq, wc)) { ok = false; return false; }
+            if (!warp_wait(b.dp_full, dpf & 1u, wc)) { ok = false; return false; }
             ++dpf;
             tc_fence_after();
             float dp[64];
@@ -506,7 +484,7 @@ __device__ void dq_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
             return true;
         });
         if (!ok) break;
-        if (!group_wait(b.acc_done, it & 1u, h, wq, wc)) { ok = false; break; }
+        if (!warp_wait(b.acc_done, it & 1u, wc)) { ok = false; break; }
         ++it;
         tc_fence_after();
         store_acc<D / 2>(acc_tm, p.dq + static_cast<size_t>(grow) * D + h * (D / 2));
@@ -527,7 +505,7 @@ __device__ void kv_load(const AttnBwdParams& p, const CUtensorMap* tq, const CUt
     uint32_t qa = 0, ob = 0, kit = 0;
     bool ok = true;
     for (uint32_t n_it = 0; ok; ++n_it) {
-        const int item = publish_item(p, b, ring, n_it, wc);
+        const int item = publish_item(p.sched, p.n_items, b.item_full, b.item_empty, ring, n_it, wc);
         if (item == -2) { ok = false; break; }
         if (item < 0) break;
         int hk, kp;
@@ -566,7 +544,7 @@ __device__ void kv_mma(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uin
     uint32_t idx = 0, kit = 0, sf = 0, pf = 0;
     bool ok = true;
     for (uint32_t n_it = 0; ok; ++n_it) {
-        const int item = take_item(b, ring, n_it, true, wc);
+        const int item = take_item(b.item_full, b.item_empty, ring, n_it, true, wc);
         if (item == -2) { ok = false; break; }
         if (item < 0) break;
         int hk, kp;
@@ -644,7 +622,7 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
     uint32_t sf = 0, dpf = 0, it = 0;
     bool ok = true;
     for (uint32_t n_it = 0; ok; ++n_it) {
-        const int item = take_item(b, ring, n_it, lane == 0, wc);
+        const int item = take_item(b.item_full, b.item_empty, ring, n_it, lane == 0, wc);
         if (item == -2) { ok = false; break; }
         if (item < 0) break;
         int hk, kp;
@@ -783,15 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
-    // the last CTA to finish re-zeroes the item counter for the next launch that uses it
-    if (threadIdx.x == 0) {
-        __threadfence();
-        if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
-            p.sched[0] = 0u;
-            p.sched[1] = 0u;
-            __threadfence();
-        }
-    }
+    if (threadIdx.x == 0) finish_items(p.sched);
 }
 
 // ------------------------------------------------------------------ D = dout . out

@@ -110,11 +110,48 @@ __device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool ok) {
     return r != 0;
 }
 
-// Persistent CTAs take work items in snake order: round k of CTA b is item k * grid + b,
-// reversed on odd rounds, so items sorted by decreasing work even out across CTAs.
-__device__ __forceinline__ int item_of_round(int round) {
-    const int b = (round & 1) ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;
-    return round * gridDim.x + b;
+// Dynamic work items of the persistent kernels.  A launch owns two counters in global
+// memory (zero at launch): the next item index and the number of CTAs done.  In each CTA
+// one loader thread draws indices and hands them to the other roles through a ring of
+// kItemRing slots in shared memory, guarded by `full` (count 1) and `empty` (count = the
+// number of takers) mbarriers.
+constexpr int kItemRing = 4;
+
+// Loader: draw entry k of the CTA's item sequence and publish it (-1 past the last item);
+// -2 on abort.
+__device__ __forceinline__ int publish_item(unsigned int* counter, int n_items, uint64_t* full, uint64_t* empty,
+                                            volatile int* ring, uint32_t k, const WaitCtl& wc) {
+    const uint32_t slot = k % kItemRing;
+    if (!mbar_wait(&empty[slot], ((k / kItemRing) & 1u) ^ 1u, wc, 32)) return -2;
+    int item = static_cast<int>(atomicAdd(counter, 1u));
+    if (item >= n_items) item = -1;
+    ring[slot] = item;
+    mbar_arrive(&full[slot]);
+    return item;
+}
+
+// Taker: entry k as the loader published it (an item index, -1 at the end), -2 on abort.
+// Every taker takes every entry, in order; one arrival per taker (`leader`: one lane of
+// a warp, or a lone issuing thread) frees the slot.
+__device__ __forceinline__ int take_item(uint64_t* full, uint64_t* empty, const volatile int* ring, uint32_t k,
+                                         bool leader, const WaitCtl& wc) {
+    const uint32_t slot = k % kItemRing;
+    if (!mbar_wait(&full[slot], (k / kItemRing) & 1u, wc)) return -2;
+    const int item = ring[slot];
+    __syncwarp(__activemask());
+    if (leader) mbar_arrive(&empty[slot]);
+    return item;
+}
+
+// End of a launch: the last CTA to finish zeroes the counters for the next launch that
+// uses them.  Called by one thread per CTA after every role is done.
+__device__ __forceinline__ void finish_items(unsigned int* counter) {
+    __threadfence();
+    if (atomicAdd(counter + 1, 1u) == gridDim.x - 1) {
+        counter[0] = 0u;
+        counter[1] = 0u;
+        __threadfence();
+    }
 }
 
 // ------------------------------------------------------------------ TMA
