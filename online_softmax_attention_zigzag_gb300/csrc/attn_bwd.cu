@@ -25,9 +25,12 @@
 // dk/dv, listed by KV head and decreasing work) from a counter in global memory as it
 // finishes the previous one; its loader hands the index to the other roles through a ring
 // in shared memory.  (Dealing the 2048 key tiles of the 32k GQA dk/dv launch out
-// statically in snake order left the CTAs ~20% apart.)  Warps 0-7 compute (warpgroup h handles columns [64h, 64h+64)
-// of the 128 x 128 tile product, thread = TMEM lane = row), warp 8 issues the MMAs (one
-// thread), warp 9 the TMA loads (one thread).  The compute warps copy S (S^T) and dP
+// statically in snake order left the CTAs ~20% apart.)  Warps 0-7 compute (warpgroup h
+// handles columns [64h, 64h+64) of the 128 x 128 tile product, thread = TMEM lane = row),
+// warp 8 issues the MMAs (one thread), warp 9 the TMA loads (one thread).  In the dq kernel
+// warp 8 issues S and dP only and warp 10 issues dQ += dS K, so that neither issuer's waits
+// hold up the other's products; a K ring slot is then released by both, and a dS buffer is
+// handed back by warp 10 once its dQ product is done.  The compute warps copy S (S^T) and dP
 // (dP^T) from TMEM into registers and release those columns at once, so the next tile's
 // products run on the tensor cores while this tile's exponentials are computed; the
 // streamed operands move through separate shared-memory rings (three slots for the one
@@ -46,12 +49,14 @@ namespace ra {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kThreads = 320;
-constexpr int kMmaWarp = 8, kLoadWarp = 9;
+constexpr int kThreads = 352;
+// warp 8: MMA issuer (dQ kernel: S and dP products); warp 9: TMA loads; warp 10: the dQ
+// kernel's second issuer (dQ += dS K)
+constexpr int kMmaWarp = 8, kLoadWarp = 9, kMma2Warp = 10;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 256;
-constexpr uint32_t kItemTakers = 9;  // work-item takers: the MMA issuer + 8 compute warps
+constexpr uint32_t kItemTakers = 10;  // work-item takers: 2 MMA issuer warps + 8 compute warps
 
 // Shared memory of both kernels: two resident tiles (Q, dO or K, V), then ring A (three
 // slots: K for dq, Q for dk/dv) and ring B (two slots: V for dq, dO for dk/dv).
@@ -233,16 +238,17 @@ struct Bars {
     uint64_t *s_full, *dp_full;      // S (S^T) / dP (dP^T) in TMEM
     uint64_t *s_free, *dp_free;      // 256 compute threads copied S / dP out of TMEM
     uint64_t *ds_full;               // [2] dq: dS buffer written; dk/dv: [0] P^T, dS^T written
-    uint64_t *acc_done, *acc_free, *drain;
+    uint64_t *acc_done, *acc_free, *drain, *drain2;
+    uint64_t *ds_free;  // [2] dQ kernel: the dQ product that read dS buffer b is done
     uint64_t *a_full, *a_empty, *b_full, *b_empty;
     uint64_t *item_full, *item_empty;  // [kItemRing] each: item ids handed from the loader
     __device__ explicit Bars(uint64_t* b)
         : res_full(b), res_empty(b + 1), s_full(b + 2), dp_full(b + 3), s_free(b + 4), dp_free(b + 5),
-          ds_full(b + 6), acc_done(b + 8), acc_free(b + 9), drain(b + 10), a_full(b + 16), a_empty(b + 19),
+          ds_full(b + 6), acc_done(b + 8), acc_free(b + 9), drain(b + 10), drain2(b + 11), ds_free(b + 12), a_full(b + 16), a_empty(b + 19),
           b_full(b + 22), b_empty(b + 24), item_full(b + 26), item_empty(b + 30) {}
 };
 
-__device__ __forceinline__ void init_bars(const Bars& b) {
+__device__ __forceinline__ void init_bars(const Bars& b, uint32_t a_releases) {
     mbar_init(b.res_full, 1);
     mbar_init(b.res_empty, 1);
     mbar_init(b.s_full, 1);
@@ -254,9 +260,12 @@ __device__ __forceinline__ void init_bars(const Bars& b) {
     mbar_init(b.acc_done, 1);
     mbar_init(b.acc_free, 256);
     mbar_init(b.drain, 1);
+    mbar_init(b.drain2, 1);
+    mbar_init(&b.ds_free[0], 1);
+    mbar_init(&b.ds_free[1], 1);
     for (int s = 0; s < 3; ++s) {
         mbar_init(&b.a_full[s], 1);
-        mbar_init(&b.a_empty[s], 1);
+        mbar_init(&b.a_empty[s], a_releases);
     }
     for (int s = 0; s < 2; ++s) {
         mbar_init(&b.b_full[s], 1);
@@ -353,13 +362,15 @@ __device__ void dq_load(const AttnBwdParams& p, const CUtensorMap* tq, const CUt
     }
 }
 
+// dQ kernel, first issuer: S = Q K^T and dP = dO V^T, each as soon as the compute warps
+// have copied the previous tile's out of TMEM.
 template <int D>
 __device__ void dq_mma(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uint32_t tmem, volatile int* ring, const WaitCtl& wc) {
     using C = BwdCfg<D>;
     const Ring& R = p.ring;
     const uint32_t sQ = smem_u32(smem), sdO = sQ + C::kTileBytes;
     const uint32_t sA = sQ + C::kAOff, sB = sQ + C::kBOff;
-    uint32_t idx = 0, qit = 0, sf = 0, dpf = 0, dsit[2] = {0, 0};
+    uint32_t idx = 0, qit = 0, sf = 0, dpf = 0;
     bool ok = true;
     for (uint32_t n_it = 0; ok; ++n_it) {
         const int item = take_item(b.item_full, b.item_empty, ring, n_it, true, wc);
@@ -375,51 +386,85 @@ __device__ void dq_mma(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uin
         tc_fence_after();
         issue_kk<D>(tmem, sQ, sA + (i0 % C::kSlotsA) * C::kTileBytes);
         mma_commit(b.s_full);
+        mma_commit(&b.a_empty[i0 % C::kSlotsA]);  // this issuer is done with K(0)
         if (!ring_wait(b.b_full, i0, C::kSlotsB, wc)) { ok = false; break; }
         tc_fence_after();
         issue_kk<D>(tmem + kTile, sdO, sB + (i0 % C::kSlotsB) * C::kTileBytes);
         mma_commit(b.dp_full);
         mma_commit(&b.b_empty[i0 % C::kSlotsB]);  // V(0) is done once dP(0) is
-        for (int j = 0; j < nj && ok; ++j) {
+        for (int j = 0; j + 1 < nj && ok; ++j) {
             const uint32_t i = i0 + j;
-            const bool more = j + 1 < nj;
-            // the next S as soon as this tile's S is out of TMEM
+            // the next S as soon as this tile's S is out of TMEM, likewise dP
             if (!mbar_wait(b.s_free, sf & 1u, wc)) { ok = false; break; }
             ++sf;
-            if (more) {
-                if (!ring_wait(b.a_full, i + 1, C::kSlotsA, wc)) { ok = false; break; }
-                tc_fence_after();
-                issue_kk<D>(tmem, sQ, sA + ((i + 1) % C::kSlotsA) * C::kTileBytes);
-                mma_commit(b.s_full);
-            }
+            if (!ring_wait(b.a_full, i + 1, C::kSlotsA, wc)) { ok = false; break; }
+            tc_fence_after();
+            issue_kk<D>(tmem, sQ, sA + ((i + 1) % C::kSlotsA) * C::kTileBytes);
+            mma_commit(b.s_full);
+            mma_commit(&b.a_empty[(i + 1) % C::kSlotsA]);
             if (!mbar_wait(b.dp_free, dpf & 1u, wc)) { ok = false; break; }
             ++dpf;
-            if (more) {
-                if (!ring_wait(b.b_full, i + 1, C::kSlotsB, wc)) { ok = false; break; }
-                tc_fence_after();
-                issue_kk<D>(tmem + kTile, sdO, sB + ((i + 1) % C::kSlotsB) * C::kTileBytes);
-                mma_commit(b.dp_full);
-                mma_commit(&b.b_empty[(i + 1) % C::kSlotsB]);
-            }
-            const int bb = j & 1;
-            if (!mbar_wait(&b.ds_full[bb], dsit[bb] & 1u, wc)) { ok = false; break; }
-            ++dsit[bb];
-            if (j == 0 && !mbar_wait(b.acc_free, (qit & 1u) ^ 1u, wc)) { ok = false; break; }
+            if (!ring_wait(b.b_full, i + 1, C::kSlotsB, wc)) { ok = false; break; }
             tc_fence_after();
-            // dQ += dS K, dS from TMEM buffer j % 2, K from its ring slot as an MN-major B
-            issue_tm<D>(tmem + kAccCol, tmem + 384 + 64 * bb, 32, sA + (i % C::kSlotsA) * C::kTileBytes, j > 0);
-            mma_commit(&b.a_empty[i % C::kSlotsA]);
+            issue_kk<D>(tmem + kTile, sdO, sB + ((i + 1) % C::kSlotsB) * C::kTileBytes);
+            mma_commit(b.dp_full);
+            mma_commit(&b.b_empty[(i + 1) % C::kSlotsB]);
         }
         if (!ok) break;
+        // the last tile's S and dP still have to be copied out before the next item's
+        if (!mbar_wait(b.s_free, sf & 1u, wc) || !mbar_wait(b.dp_free, dpf & 1u, wc)) { ok = false; break; }
+        ++sf;
+        ++dpf;
         idx = i0 + nj;
-        mma_commit(b.res_empty);
-        mma_commit(b.acc_done);
+        mma_commit(b.res_empty);  // Q and dO of this item are done with
         ++qit;
     }
     if (!ok) {
         // every MMA issued so far must finish before TMEM is released
         mma_commit(b.drain);
         drain_wait(b.drain, 0, wc.timeout_ns);
+    }
+}
+
+// dQ kernel, second issuer: dQ += dS K for every key tile, as the compute warps hand dS over.
+template <int D>
+__device__ void dq_mma2(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uint32_t tmem, volatile int* ring,
+                        const WaitCtl& wc) {
+    using C = BwdCfg<D>;
+    const Ring& R = p.ring;
+    const uint32_t sA = smem_u32(smem) + C::kAOff;
+    uint32_t idx = 0, it = 0, dsit[2] = {0, 0};
+    bool ok = true;
+    for (uint32_t n_it = 0; ok; ++n_it) {
+        const int item = take_item(b.item_full, b.item_empty, ring, n_it, true, wc);
+        if (item == -2) { ok = false; break; }
+        if (item < 0) break;
+        int hq, qp;
+        dq_item(p, item, hq, qp);
+        const int nj = count_key_tiles(R, qp);
+        for (int j = 0; j < nj && ok; ++j) {
+            const uint32_t i = idx + j;
+            const int bb = j & 1;
+            if (!mbar_wait(&b.ds_full[bb], dsit[bb] & 1u, wc)) { ok = false; break; }
+            ++dsit[bb];
+            if (j == 0 && !mbar_wait(b.acc_free, (it & 1u) ^ 1u, wc)) { ok = false; break; }
+            // K(j) landed before the S(j) that led to this dS; its slot cannot have been
+            // refilled, since this issuer has not released it yet
+            if (!ring_wait(b.a_full, i, C::kSlotsA, wc)) { ok = false; break; }
+            tc_fence_after();
+            // dQ += dS K, dS from TMEM buffer j % 2, K from its ring slot as an MN-major B
+            issue_tm<D>(tmem + kAccCol, tmem + 384 + 64 * bb, 32, sA + (i % C::kSlotsA) * C::kTileBytes, j > 0);
+            mma_commit(&b.a_empty[i % C::kSlotsA]);
+            mma_commit(&b.ds_free[bb]);
+        }
+        if (!ok) break;
+        idx += nj;
+        mma_commit(b.acc_done);
+        ++it;
+    }
+    if (!ok) {
+        mma_commit(b.drain2);
+        drain_wait(b.drain2, 0, wc.timeout_ns);
     }
 }
 
@@ -433,7 +478,7 @@ __device__ void dq_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
     const uint32_t s_tm = tmem + lane_off + h * 64;           // my 64 key columns of S
     const uint32_t dp_tm = tmem + lane_off + kTile + h * 64;  // and of dP
     const uint32_t acc_tm = tmem + lane_off + kAccCol + h * (D / 2);
-    uint32_t sf = 0, dpf = 0, it = 0;
+    uint32_t sf = 0, dpf = 0, it = 0, dsf[2] = {0, 0};
     bool ok = true;
     for (uint32_t n_it = 0; ok; ++n_it) {
         const int item = take_item(b.item_full, b.item_empty, ring, n_it, lane == 0, wc);
@@ -476,6 +521,9 @@ __device__ void dq_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
 #pragma unroll
             for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(x[2 * i] * (dp[2 * i] - dl), x[2 * i + 1] * (dp[2 * i + 1] - dl));
             const int bb = jj & 1;  // dS buffer, as the MMA issuer counts it
+            // the dQ product of two tiles ago, issued by the other issuer, has read it
+            if (!warp_wait(&b.ds_free[bb], (dsf[bb] & 1u) ^ 1u, wc)) { ok = false; return false; }
+            ++dsf[bb];
             tmem_st32(tmem + lane_off + 384 + 64 * bb + 32 * h, pk);
             tmem_wait_st();
             tc_fence_before();
@@ -723,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kBarOff + C::kNumBars * 8 + 4);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
-        init_bars(b);
+        init_bars(b, DQ ? 2u : 1u);  // dQ kernel: a K slot is released by both issuers
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -755,6 +803,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             if constexpr (DQ) dq_load<D>(p, &tq, &tdo, &tk, &tv, smem, b, ring, wc);
             else kv_load<D>(p, &tq, &tdo, &tk, &tv, smem, b, ring, wc);
+        }
+    } else if (warp == kMma2Warp) {
+        if (lane == 0) {
+            if constexpr (DQ) {
+                dq_mma2<D>(p, smem, b, tmem, ring, wc);
+            } else {  // no second issuer in the dk/dv kernel: take the items only
+                for (uint32_t n_it = 0; take_item(b.item_full, b.item_empty, ring, n_it, true, wc) >= 0; ++n_it) {
+                }
+            }
         }
     }
     tc_fence_before();
