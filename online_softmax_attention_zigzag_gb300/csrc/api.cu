@@ -279,12 +279,13 @@ int doc_scratch(int** out) {
 // g-1 run on two internal streams (one per copy direction) while group g computes on the
 // caller's stream.  Streams and events are created once per device and kept until exit.
 constexpr int kMaxGroups = 16;
+constexpr int kMaxLaunches = kMaxGroups + 2;  // the first and last group may run as two halves
 
 struct HostPipe {
     bool ready = false;
     cudaStream_t h2d = nullptr, d2h = nullptr;
     cudaEvent_t start = nullptr, done = nullptr;
-    cudaEvent_t in[kMaxGroups] = {}, out[kMaxGroups] = {};
+    cudaEvent_t in[kMaxLaunches] = {}, out[kMaxLaunches] = {};
     std::mutex mu;  // one call enqueues at a time per device
 };
 
@@ -303,7 +304,7 @@ int host_pipe(HostPipe** out) {
             cudaEventCreateWithFlags(&hp.start, ef) != cudaSuccess ||
             cudaEventCreateWithFlags(&hp.done, ef) != cudaSuccess)
             return RA_ERR_CUDA;
-        for (int i = 0; i < kMaxGroups; ++i)
+        for (int i = 0; i < kMaxLaunches; ++i)
             if (cudaEventCreateWithFlags(&hp.in[i], ef) != cudaSuccess ||
                 cudaEventCreateWithFlags(&hp.out[i], ef) != cudaSuccess)
                 return RA_ERR_CUDA;
@@ -357,37 +358,56 @@ int fwd_host(const void* q_h, const void* k_h, const void* v_h, float* out_h, fl
     char* base = static_cast<char*>(ws);
     const int G = host_groups(S, Hq, Hkv, dev->sms);
     const int hq_g = Hq / G, hkv_g = Hkv / G;
-    const size_t q_b = 2ull * hq_g * S * d, kv_b = 2ull * hkv_g * S * d;
-    const size_t o_b = 4ull * hq_g * S * d, l_b = 4ull * hq_g * S;
+    // Launches: one per group, except that the first and the last group run as two halves
+    // of their query heads when a group has one KV head: the first launch then starts after
+    // less input has crossed, and the last results start back sooner.  Each half is the
+    // same per-head computation, so the result does not depend on the split.
+    struct Launch { int g, h0, hn; };  // group g, its query heads [h0, h0 + hn)
+    Launch L[kMaxLaunches];
+    int nl = 0;
+    const bool halves = G >= 2 && hkv_g == 1 && hq_g % 2 == 0;
+    for (int gi = 0; gi < G; ++gi) {
+        if (halves && (gi == 0 || gi == G - 1)) {
+            L[nl++] = {gi, 0, hq_g / 2};
+            L[nl++] = {gi, hq_g / 2, hq_g / 2};
+        } else {
+            L[nl++] = {gi, 0, hq_g};
+        }
+    }
+    const size_t qh_b = 2ull * S * d, oh_b = 4ull * S * d, lh_b = 4ull * S;  // one query head's rows
+    const size_t kv_b = 2ull * hkv_g * S * d;
     std::lock_guard<std::mutex> lock(hp->mu);
     // the copies start only after the work already queued on `stream`
     if (cudaEventRecord(hp->start, stream) != cudaSuccess || cudaStreamWaitEvent(hp->h2d, hp->start, 0) != cudaSuccess)
         return RA_ERR_CUDA;
-    for (int gi = 0; gi < G; ++gi) {
-        char* qd = base + off[0] + gi * q_b;
-        char* kd = base + off[1] + gi * kv_b;
-        char* vd = base + off[2] + gi * kv_b;
-        if (cudaMemcpyAsync(kd, static_cast<const char*>(k_h) + gi * kv_b, kv_b, cudaMemcpyHostToDevice,
-                            hp->h2d) != cudaSuccess ||
-            cudaMemcpyAsync(vd, static_cast<const char*>(v_h) + gi * kv_b, kv_b, cudaMemcpyHostToDevice,
-                            hp->h2d) != cudaSuccess ||
-            cudaMemcpyAsync(qd, static_cast<const char*>(q_h) + gi * q_b, q_b, cudaMemcpyHostToDevice,
-                            hp->h2d) != cudaSuccess ||
-            cudaEventRecord(hp->in[gi], hp->h2d) != cudaSuccess)
+    for (int li = 0; li < nl; ++li) {
+        const int gi = L[li].g;
+        const size_t h0 = static_cast<size_t>(gi) * hq_g + L[li].h0;  // first query head of the launch
+        if (L[li].h0 == 0 &&  // K and V once per group, ahead of its first launch
+            (cudaMemcpyAsync(base + off[1] + gi * kv_b, static_cast<const char*>(k_h) + gi * kv_b, kv_b,
+                             cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess ||
+             cudaMemcpyAsync(base + off[2] + gi * kv_b, static_cast<const char*>(v_h) + gi * kv_b, kv_b,
+                             cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess))
+            return RA_ERR_CUDA;
+        if (cudaMemcpyAsync(base + off[0] + h0 * qh_b, static_cast<const char*>(q_h) + h0 * qh_b, L[li].hn * qh_b,
+                            cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess ||
+            cudaEventRecord(hp->in[li], hp->h2d) != cudaSuccess)
             return RA_ERR_CUDA;
     }
-    for (int gi = 0; gi < G; ++gi) {
-        float* od = reinterpret_cast<float*>(base + off[3] + gi * o_b);
-        float* ld = reinterpret_cast<float*>(base + off[4] + gi * l_b);
-        if (cudaStreamWaitEvent(stream, hp->in[gi], 0) != cudaSuccess) return RA_ERR_CUDA;
-        st = fwd_bf16(base + off[0] + gi * q_b, base + off[1] + gi * kv_b, base + off[2] + gi * kv_b, od, ld, S,
-                      hq_g, hkv_g, d, c, causal, layout, kv_block, 1, -1, 0, -1, stream);
+    for (int li = 0; li < nl; ++li) {
+        const int gi = L[li].g;
+        const size_t h0 = static_cast<size_t>(gi) * hq_g + L[li].h0;
+        float* od = reinterpret_cast<float*>(base + off[3] + h0 * oh_b);
+        float* ld = reinterpret_cast<float*>(base + off[4] + h0 * lh_b);
+        if (cudaStreamWaitEvent(stream, hp->in[li], 0) != cudaSuccess) return RA_ERR_CUDA;
+        st = fwd_bf16(base + off[0] + h0 * qh_b, base + off[1] + gi * kv_b, base + off[2] + gi * kv_b, od, ld, S,
+                      L[li].hn, hkv_g, d, c, causal, layout, kv_block, 1, -1, 0, -1, stream);
         if (st != RA_OK) return st;
-        if (cudaEventRecord(hp->out[gi], stream) != cudaSuccess || cudaStreamWaitEvent(hp->d2h, hp->out[gi], 0) != cudaSuccess ||
-            cudaMemcpyAsync(reinterpret_cast<char*>(out_h) + gi * o_b, od, o_b, cudaMemcpyDeviceToHost, hp->d2h) !=
-                cudaSuccess ||
-            cudaMemcpyAsync(reinterpret_cast<char*>(lse_h) + gi * l_b, ld, l_b, cudaMemcpyDeviceToHost, hp->d2h) !=
-                cudaSuccess)
+        if (cudaEventRecord(hp->out[li], stream) != cudaSuccess || cudaStreamWaitEvent(hp->d2h, hp->out[li], 0) != cudaSuccess ||
+            cudaMemcpyAsync(reinterpret_cast<char*>(out_h) + h0 * oh_b, od, L[li].hn * oh_b, cudaMemcpyDeviceToHost,
+                            hp->d2h) != cudaSuccess ||
+            cudaMemcpyAsync(reinterpret_cast<char*>(lse_h) + h0 * lh_b, ld, L[li].hn * lh_b, cudaMemcpyDeviceToHost,
+                            hp->d2h) != cudaSuccess)
             return RA_ERR_CUDA;
     }
     // `stream` completes only once the last result has reached the host
