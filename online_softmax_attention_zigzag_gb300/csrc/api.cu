@@ -279,7 +279,7 @@ int doc_scratch(int** out) {
 // g-1 run on two internal streams (one per copy direction) while group g computes on the
 // caller's stream.  Streams and events are created once per device and kept until exit.
 constexpr int kMaxGroups = 16;
-constexpr int kMaxLaunches = kMaxGroups + 2;  // the first and last group may run as two halves
+constexpr int kMaxLaunches = kMaxGroups + 4;  // the first and last group may run as three launches
 
 struct HostPipe {
     bool ready = false;
@@ -366,8 +366,17 @@ int fwd_host(const void* q_h, const void* k_h, const void* v_h, float* out_h, fl
     Launch L[kMaxLaunches];
     int nl = 0;
     const bool halves = G >= 2 && hkv_g == 1 && hq_g % 2 == 0;
+    const bool quarters = halves && hq_g % 4 == 0;
     for (int gi = 0; gi < G; ++gi) {
-        if (halves && (gi == 0 || gi == G - 1)) {
+        if (quarters && gi == 0) {  // quarter, quarter, half
+            L[nl++] = {gi, 0, hq_g / 4};
+            L[nl++] = {gi, hq_g / 4, hq_g / 4};
+            L[nl++] = {gi, hq_g / 2, hq_g / 2};
+        } else if (quarters && gi == G - 1) {  // half, quarter, quarter
+            L[nl++] = {gi, 0, hq_g / 2};
+            L[nl++] = {gi, hq_g / 2, hq_g / 4};
+            L[nl++] = {gi, 3 * hq_g / 4, hq_g / 4};
+        } else if (halves && (gi == 0 || gi == G - 1)) {
             L[nl++] = {gi, 0, hq_g / 2};
             L[nl++] = {gi, hq_g / 2, hq_g / 2};
         } else {
