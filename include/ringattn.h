@@ -48,7 +48,9 @@
  *    from counters in a static device array of 256 slots: a launch takes the next slot
  *    in turn (the backward takes two) and its last block zeroes it again.  Launches in
  *    flight at the same time on any streams use different slots unless 256 or more of
- *    them are in flight together.
+ *    them are in flight together.  A call captured into a CUDA graph keeps the slot it
+ *    took at capture: two executable graphs instantiated from one capture must not run
+ *    at the same time.
  */
 #ifndef RINGATTN_H
 #define RINGATTN_H
