@@ -25,7 +25,9 @@
 //     shared memory with TMA (128-byte swizzle), through a ring of stages guarded by
 //     mbarriers; a stage pairs the V tile of one key tile with the K tile of the next,
 //     which is what the MMA issuers consume together (one wait, one release per tile);
-//   * warps 8 and 9 (one thread each) issue tcgen05.mma for units 0 and 1: S_x = Q_x K^T
+//   * warps 8 and 9 issue tcgen05.mma for units 0 and 1 (the whole warp runs the issuer,
+//     keeping descriptors and counters warp-uniform; one elected lane issues each
+//     instruction): S_x = Q_x K^T
 //     into TMEM, and after softmax O_x += P_x V with P_x read from TMEM.  They take
 //     turns batch by batch through a counter in shared memory, so the tensor pipe sees
 //     each unit's batch whole while one issuer's waits and commits overlap the other's
@@ -329,9 +331,9 @@ __device__ __forceinline__ void mma_ss8(uint32_t d_tmem, uint32_t alo, uint32_t 
     for (int kk = 0; kk < 8; ++kk) {
         const uint32_t off = (kk / 4) * step_box + (kk % 4) * step_lo4;
         asm volatile(
-            "{\n\t.reg .b64 da, db;\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "mov.b64 da, {%1, %5};\n\tmov.b64 db, {%2, %5};\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+            "{\n\t.reg .b64 da, db;\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "mov.b64 da, {%1, %5};\n\tmov.b64 db, {%2, %5};\n\telect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
             "r"(alo + off), "r"(blo + off), "r"(idesc), "r"(kk > 0 ? 1u : acc), "r"(kSdescHi)
             : "memory");
     }
@@ -350,8 +352,13 @@ __device__ __forceinline__ void issue_s(uint32_t tmem, int x, uint32_t q_base, u
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
             const uint32_t off = (kk * 32) >> 4;
-            mma_ss(d_tmem, (static_cast<uint64_t>(kSdescHi) << 32) | (qlo + off),
-                   (static_cast<uint64_t>(kSdescHi) << 32) | (klo + off), idesc, kk > 0 ? 1u : 0u);
+            const uint64_t qa = (static_cast<uint64_t>(kSdescHi) << 32) | (qlo + off);
+            const uint64_t kb = (static_cast<uint64_t>(kSdescHi) << 32) | (klo + off);
+            asm volatile(
+                "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+                "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                "l"(qa), "l"(kb), "r"(idesc), "r"(kk > 0 ? 1u : 0u)
+                : "memory");
         }
     }
 }
@@ -367,9 +374,9 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, int x, uint32_t v_base, 
 #pragma unroll
     for (int kk = 0; kk < kTile / 16; ++kk) {
         asm volatile(
-            "{\n\t.reg .b64 db;\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "mov.b64 db, {%2, %5};\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
+            "{\n\t.reg .b64 db;\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "mov.b64 db, {%2, %5};\n\telect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
             "r"(a_tmem + kk * 8), "r"(vlo + ((kk * 16 * 128) >> 4)), "r"(idesc), "r"(kk > 0 ? 1u : acc),
             "r"(kSdescHi)
             : "memory");
@@ -410,12 +417,12 @@ __device__ void mma_role(const AttnBf16Params& p, int x, uint8_t* sQ, uint8_t* s
     auto wait_stage = [&](uint32_t& s, uint32_t& base) -> bool {
         s = st_idx % C::kStages;
         base = sKVa + s * C::kStageBytes;
-        const bool r = mbar_wait(&b.kv_full[s], (st_idx / C::kStages) & 1u, wc);
+        const bool r = mbar_wait_w(&b.kv_full[s], (st_idx / C::kStages) & 1u, wc);
         ++st_idx;
         return r;
     };
     for (uint32_t k = 0; ok; ++k) {
-        const int item = take_item(b.item_full, b.item_empty, ring, k, true, wc);
+        const int item = take_item(b.item_full, b.item_empty, ring, k, (threadIdx.x & 31) == 0, wc);
         if (item == -2) { ok = false; break; }
         if (item < 0) break;
         Item it;
@@ -427,48 +434,48 @@ __device__ void mma_role(const AttnBf16Params& p, int x, uint8_t* sQ, uint8_t* s
             for (int i = 0; i <= nj && ok; ++i) {
                 uint32_t s, base;
                 if (!wait_stage(s, base)) { ok = false; break; }
-                mbar_arrive(&b.kv_empty[s]);
+                if ((threadIdx.x & 31) == 0) mbar_arrive(&b.kv_empty[s]);
             }
             seq += 1 + nj;
             continue;
         }
         // batch numbers: S(0) of unit x is seq + x, tile j of unit x is seq + nx (j + 1) + x
-        if (!mbar_wait(&b.q_full[x], qit & 1u, wc)) { ok = false; break; }
+        if (!mbar_wait_w(&b.q_full[x], qit & 1u, wc)) { ok = false; break; }
         uint32_t s, base;
         if (!wait_stage(s, base)) { ok = false; break; }
-        if (!wait_turn(turn, seq + x, wc)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, wait_turn(turn, seq + x, wc))) { ok = false; break; }
         tc_fence_after();
         issue_s<D>(tmem, x, sQa, base + C::kTileBytes);
-        mma_commit(&b.s_full[x]);
+        mma_commit_e(&b.s_full[x]);
         *turn = seq + x + 1;
-        mma_commit(&b.kv_empty[s]);
-        if (nj == 1) mma_commit(&b.q_empty[x]);
+        mma_commit_e(&b.kv_empty[s]);
+        if (nj == 1) mma_commit_e(&b.q_empty[x]);
         for (int j = 0; j < nj && ok; ++j) {
             // this stage holds V(j) and, unless j is the last tile, K(j+1)
             if (!wait_stage(s, base)) { ok = false; break; }
-            if (!mbar_wait(&b.p_full[x], pit & 1u, wc)) { ok = false; break; }
+            if (!mbar_wait_w(&b.p_full[x], pit & 1u, wc)) { ok = false; break; }
             ++pit;
-            if (j == 0 && !mbar_wait(&b.o_free[x], (qit & 1u) ^ 1u, wc)) { ok = false; break; }
+            if (j == 0 && !mbar_wait_w(&b.o_free[x], (qit & 1u) ^ 1u, wc)) { ok = false; break; }
             const uint32_t mine = seq + nx * (j + 1) + x;
-            if (!wait_turn(turn, mine, wc)) { ok = false; break; }
+            if (!__all_sync(0xffffffffu, wait_turn(turn, mine, wc))) { ok = false; break; }
             tc_fence_after();
             issue_pv<D>(tmem, x, base, j > 0);
             if (j + 1 < nj) {
                 issue_s<D>(tmem, x, sQa, base + C::kTileBytes);
-                mma_commit(&b.s_full[x]);
+                mma_commit_e(&b.s_full[x]);
             } else {
-                mma_commit(&b.o_done[x]);
+                mma_commit_e(&b.o_done[x]);
             }
             *turn = mine + 1;
-            mma_commit(&b.kv_empty[s]);
-            if (j + 2 == nj) mma_commit(&b.q_empty[x]);
+            mma_commit_e(&b.kv_empty[s]);
+            if (j + 2 == nj) mma_commit_e(&b.q_empty[x]);
         }
         seq += nx * (nj + 1);
         ++qit;
     }
     if (!ok) {
         // every MMA this thread issued must finish before TMEM is released
-        mma_commit(&b.drain[x]);
+        mma_commit_e(&b.drain[x]);
         drain_wait(&b.drain[x], 0, wc.timeout_ns);
     }
 }
@@ -722,7 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < 8) {
         softmax_role<D, DOC>(p, warp / 4, b, tmem, ring, wc);
     } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-        if (lane == 0) mma_role<D, DOC>(p, warp - kMmaWarp, sQ, sKV, b, tmem, turn, ring, wc);
+        mma_role<D, DOC>(p, warp - kMmaWarp, sQ, sKV, b, tmem, turn, ring, wc);
     } else if (warp == kLoadWarp) {
         if (lane == 0) load_role<D, DOC>(p, &tq, &tk, &tv, sQ, sKV, b, ring, wc);
     }

@@ -27,7 +27,9 @@
 // in shared memory.  (Dealing the 2048 key tiles of the 32k GQA dk/dv launch out
 // statically in snake order left the CTAs ~20% apart.)  Warps 0-7 compute (warpgroup h
 // handles columns [64h, 64h+64) of the 128 x 128 tile product, thread = TMEM lane = row),
-// warp 8 issues the MMAs (one thread), warp 9 the TMA loads (one thread).  In the dq kernel
+// warp 8 issues the MMAs (the whole warp runs the issuer so that its descriptors stay
+// warp-uniform; one elected lane issues each instruction), warp 9 the TMA loads (one
+// thread).  In the dq kernel
 // warp 8 issues S and dP only and warp 10 issues dQ += dS K, so that neither issuer's waits
 // hold up the other's products; a K ring slot is then released by both, and a dS buffer is
 // handed back by warp 10 once its dQ product is done.  The compute warps copy S (S^T) and dP
@@ -169,7 +171,7 @@ __device__ __forceinline__ void issue_kk(uint32_t d_tmem, uint32_t a_base, uint3
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk / 4) * C::kBoxBytes + (kk % 4) * 32) >> 4;
-        mma_ss(d_tmem, desc_add(ad, off), desc_add(bd, off), idesc, kk > 0 ? 1u : 0u);
+        mma_ss_e(d_tmem, desc_add(ad, off), desc_add(bd, off), idesc, kk > 0 ? 1u : 0u);
     }
 }
 
@@ -185,8 +187,8 @@ __device__ __forceinline__ void issue_tm(uint32_t d_tmem, uint32_t a_tmem, uint3
 #pragma unroll
     for (int kk = 0; kk < kTile / 16; ++kk) {
         const uint32_t acol = (kk / 4) * a_half + (kk % 4) * 8;
-        mma_ts(d_tmem, a_tmem + acol, desc_add(bd, (kk * 16 * 128) >> 4), idesc,
-               (accumulate || kk > 0) ? 1u : 0u);
+        mma_ts_e(d_tmem, a_tmem + acol, desc_add(bd, (kk * 16 * 128) >> 4), idesc,
+                 (accumulate || kk > 0) ? 1u : 0u);
     }
 }
 
@@ -311,6 +313,9 @@ __device__ __forceinline__ bool ring_load(uint8_t* ring, uint64_t* full, uint64_
 __device__ __forceinline__ bool ring_wait(uint64_t* full, uint32_t i, int n, const WaitCtl& wc) {
     return mbar_wait(&full[i % n], (i / n) & 1u, wc);
 }
+__device__ __forceinline__ bool ring_wait_w(uint64_t* full, uint32_t i, int n, const WaitCtl& wc) {
+    return mbar_wait_w(&full[i % n], (i / n) & 1u, wc);
+}
 
 // Let every copy issued into a ring land before the CTA's shared memory goes away.
 __device__ __forceinline__ void ring_drain(uint64_t* full, uint32_t issued, int n, uint64_t timeout_ns) {
@@ -373,55 +378,55 @@ __device__ void dq_mma(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uin
     uint32_t idx = 0, qit = 0, sf = 0, dpf = 0;
     bool ok = true;
     for (uint32_t n_it = 0; ok; ++n_it) {
-        const int item = take_item(b.item_full, b.item_empty, ring, n_it, true, wc);
+        const int item = take_item(b.item_full, b.item_empty, ring, n_it, (threadIdx.x & 31) == 0, wc);
         if (item == -2) { ok = false; break; }
         if (item < 0) break;
         int hq, qp;
         dq_item(p, item, hq, qp);
         const int nj = count_key_tiles(R, qp);
         const uint32_t i0 = idx;
-        if (!mbar_wait(b.res_full, qit & 1u, wc)) { ok = false; break; }
+        if (!mbar_wait_w(b.res_full, qit & 1u, wc)) { ok = false; break; }
         // S(0), dP(0)
-        if (!ring_wait(b.a_full, i0, C::kSlotsA, wc)) { ok = false; break; }
+        if (!ring_wait_w(b.a_full, i0, C::kSlotsA, wc)) { ok = false; break; }
         tc_fence_after();
         issue_kk<D>(tmem, sQ, sA + (i0 % C::kSlotsA) * C::kTileBytes);
-        mma_commit(b.s_full);
-        mma_commit(&b.a_empty[i0 % C::kSlotsA]);  // this issuer is done with K(0)
-        if (!ring_wait(b.b_full, i0, C::kSlotsB, wc)) { ok = false; break; }
+        mma_commit_e(b.s_full);
+        mma_commit_e(&b.a_empty[i0 % C::kSlotsA]);  // this issuer is done with K(0)
+        if (!ring_wait_w(b.b_full, i0, C::kSlotsB, wc)) { ok = false; break; }
         tc_fence_after();
         issue_kk<D>(tmem + kTile, sdO, sB + (i0 % C::kSlotsB) * C::kTileBytes);
-        mma_commit(b.dp_full);
-        mma_commit(&b.b_empty[i0 % C::kSlotsB]);  // V(0) is done once dP(0) is
+        mma_commit_e(b.dp_full);
+        mma_commit_e(&b.b_empty[i0 % C::kSlotsB]);  // V(0) is done once dP(0) is
         for (int j = 0; j + 1 < nj && ok; ++j) {
             const uint32_t i = i0 + j;
             // the next S as soon as this tile's S is out of TMEM, likewise dP
-            if (!mbar_wait(b.s_free, sf & 1u, wc)) { ok = false; break; }
+            if (!mbar_wait_w(b.s_free, sf & 1u, wc)) { ok = false; break; }
             ++sf;
-            if (!ring_wait(b.a_full, i + 1, C::kSlotsA, wc)) { ok = false; break; }
+            if (!ring_wait_w(b.a_full, i + 1, C::kSlotsA, wc)) { ok = false; break; }
             tc_fence_after();
             issue_kk<D>(tmem, sQ, sA + ((i + 1) % C::kSlotsA) * C::kTileBytes);
-            mma_commit(b.s_full);
-            mma_commit(&b.a_empty[(i + 1) % C::kSlotsA]);
-            if (!mbar_wait(b.dp_free, dpf & 1u, wc)) { ok = false; break; }
+            mma_commit_e(b.s_full);
+            mma_commit_e(&b.a_empty[(i + 1) % C::kSlotsA]);
+            if (!mbar_wait_w(b.dp_free, dpf & 1u, wc)) { ok = false; break; }
             ++dpf;
-            if (!ring_wait(b.b_full, i + 1, C::kSlotsB, wc)) { ok = false; break; }
+            if (!ring_wait_w(b.b_full, i + 1, C::kSlotsB, wc)) { ok = false; break; }
             tc_fence_after();
             issue_kk<D>(tmem + kTile, sdO, sB + ((i + 1) % C::kSlotsB) * C::kTileBytes);
-            mma_commit(b.dp_full);
-            mma_commit(&b.b_empty[(i + 1) % C::kSlotsB]);
+            mma_commit_e(b.dp_full);
+            mma_commit_e(&b.b_empty[(i + 1) % C::kSlotsB]);
         }
         if (!ok) break;
         // the last tile's S and dP still have to be copied out before the next item's
-        if (!mbar_wait(b.s_free, sf & 1u, wc) || !mbar_wait(b.dp_free, dpf & 1u, wc)) { ok = false; break; }
+        if (!mbar_wait_w(b.s_free, sf & 1u, wc) || !mbar_wait_w(b.dp_free, dpf & 1u, wc)) { ok = false; break; }
         ++sf;
         ++dpf;
         idx = i0 + nj;
-        mma_commit(b.res_empty);  // Q and dO of this item are done with
+        mma_commit_e(b.res_empty);  // Q and dO of this item are done with
         ++qit;
     }
     if (!ok) {
         // every MMA issued so far must finish before TMEM is released
-        mma_commit(b.drain);
+        mma_commit_e(b.drain);
         drain_wait(b.drain, 0, wc.timeout_ns);
     }
 }
@@ -436,7 +441,7 @@ __device__ void dq_mma2(const AttnBwdParams& p, uint8_t* smem, const Bars& b, ui
     uint32_t idx = 0, it = 0, dsit[2] = {0, 0};
     bool ok = true;
     for (uint32_t n_it = 0; ok; ++n_it) {
-        const int item = take_item(b.item_full, b.item_empty, ring, n_it, true, wc);
+        const int item = take_item(b.item_full, b.item_empty, ring, n_it, (threadIdx.x & 31) == 0, wc);
         if (item == -2) { ok = false; break; }
         if (item < 0) break;
         int hq, qp;
@@ -445,25 +450,25 @@ __device__ void dq_mma2(const AttnBwdParams& p, uint8_t* smem, const Bars& b, ui
         for (int j = 0; j < nj && ok; ++j) {
             const uint32_t i = idx + j;
             const int bb = j & 1;
-            if (!mbar_wait(&b.ds_full[bb], dsit[bb] & 1u, wc)) { ok = false; break; }
+            if (!mbar_wait_w(&b.ds_full[bb], dsit[bb] & 1u, wc)) { ok = false; break; }
             ++dsit[bb];
-            if (j == 0 && !mbar_wait(b.acc_free, (it & 1u) ^ 1u, wc)) { ok = false; break; }
+            if (j == 0 && !mbar_wait_w(b.acc_free, (it & 1u) ^ 1u, wc)) { ok = false; break; }
             // K(j) landed before the S(j) that led to this dS; its slot cannot have been
             // refilled, since this issuer has not released it yet
-            if (!ring_wait(b.a_full, i, C::kSlotsA, wc)) { ok = false; break; }
+            if (!ring_wait_w(b.a_full, i, C::kSlotsA, wc)) { ok = false; break; }
             tc_fence_after();
             // dQ += dS K, dS from TMEM buffer j % 2, K from its ring slot as an MN-major B
             issue_tm<D>(tmem + kAccCol, tmem + 384 + 64 * bb, 32, sA + (i % C::kSlotsA) * C::kTileBytes, j > 0);
-            mma_commit(&b.a_empty[i % C::kSlotsA]);
-            mma_commit(&b.ds_free[bb]);
+            mma_commit_e(&b.a_empty[i % C::kSlotsA]);
+            mma_commit_e(&b.ds_free[bb]);
         }
         if (!ok) break;
         idx += nj;
-        mma_commit(b.acc_done);
+        mma_commit_e(b.acc_done);
         ++it;
     }
     if (!ok) {
-        mma_commit(b.drain2);
+        mma_commit_e(b.drain2);
         drain_wait(b.drain2, 0, wc.timeout_ns);
     }
 }
@@ -592,61 +597,61 @@ __device__ void kv_mma(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uin
     uint32_t idx = 0, kit = 0, sf = 0, pf = 0;
     bool ok = true;
     for (uint32_t n_it = 0; ok; ++n_it) {
-        const int item = take_item(b.item_full, b.item_empty, ring, n_it, true, wc);
+        const int item = take_item(b.item_full, b.item_empty, ring, n_it, (threadIdx.x & 31) == 0, wc);
         if (item == -2) { ok = false; break; }
         if (item < 0) break;
         int hk, kp;
         kv_item(p, item, hk, kp);
         const int n = count_query_tiles(R, hk, kp);
         const uint32_t i0 = idx;
-        if (!mbar_wait(b.res_full, kit & 1u, wc)) { ok = false; break; }
+        if (!mbar_wait_w(b.res_full, kit & 1u, wc)) { ok = false; break; }
         // S^T(0) = K Q(0)^T, dP^T(0) = V dO(0)^T
-        if (!ring_wait(b.a_full, i0, C::kSlotsA, wc)) { ok = false; break; }
+        if (!ring_wait_w(b.a_full, i0, C::kSlotsA, wc)) { ok = false; break; }
         tc_fence_after();
         issue_kk<D>(tmem, sK, sA + (i0 % C::kSlotsA) * C::kTileBytes);
-        mma_commit(b.s_full);
-        if (!ring_wait(b.b_full, i0, C::kSlotsB, wc)) { ok = false; break; }
+        mma_commit_e(b.s_full);
+        if (!ring_wait_w(b.b_full, i0, C::kSlotsB, wc)) { ok = false; break; }
         tc_fence_after();
         issue_kk<D>(tmem + kTile, sV, sB + (i0 % C::kSlotsB) * C::kTileBytes);
-        mma_commit(b.dp_full);
+        mma_commit_e(b.dp_full);
         for (int t = 0; t < n && ok; ++t) {
             const uint32_t i = i0 + t;
             const bool more = t + 1 < n;
             // the next S^T as soon as this tile's S^T is out of TMEM
-            if (!mbar_wait(b.s_free, sf & 1u, wc)) { ok = false; break; }
+            if (!mbar_wait_w(b.s_free, sf & 1u, wc)) { ok = false; break; }
             ++sf;
             if (more) {
-                if (!ring_wait(b.a_full, i + 1, C::kSlotsA, wc)) { ok = false; break; }
+                if (!ring_wait_w(b.a_full, i + 1, C::kSlotsA, wc)) { ok = false; break; }
                 tc_fence_after();
                 issue_kk<D>(tmem, sK, sA + ((i + 1) % C::kSlotsA) * C::kTileBytes);
-                mma_commit(b.s_full);
+                mma_commit_e(b.s_full);
             }
-            if (!mbar_wait(&b.ds_full[0], pf & 1u, wc)) { ok = false; break; }
+            if (!mbar_wait_w(&b.ds_full[0], pf & 1u, wc)) { ok = false; break; }
             ++pf;
-            if (t == 0 && !mbar_wait(b.acc_free, (kit & 1u) ^ 1u, wc)) { ok = false; break; }
+            if (t == 0 && !mbar_wait_w(b.acc_free, (kit & 1u) ^ 1u, wc)) { ok = false; break; }
             tc_fence_after();
             const uint32_t sq = sA + (i % C::kSlotsA) * C::kTileBytes;
             const uint32_t sdo = sB + (i % C::kSlotsB) * C::kTileBytes;
             issue_tm<D>(tmem + kAccCol, tmem + kTile, 64, sdo, t > 0);           // dV += P^T dO
-            mma_commit(&b.b_empty[i % C::kSlotsB]);
+            mma_commit_e(&b.b_empty[i % C::kSlotsB]);
             issue_tm<D>(tmem + kAccCol + D, tmem + kTile + 32, 64, sq, t > 0);   // dK += dS^T Q
-            mma_commit(&b.a_empty[i % C::kSlotsA]);
+            mma_commit_e(&b.a_empty[i % C::kSlotsA]);
             if (more) {
                 // dP^T(t+1) overwrites the P^T, dS^T columns the two products above read
-                if (!ring_wait(b.b_full, i + 1, C::kSlotsB, wc)) { ok = false; break; }
+                if (!ring_wait_w(b.b_full, i + 1, C::kSlotsB, wc)) { ok = false; break; }
                 tc_fence_after();
                 issue_kk<D>(tmem + kTile, sV, sB + ((i + 1) % C::kSlotsB) * C::kTileBytes);
-                mma_commit(b.dp_full);
+                mma_commit_e(b.dp_full);
             }
         }
         if (!ok) break;
         idx = i0 + n;
-        mma_commit(b.res_empty);
-        mma_commit(b.acc_done);
+        mma_commit_e(b.res_empty);
+        mma_commit_e(b.acc_done);
         ++kit;
     }
     if (!ok) {
-        mma_commit(b.drain);
+        mma_commit_e(b.drain);
         drain_wait(b.drain, 0, wc.timeout_ns);
     }
 }
@@ -794,18 +799,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < 8) {
         if constexpr (DQ) dq_compute<D>(p, b, tmem, ring, wc);
         else kv_compute<D>(p, b, tmem, reinterpret_cast<float*>(smem + C::kLdOff) + (warp / 4) * 128, ring, wc);
-    } else if (warp == kMmaWarp) {
-        if (lane == 0) {
-            if constexpr (DQ) dq_mma<D>(p, smem, b, tmem, ring, wc);
-            else kv_mma<D>(p, smem, b, tmem, ring, wc);
-        }
+    } else if (warp == kMmaWarp) {  // the whole warp: see mma_ss_e
+        if constexpr (DQ) dq_mma<D>(p, smem, b, tmem, ring, wc);
+        else kv_mma<D>(p, smem, b, tmem, ring, wc);
     } else if (warp == kLoadWarp) {
         if (lane == 0) {
             if constexpr (DQ) dq_load<D>(p, &tq, &tdo, &tk, &tv, smem, b, ring, wc);
             else kv_load<D>(p, &tq, &tdo, &tk, &tv, smem, b, ring, wc);
         }
     } else if (warp == kMma2Warp) {
-        if (lane == 0) {
+        if (lane == 0 || DQ) {
             if constexpr (DQ) {
                 dq_mma2<D>(p, smem, b, tmem, ring, wc);
             } else {  // no second issuer in the dk/dv kernel: take the items only
