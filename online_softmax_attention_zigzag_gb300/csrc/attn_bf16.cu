@@ -399,7 +399,8 @@ __device__ __forceinline__ bool wait_turn(volatile uint32_t* turn, uint32_t mine
     }
 }
 
-// One issuer thread per unit x.  The two issuers take turns batch by batch (a batch is
+// One issuer warp per unit x (run by the whole warp; tcgen05 instructions from one elected
+// lane, which tcgen05.commit tracks).  The two issuers take turns batch by batch (a batch is
 // the MMAs one unit issues between two softmax hand-offs), so the tensor pipe sees the
 // units' batches whole and in the order of the single-issuer schedule, while each
 // issuer's waits and commits overlap the other's batch.  `turn` counts the batches
@@ -474,7 +475,7 @@ __device__ void mma_role(const AttnBf16Params& p, int x, uint8_t* sQ, uint8_t* s
         ++qit;
     }
     if (!ok) {
-        // every MMA this thread issued must finish before TMEM is released
+        // every MMA this warp issued must finish before TMEM is released
         mma_commit_e(&b.drain[x]);
         drain_wait(&b.drain[x], 0, wc.timeout_ns);
     }
