@@ -71,7 +71,7 @@ struct Cfg {
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = 2 * kTileBytes;
     static constexpr int kBarOff = kKVOff + kStages * kStageBytes;
-    static constexpr int kNumBars = 14 + 2 * kStages + 2 * kItemRing;
+    static constexpr int kNumBars = 16 + 2 * kStages + 2 * kItemRing;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kRingOff = kMiscOff + 16;  // item ids handed from the loader to the other roles
     static constexpr int kSmemBytes = kRingOff + 4 * kItemRing + 1024;  // + slack to align the base
@@ -83,7 +83,8 @@ struct Bars {
     uint64_t* q_full;    // [2] loader -> mma (TMA bytes)
     uint64_t* q_empty;   // [2] mma -> loader (last S MMA of an item done)
     uint64_t* s_full;    // [2] mma -> softmax
-    uint64_t* p_full;    // [2] softmax (128 threads) -> mma
+    uint64_t* p_full;    // [2] softmax (128 threads) -> mma: all of P written
+    uint64_t* p_half;    // [2] softmax (128 threads) -> mma: P of keys [0, 64) written (and O rescaled)
     uint64_t* o_done;    // [2] mma -> softmax (last PV of an item done)
     uint64_t* o_free;    // [2] softmax (128 threads) -> mma (O read out)
     uint64_t* drain;     // [1] mma, on abort only
@@ -383,6 +384,26 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, int x, uint32_t v_base, 
     }
 }
 
+template <int D, int K0, int K1>
+__device__ __forceinline__ void issue_pv_part(uint32_t tmem, int x, uint32_t v_base, bool accumulate) {
+    using C = Cfg<D>;
+    constexpr uint32_t idesc = idesc_bf16(kTile, D, 1);
+    const uint32_t d_tmem = tmem + C::kOCol + x * D;
+    const uint32_t a_tmem = tmem + x * kTile + 64;
+    const uint32_t vlo = sdesc_lo(v_base, C::kBoxBytes);
+    const uint32_t acc = accumulate ? 1u : 0u;
+#pragma unroll
+    for (int kk = K0; kk < K1; ++kk) {
+        asm volatile(
+            "{\n\t.reg .b64 db;\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "mov.b64 db, {%2, %5};\n\telect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
+            "r"(a_tmem + kk * 8), "r"(vlo + ((kk * 16 * 128) >> 4)), "r"(idesc), "r"(kk > 0 ? 1u : acc),
+            "r"(kSdescHi)
+            : "memory");
+    }
+}
+
 // Wait until `turn` reaches `mine` (bounded: gives up on abort or after the timeout).
 __device__ __forceinline__ bool wait_turn(volatile uint32_t* turn, uint32_t mine, const WaitCtl& wc) {
     if (*turn == mine) return true;
@@ -454,13 +475,22 @@ __device__ void mma_role(const AttnBf16Params& p, int x, uint8_t* sQ, uint8_t* s
         for (int j = 0; j < nj && ok; ++j) {
             // this stage holds V(j) and, unless j is the last tile, K(j+1)
             if (!wait_stage(s, base)) { ok = false; break; }
-            if (!mbar_wait_w(&b.p_full[x], pit & 1u, wc)) { ok = false; break; }
-            ++pit;
+            // Under the document mask items are short, and P of the tile's first 64 keys
+            // goes into O while the softmax finishes the rest; in the ring, all of P at once.
+            if (!mbar_wait_w(DOC ? &b.p_half[x] : &b.p_full[x], pit & 1u, wc)) { ok = false; break; }
             if (j == 0 && !mbar_wait_w(&b.o_free[x], (qit & 1u) ^ 1u, wc)) { ok = false; break; }
             const uint32_t mine = seq + nx * (j + 1) + x;
             if (!__all_sync(0xffffffffu, wait_turn(turn, mine, wc))) { ok = false; break; }
             tc_fence_after();
-            issue_pv<D>(tmem, x, base, j > 0);
+            if constexpr (DOC) {
+                issue_pv_part<D, 0, kTile / 32>(tmem, x, base, j > 0);
+                if (!mbar_wait_w(&b.p_full[x], pit & 1u, wc)) { ok = false; break; }
+                tc_fence_after();
+                issue_pv_part<D, kTile / 32, kTile / 16>(tmem, x, base, true);
+            } else {
+                issue_pv<D>(tmem, x, base, j > 0);
+            }
+            ++pit;
             if (j + 1 < nj) {
                 issue_s<D>(tmem, x, sQa, base + C::kTileBytes);
                 mma_commit_e(&b.s_full[x]);
@@ -599,18 +629,38 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
                 }
                 // every score is in registers: P may overwrite S's upper half
                 tmem_st32(p_tmem + hh * 32, pk);
+                if (DOC && hh == 0) {  // hand the first 64 keys' P (and a rescaled O) over at once
+                    // O is stable here: the commit that signalled this S also covered the
+                    // previous P V, and this tile's P V waits for this arrival.
+                    if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+                        for (int cc = 0; cc < D; cc += 32) {
+                            uint32_t o0[32];
+                            tmem_ld32(o_tmem + cc, o0);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o0[i] = __float_as_uint(__uint_as_float(o0[i]) * f);
+                            tmem_st32(o_tmem + cc, o0);
+                        }
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&b.p_half[x]);
+                }
             }
-            // O is stable here: the commit that signalled this S also covered the
-            // previous P V, and the next P V waits for this tile's arrivals.
-            if (__any_sync(0xffffffffu, need)) {
+            if constexpr (!DOC) {
+                // O is stable here: the commit that signalled this S also covered the
+                // previous P V, and the next P V waits for this tile's arrivals.
+                if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-                for (int cc = 0; cc < D; cc += 32) {
-                    uint32_t o0[32];
-                    tmem_ld32(o_tmem + cc, o0);
-                    tmem_wait_ld();
+                    for (int cc = 0; cc < D; cc += 32) {
+                        uint32_t o0[32];
+                        tmem_ld32(o_tmem + cc, o0);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o0[i] = __float_as_uint(__uint_as_float(o0[i]) * f);
-                    tmem_st32(o_tmem + cc, o0);
+                        for (int i = 0; i < 32; ++i) o0[i] = __float_as_uint(__uint_as_float(o0[i]) * f);
+                        tmem_st32(o_tmem + cc, o0);
+                    }
                 }
             }
             l += (se[0] + se[1]) + (se[2] + se[3]);
@@ -682,6 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     b.kv_empty = bars + 14 + C::kStages;
     b.item_full = bars + 14 + 2 * C::kStages;
     b.item_empty = bars + 14 + 2 * C::kStages + kItemRing;
+    b.p_half = bars + 14 + 2 * C::kStages + 2 * kItemRing;
     volatile int* ring = reinterpret_cast<volatile int*>(smem + C::kRingOff);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
@@ -694,6 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&b.q_empty[x], 1);
             mbar_init(&b.s_full[x], 1);
             mbar_init(&b.p_full[x], 128);
+            mbar_init(&b.p_half[x], 128);
             mbar_init(&b.o_done[x], 1);
             mbar_init(&b.o_free[x], 128);
         }
