@@ -162,3 +162,52 @@ def dq_rows(q, k, v, dout, heads, positions, causal: bool, with_abs: bool = Fals
             res[n] = dS @ kh[:n_keys]
             res_abs[n] = np.abs(dS) @ np.abs(kh[:n_keys])
     return (res, res_abs) if with_abs else res
+
+
+def dkv_rows(q, k, v, dout, kv_heads, positions, causal: bool, with_abs: bool = False, batch_rows: int = 512):
+    """dk and dv at selected (KV head, natural key position) rows only.
+
+    A key's gradients add up over every query row that sees it (rows i >= j when
+    causal) in every query head of its group: dk_j = sum_i dS_ij q_i and
+    dv_j = sum_i P_ij dout_i.  Each such row needs its own lse and D (its whole row of
+    scores), so the cost is set by the earliest selected key: keys near the end of a
+    causal sequence are cheap.  with_abs: also return the sums of absolute terms
+    sum_i |dS_ij| |q_i| and sum_i P_ij |dout_i| (as grad_abs_sums)."""
+    kv_heads = np.asarray(kv_heads, dtype=np.int64)
+    positions = np.asarray(positions, dtype=np.int64)
+    Hq, S, d = q.shape
+    Hkv = k.shape[0]
+    g = Hq // Hkv
+    dk = np.zeros((len(kv_heads), d))
+    dv = np.zeros((len(kv_heads), d))
+    ak = np.zeros((len(kv_heads), d))
+    av = np.zeros((len(kv_heads), d))
+    for hk in np.unique(kv_heads):
+        sel = np.nonzero(kv_heads == hk)[0]
+        J = positions[sel]
+        kh, vh = _f64(k[int(hk)]), _f64(v[int(hk)])
+        i0 = int(J.min()) if causal else 0
+        rows = np.arange(i0, S)                       # every row that sees a selected key
+        for h in range(int(hk) * g, (int(hk) + 1) * g):
+            qh, doh = _f64(q[h]), _f64(dout[h])
+            for b0 in range(0, len(rows), batch_rows):
+                I = rows[b0:b0 + batch_rows]
+                n_keys = int(I.max()) + 1 if causal else S
+                s = qh[I] @ kh[:n_keys].T              # the rows' whole score rows
+                if causal:
+                    s = np.where(np.arange(n_keys)[None, :] > I[:, None], -np.inf, s)
+                M = s.max(axis=1, keepdims=True)
+                e = np.exp(s - M)
+                L = e.sum(axis=1, keepdims=True)
+                lse = (M + np.log(L))[:, 0]
+                D = np.einsum("id,id->i", doh[I], (e @ vh[:n_keys]) / L)
+                sj = qh[I] @ kh[J].T                   # [rows, selected keys]
+                if causal:
+                    sj = np.where(J[None, :] > I[:, None], -np.inf, sj)
+                P = np.exp(sj - lse[:, None])
+                dS = P * (doh[I] @ vh[J].T - D[:, None])
+                dk[sel] += dS.T @ qh[I]
+                dv[sel] += P.T @ doh[I]
+                ak[sel] += np.abs(dS).T @ np.abs(qh[I])
+                av[sel] += P.T @ np.abs(doh[I])
+    return (dk, dv, ak, av) if with_abs else (dk, dv)

@@ -3,21 +3,26 @@
 Follows "Ring Attention and Ulysses shard a sequence two different ways..."
 (section "Ring Attention: point-to-point rotation, and an online softmax that
 never sees the whole row at once"): each rank keeps its queries fixed and
-works through the KV blocks as they arrive, one online update per block:
+works through the KV blocks as they arrive.  What a rank carries between
+blocks, per query row, is a reference maximum ``m``, the sum ``l`` of the
+exponentials of the scores seen so far taken against ``m``, and the matching
+weighted sum ``acc`` of value rows.  One arriving block is absorbed in the
+order the page's update rule gives:
 
-    block_max   = row max of the block's scores
-    new_max     = max(running_max, block_max)
-    correction  = exp(running_max - new_max)
-    p           = exp(scores - new_max)
-    running_sum = running_sum * correction + row sum of p
-    output      = output * correction + p @ V_block
-    running_max = new_max
+1. the block's largest score per row;
+2. the new reference: the larger of that and the old one;
+3. the factor that moves everything accumulated so far onto the new
+   reference, e raised to (old reference - new reference);
+4. the block's exponentials against the new reference;
+5. ``l`` and ``acc`` rescaled by that factor, the block's exponentials (and
+   their product with the block's values) added;
+6. the new reference kept.
 
-and divides by the running sum at the end.  The ring order is taken from
-"Interrogating parallelism, part 5" (section "How does attention survive being
-split?"): rank i sends its KV block to rank i+1, so at hop h rank r holds the
-block that rank (r - h) mod c started with; after c-1 hops every query block
-has seen every KV block.
+At the end out = acc / l and the log-sum-exp is m + ln l.  The ring order is
+taken from "Interrogating parallelism, part 5" (section "How does attention
+survive being split?"): rank i sends its KV block to rank i+1, so at hop h
+rank r holds the block that rank (r - h) mod c started with; after c-1 hops
+every query block has seen every KV block.
 
 Readings where the pages are silent:
 
@@ -27,8 +32,8 @@ Readings where the pages are silent:
 * Causal masking uses natural positions (key j is visible to query i when
   j <= i).  A row whose keys in a block are all masked takes no update from
   that block (the printed rule would form exp(-inf - (-inf)) there).
-* The log-sum-exp of a row is running_max + ln(running_sum); a row that saw no
-  key at all has output 0 and log-sum-exp -inf.
+* The log-sum-exp of a row is m + ln(l); a row that saw no key at all has
+  output 0 and log-sum-exp -inf.
 """
 from __future__ import annotations
 
@@ -37,33 +42,52 @@ import numpy as np
 from .layout import rank_positions
 
 
+class _RowState:
+    """Per-row online-softmax state of one rank's queries: reference maximum m,
+    exponential sum l and weighted value sum acc, all relative to m."""
+
+    def __init__(self, n_rows: int, d_v: int):
+        self.m = np.full(n_rows, -np.inf)
+        self.l = np.zeros(n_rows)
+        self.acc = np.zeros((n_rows, d_v))
+
+    def absorb(self, scores: np.ndarray, values: np.ndarray) -> None:
+        """Fold one block in: ``scores`` [rows, keys] (-inf where masked),
+        ``values`` [keys, d_v]."""
+        top = scores.max(axis=1)                                 # step 1
+        ref = np.maximum(self.m, top)                            # step 2
+        live = ref > -np.inf        # rows that have met a visible key by now
+        safe_ref = np.where(live, ref, 0.0)
+        with np.errstate(invalid="ignore"):
+            # step 3; a row that had seen nothing yet has l = acc = 0, and any
+            # finite factor leaves that as it is
+            alpha = np.where(live & (self.m > -np.inf), np.exp(self.m - safe_ref), 0.0)
+        w = np.exp(scores - safe_ref[:, None])                   # step 4 (masked: 0)
+        w[~live] = 0.0
+        self.l = alpha * self.l + w.sum(axis=1)                  # step 5
+        self.acc = alpha[:, None] * self.acc + w @ values
+        self.m = ref                                             # step 6
+
+    def finish(self):
+        """(out, lse) of every row; out = 0 and lse = -inf for a row that saw no key."""
+        have = self.l > 0
+        den = np.where(have, self.l, 1.0)
+        out = np.where(have[:, None], self.acc / den[:, None], 0.0)
+        lse = np.where(have, np.where(have, self.m, 0.0) + np.log(den), -np.inf)
+        return out, lse
+
+
 def ring_rank(q_rows, q_pos, k, v, kv_blocks_pos, causal: bool):
     """One rank: queries ``q_rows`` at natural positions ``q_pos`` visit the
     key/value rows at the natural positions listed in ``kv_blocks_pos``, one
     online update per list entry, in list order."""
-    n, _ = q_rows.shape
-    dv = v.shape[1]
-    running_max = np.full(n, -np.inf)
-    running_sum = np.zeros(n)
-    output = np.zeros((n, dv))
-    with np.errstate(invalid="ignore", over="ignore"):
-        for pos_k in kv_blocks_pos:
-            scores = q_rows @ k[pos_k].T
-            if causal:
-                scores = np.where(pos_k[None, :] > q_pos[:, None], -np.inf, scores)
-            block_max = scores.max(axis=1)
-            new_max = np.maximum(running_max, block_max)
-            seen = np.isfinite(new_max)          # rows with at least one visible key so far
-            correction = np.where(seen, np.exp(running_max - new_max), 1.0)
-            p = np.where(seen[:, None], np.exp(scores - new_max[:, None]), 0.0)
-            running_sum = running_sum * correction + p.sum(axis=1)
-            output = output * correction[:, None] + p @ v[pos_k]
-            running_max = new_max
-    seen = running_sum > 0
-    out = np.where(seen[:, None], output / np.where(seen, running_sum, 1.0)[:, None], 0.0)
-    with np.errstate(divide="ignore"):
-        lse = np.where(seen, running_max + np.log(np.where(seen, running_sum, 1.0)), -np.inf)
-    return out, lse
+    state = _RowState(q_rows.shape[0], v.shape[1])
+    for keys in kv_blocks_pos:
+        blk = q_rows @ k[keys].T
+        if causal:
+            blk = np.where(keys[None, :] <= q_pos[:, None], blk, -np.inf)
+        state.absorb(blk, v[keys])
+    return state.finish()
 
 
 def ring_schedule(S: int, c: int, layout: int, r: int, kv_block: int, hops=None):

@@ -487,3 +487,67 @@ def pin_ring_backward(ring_grad_fn, grad_fn):
         do = rand((Hq, S, d), seed + 3)
         for a, b in zip(ring_grad_fn(q, k, v, do, c, lay, causal, kvb), grad_fn(q, k, v, do, causal)):
             assert np.abs(a - b).max() < 1e-12, "ring backward differs from the full gradient"
+
+
+def brute_abs_sums(q, k, v, dout, causal):
+    """Pure-Python loops (math.exp only) over every term of every gradient entry:
+    sum_j |dS_ij| |k_jt| for dq, sum_i |dS_ij| |q_it| for dk (summed over the query heads
+    of a KV head), sum_i P_ij |dout_it| for dv; tiny inputs."""
+    Hq, S, d = len(q), len(q[0]), len(q[0][0])
+    Hkv = len(k)
+    g = Hq // Hkv
+    aq = [[[0.0] * d for _ in range(S)] for _ in range(Hq)]
+    ak = [[[0.0] * d for _ in range(S)] for _ in range(Hkv)]
+    av = [[[0.0] * d for _ in range(S)] for _ in range(Hkv)]
+    for h in range(Hq):
+        hk = h // g
+        for i in range(S):
+            keys = [j for j in range(S) if (not causal or j <= i)]
+            sc = {j: sum(float(q[h][i][t]) * float(k[hk][j][t]) for t in range(d)) for j in keys}
+            M = max(sc.values())
+            L = sum(math.exp(s - M) for s in sc.values())
+            P = {j: math.exp(sc[j] - M) / L for j in keys}
+            out = [sum(P[j] * float(v[hk][j][t]) for j in keys) for t in range(d)]
+            D = sum(float(dout[h][i][t]) * out[t] for t in range(d))
+            for j in keys:
+                dP = sum(float(dout[h][i][t]) * float(v[hk][j][t]) for t in range(d))
+                dS = P[j] * (dP - D)
+                for t in range(d):
+                    aq[h][i][t] += abs(dS) * abs(float(k[hk][j][t]))
+                    ak[hk][j][t] += abs(dS) * abs(float(q[h][i][t]))
+                    av[hk][j][t] += P[j] * abs(float(dout[h][i][t]))
+    return np.array(aq), np.array(ak), np.array(av)
+
+
+def pin_abs_sums(abs_fn, grad_fn):
+    """The sums of absolute terms that scale the backward tolerance: against the
+    pure-Python brute force, and exactly equal to |dv| when every dout entry is positive
+    (then every term of dv_j = sum_i P_ij dout_i is positive)."""
+    for causal in (False, True):
+        for (Hq, Hkv, S, d, seed) in ((2, 1, 6, 3, 61), (4, 2, 5, 2, 62)):
+            q, k, v = rand((Hq, S, d), seed), rand((Hkv, S, d), seed + 1), rand((Hkv, S, d), seed + 2)
+            do = rand((Hq, S, d), seed + 3)
+            got = abs_fn(q, k, v, do, causal)
+            want = brute_abs_sums(q, k, v, do, causal)
+            for name, a, b in zip(("dq", "dk", "dv"), got, want):
+                assert np.abs(a - b).max() < 1e-12, f"abs sums of {name} differ from brute force"
+            do_pos = np.abs(do) + 0.1
+            _, _, av = abs_fn(q, k, v, do_pos, causal)
+            _, _, dv = grad_fn(q, k, v, do_pos, causal)
+            assert np.abs(av - dv).max() < 1e-12, "with dout > 0 the dv abs sums must equal dv"
+
+
+def pin_kv_rows(rows_fn, grad_fn, abs_fn):
+    """dk, dv (and their abs sums) at selected key rows equal the whole gradient's rows."""
+    for causal in (False, True):
+        for (Hq, Hkv, S, d, seed) in ((4, 2, 33, 5, 71), (3, 1, 20, 4, 72)):
+            q, k, v = rand((Hq, S, d), seed), rand((Hkv, S, d), seed + 1), rand((Hkv, S, d), seed + 2)
+            do = rand((Hq, S, d), seed + 3)
+            _, dk, dv = grad_fn(q, k, v, do, causal)
+            _, ak, av = abs_fn(q, k, v, do, causal)
+            rng = np.random.default_rng(seed)
+            hk = rng.integers(0, Hkv, 9)
+            pos = np.concatenate([[0, S - 1], rng.integers(0, S, 7)])
+            r_dk, r_dv, r_ak, r_av = rows_fn(q, k, v, do, hk, pos, causal, with_abs=True, batch_rows=4)
+            for name, a, b in (("dk", r_dk, dk), ("dv", r_dv, dv), ("|dk|", r_ak, ak), ("|dv|", r_av, av)):
+                assert np.abs(a - b[hk, pos]).max() < 1e-12, f"{name} rows differ from the whole gradient"

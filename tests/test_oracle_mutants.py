@@ -62,22 +62,27 @@ def test_unmutated_copy_passes():
 # ---------------------------------------------------------------- ring mutants
 
 def _ring_rank(q_rows, q_pos, k, v, blocks, causal, *, no_out_corr=False, no_sum_corr=False, flip=False):
+    """The oracle's per-rank accumulator (reference max, exponential sum, weighted
+    values), with one of its rescaling steps planted wrong."""
     n = q_rows.shape[0]
-    m = np.full(n, -np.inf); l = np.zeros(n); o = np.zeros((n, v.shape[1]))
-    with np.errstate(invalid="ignore", over="ignore"):
-        for pk in blocks:
-            s = q_rows @ k[pk].T
-            if causal:
-                s = np.where(pk[None, :] > q_pos[:, None], -np.inf, s)
-            nm = np.maximum(m, s.max(1))
-            seen = np.isfinite(nm)
-            corr = np.where(seen, np.exp((nm - m) if flip else (m - nm)), 1.0)
-            corr = np.where(np.isfinite(corr), corr, 0.0)
-            p = np.where(seen[:, None], np.exp(s - nm[:, None]), 0.0)
-            l = (l if no_sum_corr else l * corr) + p.sum(1)
-            o = (o if no_out_corr else o * corr[:, None]) + p @ v[pk]
-            m = nm
-    return o / l[:, None], m + np.log(l)
+    ref = np.full(n, -np.inf); tot = np.zeros(n); wsum = np.zeros((n, v.shape[1]))
+    for keys in blocks:
+        blk = q_rows @ k[keys].T
+        if causal:
+            blk = np.where(keys[None, :] <= q_pos[:, None], blk, -np.inf)
+        nxt = np.maximum(ref, blk.max(axis=1))
+        live = nxt > -np.inf
+        base = np.where(live, nxt, 0.0)
+        with np.errstate(invalid="ignore", over="ignore"):
+            step = (base - ref) if flip else (ref - base)
+            alpha = np.where(live & (ref > -np.inf), np.exp(step), 0.0)
+        w = np.exp(blk - base[:, None])
+        w[~live] = 0.0
+        tot = (tot if no_sum_corr else alpha * tot) + w.sum(axis=1)
+        wsum = (wsum if no_out_corr else alpha[:, None] * wsum) + w @ v[keys]
+        ref = nxt
+    with np.errstate(divide="ignore", invalid="ignore"):
+        return wsum / tot[:, None], ref + np.log(tot)
 
 
 def _ring(q, k, v, c, lay, causal, kvb, **kw):
@@ -310,3 +315,44 @@ def test_grad_unmutated_copy_passes():
     fn = lambda q, k, v, do, causal: _grad(q, k, v, do, causal)  # noqa: E731
     pins.pin_grad_vs_autograd(fn)
     pins.pin_grad_closed_forms(fn)
+
+
+# ---------------------------------------------------------------- abs-sum mutants (backward tolerance scale)
+
+def _abs_sums(q, k, v, dout, causal, *, inflate=1.0, p_for_ds=False, signed_k=False, ak_uses_p=False):
+    from oracle import backward as ob
+    q, k, v, dout = (np.asarray(x, float) for x in (q, k, v, dout))
+    Hq, S, d = q.shape
+    g = Hq // k.shape[0]
+    aq = np.zeros_like(q); ak = np.zeros_like(k); av = np.zeros_like(v)
+    for h in range(Hq):
+        hk = h // g
+        P, _ = ob._probs(q[h], k[hk], causal)
+        D = np.einsum("sd,sd->s", dout[h], P @ v[hk])[:, None]
+        adS = np.abs(P * (dout[h] @ v[hk].T - D))
+        aq[h] = (P if p_for_ds else adS) @ (k[hk] if signed_k else np.abs(k[hk]))
+        ak[hk] += (P if ak_uses_p else adS).T @ np.abs(q[h])
+        av[hk] += P.T @ np.abs(dout[h])
+    return aq * inflate, ak * inflate, av * inflate
+
+
+ABS_MUTANTS = {
+    "inflated_by_two": dict(inflate=2.0),
+    "P_in_place_of_dS_for_dq": dict(p_for_ds=True),
+    "k_not_taken_absolute": dict(signed_k=True),
+    "P_in_place_of_dS_for_dk": dict(ak_uses_p=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ABS_MUTANTS))
+def test_abs_sums_mutant_caught(name):
+    from oracle import backward
+    kw = ABS_MUTANTS[name]
+    fn = lambda q, k, v, do, causal: _abs_sums(q, k, v, do, causal, **kw)  # noqa: E731
+    with pytest.raises(AssertionError):
+        pins.pin_abs_sums(fn, backward.attention_grad)
+
+
+def test_abs_sums_unmutated_copy_passes():
+    from oracle import backward
+    pins.pin_abs_sums(lambda q, k, v, do, causal: _abs_sums(q, k, v, do, causal), backward.attention_grad)

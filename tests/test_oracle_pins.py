@@ -155,6 +155,16 @@ def test_backward_abs_sums_bound_the_gradients():
             assert (np.abs(g) <= a + 1e-12).all() and (a >= 0).all()
 
 
+def test_backward_abs_sums_vs_brute_force():
+    from oracle import backward
+    pins.pin_abs_sums(backward.grad_abs_sums, backward.attention_grad)
+
+
+def test_backward_kv_rows_match_whole():
+    from oracle import backward
+    pins.pin_kv_rows(backward.dkv_rows, backward.attention_grad, backward.grad_abs_sums)
+
+
 def test_backward_dq_rows_match_whole():
     from oracle import backward
     rng = np.random.default_rng(9)
