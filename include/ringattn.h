@@ -44,6 +44,10 @@
  *    crosses the ABI and there is no CPU fallback.
  *  - The library allocates no device memory per call; scratch it needs is passed in,
  *    except for ringattn_fwd_docmask_noalloc, which uses a static device array.
+ *  - The first call of any entry point on a device performs the library's one-time
+ *    set-up for that device (its attributes and the device addresses of the library's
+ *    static arrays), with that device current; make that first call before any stream
+ *    capture begins.
  *  - The fused bf16 kernels (ringattn_fwd*, ringattn_bwd*) hand out their work items
  *    from counters in a static device array of 256 slots: a launch takes the next slot
  *    in turn (the backward takes two) and its last block zeroes it again.  Launches in
@@ -151,8 +155,10 @@ int ringattn_fwd_docmask(const void* q, const void* k, const void* v, float* out
  *    contents never matter to a call on its own; but two calls whose work overlaps on the
  *    GPU (different streams, no ordering between them) race on the array and give wrong
  *    results.  Order such calls on one stream or with events.
- *  - The first call on each device looks up the array's device address (once, with that
- *    device current); make that first call before any stream capture begins.
+ *  - The array's device address is looked up in the library's one-time set-up of each
+ *    device, which the first call of any entry point on that device performs (with that
+ *    device current); as for every entry point, make that first call before any stream
+ *    capture begins.
  * Requirements and errors otherwise as ringattn_fwd_docmask.
  */
 #define RINGATTN_DOCMASK_NOALLOC_MAX_S 262144

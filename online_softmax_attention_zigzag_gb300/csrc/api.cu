@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <climits>
 #include <cstdint>
 #include <cstdlib>
@@ -14,6 +16,16 @@
 #include "internal.h"
 
 namespace {
+
+// NVTX range over one entry point's host work (argument checks and the launches it
+// enqueues), so that a timeline tool shows permute, attention, merge and the other
+// calls by name.  Without a tool attached a push/pop costs a few nanoseconds.
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Device error word: bounded waits that run out write RA_ERR_TIMEOUT here.  It is a
 // static device variable, so the library allocates nothing; host code reaches it
@@ -25,6 +37,12 @@ __device__ int g_err_word[4];  // status, record set, barrier address, (block <<
 // same slot would share counters: that needs kSchedSlots launches in flight together.)
 constexpr int kSchedSlots = 256;
 __device__ unsigned int g_sched[2 * kSchedSlots];
+// Scratch of ringattn_fwd_docmask_noalloc: the document start of every position, for
+// callers that cannot allocate it.  A file-scope device array, so it exists on every
+// device that loads the library and is never allocated or freed by a call.  In host
+// code the name is only a stand-in for the symbol: the device address comes from
+// cudaGetSymbolAddress, looked up in device_info() with the device current.
+__device__ __align__(256) int g_doc_start_scratch[RINGATTN_DOCMASK_NOALLOC_MAX_S];
 
 constexpr int kMaxDevices = 64;
 
@@ -34,6 +52,7 @@ struct DeviceInfo {
     int sms = 0;
     int* err = nullptr;
     unsigned int* sched = nullptr;  // g_sched on this device
+    int* doc_scratch = nullptr;     // g_doc_start_scratch on this device
     unsigned int next_slot = 0;     // guarded by g_mu
 };
 
@@ -63,6 +82,8 @@ int device_info(DeviceInfo** out) {
             d.err = static_cast<int*>(p);
             if (cudaGetSymbolAddress(&p, g_sched) != cudaSuccess) return RA_ERR_CUDA;
             d.sched = static_cast<unsigned int*>(p);
+            if (cudaGetSymbolAddress(&p, g_doc_start_scratch) != cudaSuccess || !p) return RA_ERR_CUDA;
+            d.doc_scratch = static_cast<int*>(p);
             d.status = RA_OK;
         }
         d.ready = true;
@@ -248,31 +269,6 @@ int fwd_f32(const float* q, const float* k, const float* v, float* out, float* l
     return ra::launch_attn_f32(p, stream);
 }
 
-// Scratch of ringattn_fwd_docmask_noalloc: the document start of every position, for
-// callers that cannot allocate it.  A file-scope device array, so it exists on every
-// device that loads the library and is never allocated or freed by a call.  In host
-// code the name is only a stand-in for the symbol: the device address comes from
-// cudaGetSymbolAddress, looked up once per device with that device current.
-__device__ __align__(256) int g_doc_start_scratch[RINGATTN_DOCMASK_NOALLOC_MAX_S];
-
-int* g_doc_scratch_addr[kMaxDevices];  // per device; guarded by g_mu
-
-// Device address of g_doc_start_scratch on the current device (set-up on first use).
-int doc_scratch(int** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return RA_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return RA_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_doc_scratch_addr[dev]) {
-        int* ptr = nullptr;
-        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_doc_start_scratch) != cudaSuccess || !ptr)
-            return RA_ERR_CUDA;
-        g_doc_scratch_addr[dev] = ptr;
-    }
-    *out = g_doc_scratch_addr[dev];
-    return RA_OK;
-}
-
 // ------------------------------------------------------------------ host-buffer path
 // ringattn_fwd_host runs the natural-order kernel once per group of KV heads, so that the
 // copies of one group overlap the attention of another: H2D of group g+1 and D2H of group
@@ -431,12 +427,14 @@ extern "C" {
 
 int ringattn_fwd(const void* q, const void* k, const void* v, float* out, float* lse, int S, int Hq, int Hkv, int d,
                  int c, int causal, int layout, int kv_block, ra_stream_t stream) {
+    NvtxRange nvtx("ringattn_fwd");
     return fwd_bf16(q, k, v, out, lse, S, Hq, Hkv, d, c, causal, layout, kv_block, 0, -1, 0, -1,
                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 int ringattn_fwd_rank(const void* q, const void* k, const void* v, float* out, float* lse, int S, int Hq, int Hkv,
                       int d, int c, int causal, int layout, int kv_block, int rank, ra_stream_t stream) {
+    NvtxRange nvtx("ringattn_fwd_rank");
     if (rank < 0) return RA_ERR_INVALID_ARG;
     return fwd_bf16(q, k, v, out, lse, S, Hq, Hkv, d, c, causal, layout, kv_block, 0, -1, 0, rank,
                     reinterpret_cast<cudaStream_t>(stream));
@@ -444,6 +442,7 @@ int ringattn_fwd_rank(const void* q, const void* k, const void* v, float* out, f
 
 int ringattn_fwd_docmask(const void* q, const void* k, const void* v, float* out, float* lse, const int* doc_id,
                          int* doc_start, int S, int Hq, int Hkv, int d, int c, int layout, ra_stream_t stream) {
+    NvtxRange nvtx("ringattn_fwd_docmask");
     if (!doc_id || !doc_start || static_cast<const void*>(doc_id) == static_cast<const void*>(doc_start))
         return RA_ERR_INVALID_ARG;
     if (((reinterpret_cast<uintptr_t>(doc_id) | reinterpret_cast<uintptr_t>(doc_start)) & 3u) != 0)
@@ -459,21 +458,20 @@ int ringattn_fwd_docmask(const void* q, const void* k, const void* v, float* out
 int ringattn_fwd_docmask_noalloc(const void* q, const void* k, const void* v, float* out, float* lse,
                                  const int* doc_id, int S, int Hq, int Hkv, int d, int c, int layout,
                                  ra_stream_t stream) {
+    NvtxRange nvtx("ringattn_fwd_docmask_noalloc");
     if (!doc_id || (reinterpret_cast<uintptr_t>(doc_id) & 3u) != 0) return RA_ERR_INVALID_ARG;
     if (S > RINGATTN_DOCMASK_NOALLOC_MAX_S) return RA_ERR_UNSUPPORTED;  // beyond the static scratch
     if (c < 1 || (layout != 0 && layout != 1)) return RA_ERR_INVALID_ARG;
     const int nch = c * (layout == 1 ? 2 : 1);
     if (S < 1 || S % nch != 0) return RA_ERR_INVALID_ARG;
-    // the device check comes before the symbol lookup, which needs a usable device
+    // the scratch address comes from the device's one-time set-up (device_info)
     DeviceInfo* dev = nullptr;
     int st = device_info(&dev);
     if (st != RA_OK) return st;
-    int* scratch = nullptr;
-    if ((st = doc_scratch(&scratch)) != RA_OK) return st;
     // doc_start_kernel rewrites scratch[0, S) on `stream` before the attention kernel
     // reads it, so nothing left by an earlier call is ever read
     return fwd_bf16(q, k, v, out, lse, S, Hq, Hkv, d, c, 1, layout, S / nch, 0, -1, 0, -1,
-                    reinterpret_cast<cudaStream_t>(stream), doc_id, scratch);
+                    reinterpret_cast<cudaStream_t>(stream), doc_id, dev->doc_scratch);
 }
 
 int ringattn_host_workspace_bytes(int S, int Hq, int Hkv, int d, long long* bytes) {
@@ -487,6 +485,7 @@ int ringattn_host_workspace_bytes(int S, int Hq, int Hkv, int d, long long* byte
 int ringattn_fwd_host(const void* q_h, const void* k_h, const void* v_h, float* out_h, float* lse_h, int S, int Hq,
                       int Hkv, int d, int c, int causal, int layout, int kv_block, void* workspace,
                       long long workspace_bytes, ra_stream_t stream) {
+    NvtxRange nvtx("ringattn_fwd_host");
     if (workspace_bytes < 0) return RA_ERR_INVALID_ARG;
     return fwd_host(q_h, k_h, v_h, out_h, lse_h, S, Hq, Hkv, d, c, causal, layout, kv_block, workspace,
                     static_cast<size_t>(workspace_bytes), reinterpret_cast<cudaStream_t>(stream));
@@ -494,6 +493,7 @@ int ringattn_fwd_host(const void* q_h, const void* k_h, const void* v_h, float* 
 
 int ringattn_relayout(const void* src, void* dst, int S, int H, int row_bytes, int c, int layout, int to_heads,
                       ra_stream_t stream) {
+    NvtxRange nvtx("ringattn_relayout");
     if (!src || !dst || src == dst) return RA_ERR_INVALID_ARG;
     if (S < 1 || H < 1 || row_bytes < 1 || c < 1) return RA_ERR_INVALID_ARG;
     if ((layout != 0 && layout != 1) || (to_heads != 0 && to_heads != 1)) return RA_ERR_INVALID_ARG;
@@ -513,6 +513,7 @@ int ringattn_relayout(const void* src, void* dst, int S, int H, int row_bytes, i
 int ringattn_ulysses_fwd(const void* q_seq, const void* k_seq, const void* v_seq, float* out_seq, float* lse_seq,
                          int S, int Hq, int Hkv, int d, int c, int causal, int layout, void* workspace,
                          long long workspace_bytes, ra_stream_t stream) {
+    NvtxRange nvtx("ringattn_ulysses_fwd");
     if (!q_seq || !k_seq || !v_seq || !out_seq || !lse_seq || !workspace) return RA_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < 0) return RA_ERR_INVALID_ARG;
     if (!aligned16(q_seq) || !aligned16(k_seq) || !aligned16(v_seq) || !aligned16(out_seq) ||
@@ -602,6 +603,7 @@ extern "C" {
 int ringattn_bwd(const void* q, const void* k, const void* v, const float* out, const float* lse, const void* dout,
                  float* dq, float* dk, float* dv, float* delta, int S, int Hq, int Hkv, int d, int c, int causal,
                  int layout, int kv_block, ra_stream_t stream) {
+    NvtxRange nvtx("ringattn_bwd");
     return bwd_bf16(q, k, v, out, lse, dout, dq, dk, dv, delta, S, Hq, Hkv, d, c, causal, layout, kv_block, 0,
                     reinterpret_cast<cudaStream_t>(stream));
 }
@@ -609,12 +611,14 @@ int ringattn_bwd(const void* q, const void* k, const void* v, const float* out, 
 int ringattn_bwd_natural(const void* q, const void* k, const void* v, const float* out, const float* lse,
                          const void* dout, float* dq, float* dk, float* dv, float* delta, int S, int Hq, int Hkv,
                          int d, int c, int causal, int layout, int kv_block, ra_stream_t stream) {
+    NvtxRange nvtx("ringattn_bwd_natural");
     return bwd_bf16(q, k, v, out, lse, dout, dq, dk, dv, delta, S, Hq, Hkv, d, c, causal, layout, kv_block, 1,
                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 int ringattn_fwd_natural(const void* q, const void* k, const void* v, float* out, float* lse, int S, int Hq,
                          int Hkv, int d, int c, int causal, int layout, int kv_block, ra_stream_t stream) {
+    NvtxRange nvtx("ringattn_fwd_natural");
     return fwd_bf16(q, k, v, out, lse, S, Hq, Hkv, d, c, causal, layout, kv_block, 1, -1, 0, -1,
                     reinterpret_cast<cudaStream_t>(stream));
 }
@@ -622,6 +626,7 @@ int ringattn_fwd_natural(const void* q, const void* k, const void* v, float* out
 int ringattn_fwd_hop(const void* q, const void* k, const void* v, float* o_part, float* lse_part, int S, int Hq,
                      int Hkv, int d, int c, int causal, int layout, int kv_block, int hop, int sub,
                      ra_stream_t stream) {
+    NvtxRange nvtx("ringattn_fwd_hop");
     if (hop < 0) return RA_ERR_INVALID_ARG;
     return fwd_bf16(q, k, v, o_part, lse_part, S, Hq, Hkv, d, c, causal, layout, kv_block, 0, hop, sub, -1,
                     reinterpret_cast<cudaStream_t>(stream));
@@ -629,6 +634,7 @@ int ringattn_fwd_hop(const void* q, const void* k, const void* v, float* o_part,
 
 int ringattn_fwd_f32(const float* q, const float* k, const float* v, float* out, float* lse, int S, int Hq,
                      int Hkv, int d, int c, int causal, int layout, int kv_block, ra_stream_t stream) {
+    NvtxRange nvtx("ringattn_fwd_f32");
     return fwd_f32(q, k, v, out, lse, S, Hq, Hkv, d, c, causal, layout, kv_block, -1, 0,
                    reinterpret_cast<cudaStream_t>(stream));
 }
@@ -636,6 +642,7 @@ int ringattn_fwd_f32(const float* q, const float* k, const float* v, float* out,
 int ringattn_fwd_hop_f32(const float* q, const float* k, const float* v, float* o_part, float* lse_part, int S,
                          int Hq, int Hkv, int d, int c, int causal, int layout, int kv_block, int hop, int sub,
                          ra_stream_t stream) {
+    NvtxRange nvtx("ringattn_fwd_hop_f32");
     if (hop < 0) return RA_ERR_INVALID_ARG;
     return fwd_f32(q, k, v, o_part, lse_part, S, Hq, Hkv, d, c, causal, layout, kv_block, hop, sub,
                    reinterpret_cast<cudaStream_t>(stream));
@@ -643,6 +650,7 @@ int ringattn_fwd_hop_f32(const float* q, const float* k, const float* v, float* 
 
 int ringattn_merge(float* o_run, float* lse_run, const float* o_part, const float* lse_part, long long rows, int d,
                    ra_stream_t stream) {
+    NvtxRange nvtx("ringattn_merge");
     if (rows < 0 || d < 1 || d > 4096) return RA_ERR_INVALID_ARG;
     if (rows > 0 && (!o_run || !lse_run || !o_part || !lse_part)) return RA_ERR_INVALID_ARG;
     if (rows == 0) return RA_OK;
@@ -654,6 +662,7 @@ int ringattn_merge(float* o_run, float* lse_run, const float* o_part, const floa
 
 int ringattn_permute(const void* src, void* dst, int S, int H, int row_bytes, int c, int layout, int inverse,
                      ra_stream_t stream) {
+    NvtxRange nvtx("ringattn_permute");
     if (!src || !dst || src == dst) return RA_ERR_INVALID_ARG;
     if (S < 1 || H < 1 || row_bytes < 1 || c < 1) return RA_ERR_INVALID_ARG;
     if ((layout != 0 && layout != 1) || (inverse != 0 && inverse != 1)) return RA_ERR_INVALID_ARG;
