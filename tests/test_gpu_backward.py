@@ -102,10 +102,15 @@ def test_backward_4096_mha_both_layouts(ra):
             assert excess.max() <= 1e-6 * a.max(), (layout, name)
 
 
-def test_backward_32k_sampled_dq_and_dv_column_sums(ra):
-    """The 32k GQA zigzag workload: dq on sampled rows against the oracle, and for every
-    KV head the exact identity sum_j dv_j = sum over its query heads and rows of dout_i
-    (the softmax weights of a row sum to one), within 2^-8 of sum |dout_i|."""
+def test_backward_32k_sampled_rows_and_dv_column_sums(ra):
+    """The 32k GQA zigzag workload.
+    * dq on 256 sampled rows against the oracle;
+    * dk and dv on 256 sampled (KV head, key) rows among the last 512 keys of the sequence,
+      against the oracle (a key's gradient adds up over every later row of its 8 query
+      heads, so keys near the end are the ones the oracle can afford at this size);
+    * for every KV head the exact identity sum_j dv_j = sum over its query heads and rows
+      of dout_i (the softmax weights of a row sum to one), within 2^-8 of sum |dout_i|,
+      which reaches every key tile of the dK/dV kernel."""
     from online_softmax_attention_zigzag_gb300.configs import CAUSAL_GQA_S32K as w
     from online_softmax_attention_zigzag_gb300.inputs import make_qkv, sample_rows
     q, k, v = make_qkv(w)
@@ -129,6 +134,17 @@ def test_backward_32k_sampled_dq_and_dv_column_sums(ra):
     got = dq_n[hs, ps].double().numpy()
     excess = np.abs(got - want) - REL * a
     assert excess.max() <= 1e-6 * a.max(), float(excess.max())
+    # dk, dv at keys among the last 512 positions (and the very last key of each head)
+    kh, kp = sample_rows(w.bhkv, 512, 256, seed=1235)
+    kp = kp + (S - 512)
+    kh = torch.cat([kh, torch.arange(w.bhkv)])
+    kp = torch.cat([kp, torch.full((w.bhkv,), S - 1, dtype=torch.int64)])
+    wdk, wdv, adk, adv = obwd.dkv_rows(q, k, v, dout, kh.numpy(), kp.numpy(), True, with_abs=True)
+    dk_n, dv_n = natural(dk.cpu(), S, c, L), natural(dv.cpu(), S, c, L)
+    for name, g_, w_, a_ in (("dk", dk_n, wdk, adk), ("dv", dv_n, wdv, adv)):
+        got = g_[kh, kp].double().numpy()
+        excess = np.abs(got - w_) - REL * a_
+        assert excess.max() <= 1e-6 * a_.max(), (name, float(excess.max()))
     g = w.hq // w.hkv
     dsum = dv.double().sum(dim=1).cpu()                                  # [Hkv, d]
     want_sum = dout.double().reshape(w.bhkv, g, S, w.d).sum(dim=(1, 2))  # [Hkv, d]

@@ -316,42 +316,84 @@ def test_bf16_gqa_32k_sampled(ra):
 
 
 def test_bf16_gqa_128k_sampled(ra):
-    """S=131072, 32/8 heads, d=128, c=16 zigzag: 1024 rows + edge rows."""
+    """S=131072, 32/8 heads, d=128, c=16 zigzag: 4096 rows + edge rows."""
     from online_softmax_attention_zigzag_gb300.configs import CAUSAL_GQA_S128K as w
-    errs, *_ = _sampled_check(ra, w, 1024)
+    errs, *_ = _sampled_check(ra, w, 4096)
     for name, (eo, el) in errs.items():
         assert eo <= TOL_BF16_OUT and el <= TOL_BF16_LSE, (name, eo, el)
 
 
-def test_bf16_noncausal_outliers_64k_fused_and_per_hop(ra):
-    """B=2, S=65536, 16 heads, non-causal, 1% of Q/K entries x8, c=8 contiguous.
-    Fused path on sampled rows; the per-hop path (kv_block 8192) folded with the merge
-    kernel must agree with the fused result."""
+@pytest.fixture(scope="module")
+def outliers_64k(ra):
+    """The non-causal B=2 S=65536 16-head workload (1% of Q/K entries x8, c=8 contiguous):
+    rank-major device inputs, the fused result and the oracle on 4096 sampled rows plus
+    the edge rows.  Shared by the fused check and the per-hop sweep."""
     from online_softmax_attention_zigzag_gb300.configs import NONCAUSAL_MHA_B2_S64K as w
-    errs, out, lse, (q, k, v) = _sampled_check(ra, w, 1024)
-    for name, (eo, el) in errs.items():
-        assert eo <= TOL_BF16_OUT and el <= TOL_BF16_LSE, (name, eo, el)
-    del q, k, v
-    from online_softmax_attention_zigzag_gb300.inputs import make_qkv
+    from online_softmax_attention_zigzag_gb300.inputs import edge_rows, make_qkv, sample_rows
     q, k, v = make_qkv(w)
-    S, c, kvb = w.seq, w.c, 8192
-    qd, kd, vd = (torch.empty_like(x, device=dev()) for x in (q, k, v))
+    hs, ps = sample_rows(w.bhq, w.seq, 4096)
+    he, pe = edge_rows(w.bhq, w.seq, w.n_chunks)
+    hs, ps = torch.cat([hs, he]), torch.cat([ps, pe])
+    ro, rl = oatt.full_attention_rows(q, k, v, hs.numpy(), ps.numpy(), False)
+    qd, kd, vd = (torch.empty(x.shape, dtype=x.dtype, device=dev()) for x in (q, k, v))
     for src, dst in ((q, qd), (k, kd), (v, vd)):
-        ra.permute(src.to(dev()), dst, c=c, layout=w.layout, inverse=0)
+        ra.permute(src.to(dev()), dst, c=w.c, layout=w.layout, inverse=0)
+    del q, k, v
+    o = torch.empty((w.bhq, w.seq, w.d), dtype=torch.float32, device=dev())
+    l = torch.empty((w.bhq, w.seq), dtype=torch.float32, device=dev())
+    ra.fwd(qd, kd, vd, o, l, c=w.c, causal=w.causal, layout=w.layout, kv_block=w.kv_block)
+    on, ln = torch.empty_like(o), torch.empty_like(l)
+    ra.permute(o, on, c=w.c, layout=w.layout, inverse=1)
+    ra.permute(l, ln, c=w.c, layout=w.layout, inverse=1)
+    torch.cuda.synchronize()
+    _status_ok(ra)
+    del o, l
+    yield dict(w=w, qkv=(qd, kd, vd), rows=(hs, ps), oracle=(ro, rl), fused=(on, ln))
+    torch.cuda.empty_cache()
+
+
+def test_bf16_noncausal_outliers_64k_fused(ra, outliers_64k):
+    """Fused path on 4096 sampled rows and the edge rows against the oracle."""
+    hs, ps = outliers_64k["rows"]
+    ro, rl = outliers_64k["oracle"]
+    on, ln = outliers_64k["fused"]
+    hd, pd = hs.to(dev()), ps.to(dev())
+    assert max_err(on[hd, pd].cpu(), ro) <= TOL_BF16_OUT
+    assert max_err(ln[hd, pd].cpu(), rl) <= TOL_BF16_LSE
+
+
+@pytest.mark.parametrize("kv_block", [512, 1024, 2048, 4096, 8192])
+def test_bf16_noncausal_outliers_64k_per_hop_sweep(ra, outliers_64k, kv_block):
+    """The ring-faithful per-hop path at every message size of the sweep: one
+    ringattn_fwd_hop partial per message (c hops x chunk / kv_block sub-blocks), each
+    folded into the running result by the merge kernel.  The folded result against the
+    oracle on the sampled and edge rows, and against the fused result everywhere."""
+    w = outliers_64k["w"]
+    qd, kd, vd = outliers_64k["qkv"]
+    hs, ps = outliers_64k["rows"]
+    ro, rl = outliers_64k["oracle"]
+    on, ln = outliers_64k["fused"]
+    S, c = w.seq, w.c
     o_run = torch.zeros((w.bhq, S, w.d), dtype=torch.float32, device=dev())
     l_run = torch.full((w.bhq, S), -float("inf"), dtype=torch.float32, device=dev())
     op, lp = torch.empty_like(o_run), torch.empty_like(l_run)
     for hop in range(c):
-        for sub in range((S // c) // kvb):
-            ra.fwd_hop(qd, kd, vd, op, lp, c=c, causal=w.causal, layout=w.layout, kv_block=kvb, hop=hop, sub=sub)
+        for sub in range((S // c) // kv_block):
+            ra.fwd_hop(qd, kd, vd, op, lp, c=c, causal=w.causal, layout=w.layout, kv_block=kv_block, hop=hop,
+                       sub=sub)
             ra.merge(o_run, l_run, op, lp)
+    del op, lp
     o_nat, l_nat = torch.empty_like(o_run), torch.empty_like(l_run)
     ra.permute(o_run, o_nat, c=c, layout=w.layout, inverse=1)
     ra.permute(l_run, l_nat, c=c, layout=w.layout, inverse=1)
     torch.cuda.synchronize()
     _status_ok(ra)
-    assert (o_nat - out).abs().max().item() <= TOL_BF16_OUT
-    assert (l_nat - lse).abs().max().item() <= TOL_BF16_LSE
+    del o_run, l_run
+    hd, pd = hs.to(dev()), ps.to(dev())
+    assert max_err(o_nat[hd, pd].cpu(), ro) <= TOL_BF16_OUT
+    assert max_err(l_nat[hd, pd].cpu(), rl) <= TOL_BF16_LSE
+    assert (o_nat - on).abs().max().item() <= TOL_BF16_OUT
+    assert (l_nat - ln).abs().max().item() <= TOL_BF16_LSE
 
 
 # ------------------------------------------------------------------ failure path
