@@ -36,7 +36,9 @@ from online_softmax_attention_zigzag_gb300.configs import (  # noqa: E402
 from online_softmax_attention_zigzag_gb300.inputs import doc_ids, make_qkv, sample_rows  # noqa: E402
 
 METRIC = "causal-adjusted attention TFLOP/s and % of GB300 bf16 tensor peak, 1 GPU"
-NOMINAL_BF16_TFLOPS = 2250.0  # GB300 dense bf16 tensor rate, vendor figure (without 2:4 sparsity)
+# GB300 dense bf16 tensor rate: NVIDIA's HGX B300 datasheet lists 36 PFLOPS FP16/BF16 for
+# eight GPUs with 2:4 sparsity, i.e. 4.5 PFLOPS sparse and 2.25 PFLOPS dense per GPU.
+NOMINAL_BF16_TFLOPS = 2250.0
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
@@ -150,51 +152,53 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle baseline
-def cpu_oracle_sample(w, budget_s: float, seed: int = 7, qkv=None):
-    """Time the float64 oracle on sampled query rows of workload ``w``; returns
-    (TFLOP/s, rows, seconds, threads).  Input generation is not timed."""
+CPU_UNIT_ROWS = 4096  # query rows per timed unit of the CPU oracle (one full_attention_rows call)
+
+
+def cpu_oracle_units(w, qkv, budget_s: float, first_unit: int = 0, min_units: int = 1):
+    """Time the float64 oracle on units of CPU_UNIT_ROWS seeded random query rows of
+    workload ``w`` (unit i draws its rows with seed 7000 + i), until ``budget_s`` seconds
+    of oracle time and at least ``min_units`` units are spent.  Returns a list of
+    (flop, seconds) per unit.  Input generation is not timed.  The GPU arm's cpu_baseline
+    and the reference arm both time these units, so they report the same quantity."""
     from oracle.attention import full_attention_rows
-    q, k, v = qkv if qkv is not None else make_qkv(w)
-    hs, ps = sample_rows(w.bhq, w.seq, 1 << 20, seed=seed)
-    perm = np.random.default_rng(seed).permutation(len(hs))
-    hs, ps = hs.numpy()[perm], ps.numpy()[perm]
-
-    def flop(pos):
-        keys = (pos + 1) if w.causal else np.full_like(pos, w.seq)
-        return float(np.sum(4.0 * w.d * keys))
-
-    n, done_rows, done_flop, t_used = 32, 0, 0.0, 0.0
-    while t_used < budget_s and done_rows < len(hs):
-        sel = slice(done_rows, min(done_rows + n, len(hs)))
+    q, k, v = qkv
+    res, spent, i = [], 0.0, first_unit
+    while spent < budget_s or len(res) < min_units:
+        hs, ps = sample_rows(w.bhq, w.seq, CPU_UNIT_ROWS, seed=7000 + i)
+        hs, ps = hs.numpy(), ps.numpy()
+        keys = (ps + 1) if w.causal else np.full_like(ps, w.seq)
+        flop = float(np.sum(4.0 * w.d * keys))
         t0 = time.perf_counter()
-        full_attention_rows(q, k, v, hs[sel], ps[sel], bool(w.causal))
-        t_used += time.perf_counter() - t0
-        done_flop += flop(ps[sel])
-        done_rows = sel.stop
-        n = min(4 * n, 4096)
+        full_attention_rows(q, k, v, hs, ps, bool(w.causal))
+        dt = time.perf_counter() - t0
+        res.append((flop, dt))
+        spent += dt
+        i += 1
+    return res
+
+
+def cpu_threads() -> int:
     try:
         from threadpoolctl import threadpool_info
-        threads = max(i.get("num_threads", 1) for i in threadpool_info()) if threadpool_info() else 1
+        info = threadpool_info()
+        if info:
+            return max(i.get("num_threads", 1) for i in info)
     except Exception:
-        threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return done_flop / t_used / 1e12, done_rows, t_used, threads
+        pass
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
 
 
 def run_reference(args, w, rank):
+    """The reference arm: the float64 CPU oracle as it stands, one unit of
+    CPU_UNIT_ROWS sampled query rows per step, rank 0 only."""
     if rank != 0:
         return
-    per_step = []
-    rows_total = 0
-    threads = 1
-    budget = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
     qkv = make_qkv(w)
-    for i in range(args.warmup + args.steps):
-        tf, rows, secs, threads = cpu_oracle_sample(w, budget, seed=100 + i, qkv=qkv)
-        if i >= args.warmup:
-            per_step.append((tf, rows, secs))
-            rows_total += rows
-    value = float(np.mean([x[0] for x in per_step]))
-    secs = sum(x[2] for x in per_step)
+    units = cpu_oracle_units(w, qkv, 0.0, first_unit=0, min_units=args.warmup + args.steps)[args.warmup:]
+    flop = sum(f for f, _ in units)
+    secs = sum(t for _, t in units)
+    value = flop / secs / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
@@ -202,8 +206,9 @@ def run_reference(args, w, rank):
         "data": "synthetic (seeded N(0,1))",
         "config": {"workload": w.name, "S": w.seq, "Hq": w.hq, "Hkv": w.hkv, "d": w.d, "c": w.c,
                    "causal": w.causal, "layout": "zigzag" if w.layout else "contiguous", "batch": w.batch},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"{rows_total} sampled query rows over {args.steps} steps, float64 numpy"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                         "sample": f"{args.steps} units of {CPU_UNIT_ROWS} seeded random query rows "
+                                   f"({secs:.1f} s), float64 numpy"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -339,7 +344,7 @@ def backward_only(ra, w, dev, stream, reps, peak):
             "flop": "2.5 x the causal-adjusted forward FLOP"}
 
 
-def per_hop_sweep(ra, w, dev, stream):
+def per_hop_sweep(ra, w, dev, stream, reps=3):
     """Fused kernel vs the ring-faithful per-hop path (one partial per message, folded in
     with the merge kernel) for each kv_block of the workload's sweep."""
     q_h, k_h, v_h = make_qkv(w)
@@ -353,7 +358,7 @@ def per_hop_sweep(ra, w, dev, stream):
     out = []
     for kvb in (w.kv_sweep or (w.kv_block,)):
         kw = dict(c=w.c, causal=w.causal, layout=w.layout, kv_block=kvb)
-        fused_ms = time_events(lambda: ra.fwd(qr, kr, vr, o, l, **kw), 3, stream)
+        fused_ms = time_events(lambda: ra.fwd(qr, kr, vr, o, l, **kw), reps, stream)
         n_msg = (w.seq // w.c) // kvb
 
         def ring():
@@ -364,7 +369,7 @@ def per_hop_sweep(ra, w, dev, stream):
                     ra.fwd_hop(qr, kr, vr, op, lp, hop=hop, sub=sub, **kw)
                     ra.merge(o, l, op, lp)
         ring_ms = time_events(ring, 1, stream)
-        merge_ms = time_events(lambda: ra.merge(o, l, op, lp), 3, stream)
+        merge_ms = time_events(lambda: ra.merge(o, l, op, lp), reps, stream)
         mbytes = rows * (12 * w.d + 12)
         out.append({"kv_block": kvb, "messages": w.c * n_msg, "fused_ms": fused_ms,
                     "fused_tflops": w.flops() / (fused_ms * 1e-3) / 1e12, "per_hop_ms": ring_ms,
@@ -376,7 +381,7 @@ def per_hop_sweep(ra, w, dev, stream):
     return out
 
 
-def per_rank(ra, workloads, dev, stream):
+def per_rank(ra, workloads, dev, stream, reps=5):
     """One ringattn_fwd_rank launch per virtual rank, contiguous and zigzag: device time,
     128x128 tiles and visible (query, key) pairs of each rank.  The time of a ring step is
     the slowest rank's; zigzag evens the ranks out."""
@@ -394,11 +399,11 @@ def per_rank(ra, workloads, dev, stream):
             units, pairs, tiles = ra.rank_work(w.seq, w.c, w.causal, w.layout, 128)
             ranks = []
             for r in range(w.c):
-                ms = time_events(lambda: ra.fwd_rank(qr, kr, vr, o, l, rank=r, **kw), 5, stream)
+                ms = time_events(lambda: ra.fwd_rank(qr, kr, vr, o, l, rank=r, **kw), reps, stream)
                 fl = 4.0 * w.d * w.bhq * float(pairs[r])
                 ranks.append({"rank": r, "kernel_ms": ms, "units": int(units[r]), "tiles_per_head": int(tiles[r]),
                               "pairs_per_head": int(pairs[r]), "tflops": fl / (ms * 1e-3) / 1e12})
-            full_ms = time_events(lambda: ra.fwd(qr, kr, vr, o, l, **kw), 5, stream)
+            full_ms = time_events(lambda: ra.fwd(qr, kr, vr, o, l, **kw), reps, stream)
             t = [x["kernel_ms"] for x in ranks]
             out.append({"workload": w.name, "layout": "zigzag" if layout else "contiguous", "ranks": ranks,
                         "max_over_min_ms": max(t) / min(t), "sum_ms": sum(t), "all_ranks_one_launch_ms": full_ms})
@@ -585,12 +590,25 @@ def main():
         extra.append(ulysses_only(ra, w, dev, stream, 5, peaks()[0], peaks()[2]))
         torch.cuda.empty_cache()
         extra.append(backward_only(ra, w, dev, stream, 3, peaks()[0]))
+        torch.cuda.empty_cache()
+        # the non-causal B=2 S=65536 outlier workload: fused kernel against the per-hop
+        # path (one partial per ring message + merge) at every message size of its sweep
+        w5 = WORKLOADS["noncausal_mha_B2_S65536_h16_d128_c8_contig"]
+        extra.append({"mode": "per-hop sweep (fused kernel vs one partial per message + merge)",
+                      "workload": w5.name, "sweep": per_hop_sweep(ra, w5, dev, stream, reps=2)})
+        torch.cuda.empty_cache()
+        # per-rank work of the 4096-token MHA workload, contiguous and zigzag: one launch
+        # restricted to each virtual rank's rows
+        extra.append({"mode": "per-rank launches", "per_rank": per_rank(ra, [CAUSAL_MHA_S4K], dev, stream)})
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        tf, rows_s, secs, threads = cpu_oracle_sample(w, args.cpu_seconds, qkv=(q_h, k_h, v_h))
-        cpu = {"value": tf, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"{rows_s} sampled query rows ({secs:.1f} s), float64 numpy, same inputs"}
+        units = cpu_oracle_units(w, (q_h, k_h, v_h), args.cpu_seconds)
+        secs = sum(t for _, t in units)
+        cpu = {"value": sum(f for f, _ in units) / secs / 1e12, "unit": UNIT, "cores": cpu_threads(),
+               "kind": "oracle",
+               "sample": f"{len(units)} units of {CPU_UNIT_ROWS} seeded random query rows ({secs:.1f} s), "
+                         "float64 numpy, same inputs (the reference arm times the same units)"}
 
     if rank == 0:
         line = {

@@ -14,35 +14,11 @@
 // A row is one (token, head) vector of `row` bytes (d bf16 values, d fp32 values, or one
 // fp32 lse).  The kernel walks the destination one chunk-sized slab at a time, so each
 // source row address comes from one chunk-base lookup and a division by a constant.
+#include "fastdiv.h"
 #include "internal.h"
 
 namespace ra {
 namespace {
-
-// Division of n < 2^31 by a fixed d >= 1 with one wide multiply and a shift
-// (Granlund and Montgomery, "Division by invariant integers using multiplication",
-// 1994): with l = ceil(log2 d) and mult = ceil(2^(31+l) / d), n / d = (n * mult) >> (31+l)
-// exactly, because n * (mult - 2^(31+l)/d) / 2^(31+l) < 2^-l <= 1/d.
-struct FastDiv {
-    unsigned long long mult;
-    int shift;
-    unsigned d;
-};
-
-FastDiv make_fastdiv(unsigned d) {
-    int l = 0;
-    while ((1ull << l) < d) ++l;
-    const unsigned long long num = 1ull << (31 + l);
-    FastDiv f;
-    f.mult = (num + d - 1) / d;
-    f.shift = 31 + l;
-    f.d = d;
-    return f;
-}
-
-__device__ __forceinline__ unsigned fdiv(unsigned n, const FastDiv& f) {
-    return static_cast<unsigned>((static_cast<unsigned long long>(n) * f.mult) >> f.shift);
-}
 
 struct RelayoutArgs {
     long long S;          // tokens
