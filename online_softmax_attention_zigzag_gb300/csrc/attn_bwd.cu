@@ -5,10 +5,11 @@
 // exact gradient of that forward.  With P_ij = exp(q_i . k_j - lse_i) over visible keys,
 // D_i = dout_i . out_i and dS_ij = P_ij (dout_i . v_j - D_i):
 //     dV_j = sum_i P_ij dout_i,   dK_j = sum_i dS_ij q_i,   dQ_i = sum_j dS_ij k_j,
-// a KV head summing over the query heads that use it.  The ring order is kept: a query
-// tile meets the KV blocks hop by hop as in the forward (the dq kernel), and a KV block
-// travels round the ring with its dK, dV accumulators, meeting rank (s + h) mod c's
-// queries at hop h (the dk/dv kernel).  Only the order of the fp32 sums depends on it.
+// a KV head summing over the query heads that use it.  In the dq kernel a query tile meets
+// the KV blocks hop by hop in ring order, as in the forward.  In the dk/dv kernel a key
+// tile meets the query tiles from the end of the sequence down, every query head of its
+// group at each position, which keeps the Q and dO tiles the CTAs read at one time in L2
+// (see for_each_query_tile).  Only the order of the fp32 sums depends on either order.
 //
 // Three kernels, all on the caller's stream:
 //   * bwd_delta_kernel   D_i = dout_i . out_i, one warp per row (HBM-bound);
@@ -134,27 +135,25 @@ __device__ __forceinline__ int count_key_tiles(const Ring& R, int qp) {
     return n;
 }
 
-// Query tiles the key tile at kp meets as its block travels: hop h visits rank
-// (s + h) mod c; each query tile is met once per query head of the KV group.
+// Query tiles the key tile at kp meets, every query head of the KV group for each tile
+// position, positions in descending natural order (down to kp under the causal mask).
+// Every CTA of a launch starts its item at the end of the sequence and moves down at the
+// same rate (a position costs the same for every key tile), so the CTAs read the same Q
+// and dO tiles at about the same time and each tile comes from DRAM about once; the
+// ring's order (hop h meets rank (s + h) mod c, each CTA starting at its own rank) had
+// every CTA in a different part of the 8 heads' Q and dO and read them ~9 times over.
+// Only the order of the fp32 sums into dK, dV depends on it.
 template <class F>
 __device__ __forceinline__ void for_each_query_tile(const Ring& R, int hk, int kp, F&& f) {
-    const int s = rank_of(R, kp);
-    for (int hop = 0; hop < R.c; ++hop) {
-        const int r = (s + hop) % R.c;
-        for (int slot = 0; slot < R.nslot; ++slot) {
-            const int base = (slot ? 2 * R.c - 1 - r : r) * R.m;
-            const int first = (R.causal && kp > base) ? kp : base;
-            for (int t0 = first; t0 < base + R.m; t0 += kTile)
-                for (int x = 0; x < R.g; ++x)
-                    if (!f(hk * R.g + x, t0)) return;
-        }
-    }
+    const int lo = R.causal ? kp : 0;
+    for (int t0 = R.S - kTile; t0 >= lo; t0 -= kTile)
+        for (int x = 0; x < R.g; ++x)
+            if (!f(hk * R.g + x, t0)) return;
 }
 
 __device__ __forceinline__ int count_query_tiles(const Ring& R, int hk, int kp) {
-    int n = 0;
-    for_each_query_tile(R, hk, kp, [&](int, int) { ++n; return true; });
-    return n;
+    (void)hk;
+    return ((R.S - (R.causal ? kp : 0)) / kTile) * R.g;
 }
 
 // Named barrier over one compute warpgroup (128 threads); returns the AND of `ok`.
