@@ -778,7 +778,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const WaitCtl wc{abort_flag, p.err, p.timeout_ns};
 
-    // warps 0-15: softmax, warpgroup g = warp / 4 owns tile g / 2, key half g % 2
+    // warps 0-7: two softmax warpgroups, warpgroup x = warp / 4 owns unit x (full rows);
+    // warps 8 and 9 issue the MMAs of units 0 and 1; warp 10 loads
     if (warp < 8) {
         softmax_role<D, DOC>(p, warp / 4, b, tmem, ring, wc);
     } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
