@@ -151,6 +151,18 @@ __device__ __forceinline__ void for_each_query_tile(const Ring& R, int hk, int k
             if (!f(hk * R.g + x, t0)) return;
 }
 
+// The query tile for_each_query_tile visits after (hq, t0) for the key tile at kp;
+// false when (hq, t0) is the last.
+__device__ __forceinline__ bool next_query_tile(const Ring& R, int hk, int kp, int hq, int t0, int& nhq, int& nt0) {
+    nhq = hq + 1;
+    nt0 = t0;
+    if (nhq == (hk + 1) * R.g) {
+        nhq = hk * R.g;
+        nt0 = t0 - kTile;
+    }
+    return nt0 >= (R.causal ? kp : 0);
+}
+
 __device__ __forceinline__ int count_query_tiles(const Ring& R, int hk, int kp) {
     (void)hk;
     return ((R.S - (R.causal ? kp : 0)) / kTile) * R.g;
@@ -238,14 +250,15 @@ struct Bars {
     uint64_t *res_full, *res_empty;  // resident tiles landed / item's MMAs done with them
     uint64_t *s_full, *dp_full;      // S (S^T) / dP (dP^T) in TMEM
     uint64_t *s_free, *dp_free;      // 256 compute threads copied S / dP out of TMEM
-    uint64_t *ds_full;               // [2] dq: dS buffer written; dk/dv: [0] P^T, dS^T written
+    uint64_t *ds_full;               // [2] dq: dS buffer written; dk/dv: [0] dS^T written
+    uint64_t *pt_full;               // dk/dv: P^T written (the same barrier as ds_full[1])
     uint64_t *acc_done, *acc_free, *drain, *drain2;
     uint64_t *ds_free;  // [2] dQ kernel: the dQ product that read dS buffer b is done
     uint64_t *a_full, *a_empty, *b_full, *b_empty;
     uint64_t *item_full, *item_empty;  // [kItemRing] each: item ids handed from the loader
     __device__ explicit Bars(uint64_t* b)
         : res_full(b), res_empty(b + 1), s_full(b + 2), dp_full(b + 3), s_free(b + 4), dp_free(b + 5),
-          ds_full(b + 6), acc_done(b + 8), acc_free(b + 9), drain(b + 10), drain2(b + 11), ds_free(b + 12), a_full(b + 16), a_empty(b + 19),
+          ds_full(b + 6), pt_full(b + 7), acc_done(b + 8), acc_free(b + 9), drain(b + 10), drain2(b + 11), ds_free(b + 12), a_full(b + 16), a_empty(b + 19),
           b_full(b + 22), b_empty(b + 24), item_full(b + 26), item_empty(b + 30) {}
 };
 
@@ -502,19 +515,24 @@ __device__ void dq_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
             float x[64];
             tmem_take64(s_tm, x, b.s_free);
             const int lim = qpos - (t0 + h * 64);  // my keys [0, lim] are visible
-            const bool mask = R.causal && lim < 63;
+            // only tiles on the diagonal mask; branch on the warp, not per element
+            if (__any_sync(0xffffffffu, R.causal && lim < 63)) {
+                const int lm = R.causal ? lim : 63;
 #pragma unroll
-            for (int i = 0; i < 64; i += 2) {
-                float p0, p1;
-                ffma2(p0, p1, x[i], x[i + 1], kLog2e, kLog2e, nl, nl);
-                p0 = ex2(p0);
-                p1 = ex2(p1);
-                if (mask) {
-                    p0 = (i > lim) ? 0.f : p0;
-                    p1 = (i + 1 > lim) ? 0.f : p1;
+                for (int i = 0; i < 64; i += 2) {
+                    float p0, p1;
+                    ffma2(p0, p1, x[i], x[i + 1], kLog2e, kLog2e, nl, nl);
+                    x[i] = (i > lm) ? 0.f : ex2(p0);
+                    x[i + 1] = (i + 1 > lm) ? 0.f : ex2(p1);
                 }
-                x[i] = p0;
-                x[i + 1] = p1;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 64; i += 2) {
+                    float p0, p1;
+                    ffma2(p0, p1, x[i], x[i + 1], kLog2e, kLog2e, nl, nl);
+                    x[i] = ex2(p0);
+                    x[i + 1] = ex2(p1);
+                }
             }
             if (!warp_wait(b.dp_full, dpf & 1u, wc)) { ok = false; return false; }
             ++dpf;
@@ -523,7 +541,12 @@ __device__ void dq_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
             tmem_take64(dp_tm, dp, b.dp_free);
             uint32_t pk[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(x[2 * i] * (dp[2 * i] - dl), x[2 * i + 1] * (dp[2 * i + 1] - dl));
+            for (int i = 0; i < 32; ++i) {
+                float a0, a1;
+                fadd2(a0, a1, dp[2 * i], dp[2 * i + 1], -dl, -dl);  // dP - D
+                fmul2(a0, a1, a0, a1, x[2 * i], x[2 * i + 1]);     // P (dP - D)
+                pk[i] = pack_bf16x2(a0, a1);
+            }
             const int bb = jj & 1;  // dS buffer, as the MMA issuer counts it
             // the dQ product of two tiles ago, issued by the other issuer, has read it
             if (!warp_wait(&b.ds_free[bb], (dsf[bb] & 1u) ^ 1u, wc)) { ok = false; return false; }
@@ -593,7 +616,7 @@ __device__ void kv_mma(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uin
     const Ring& R = p.ring;
     const uint32_t sK = smem_u32(smem), sV = sK + C::kTileBytes;
     const uint32_t sA = sK + C::kAOff, sB = sK + C::kBOff;
-    uint32_t idx = 0, kit = 0, sf = 0, pf = 0;
+    uint32_t idx = 0, kit = 0, pf = 0, dsf = 0;
     bool ok = true;
     for (uint32_t n_it = 0; ok; ++n_it) {
         const int item = take_item(b.item_full, b.item_empty, ring, n_it, (threadIdx.x & 31) == 0, wc);
@@ -613,30 +636,34 @@ __device__ void kv_mma(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uin
         tc_fence_after();
         issue_kk<D>(tmem + kTile, sV, sB + (i0 % C::kSlotsB) * C::kTileBytes);
         mma_commit_e(b.dp_full);
+        // Per query tile t the tensor pipe takes dV(t), S^T(t+1), dK(t), dP^T(t+1) in that
+        // order.  P^T(t) sits over S^T(t)'s columns and dS^T(t) over dP^T(t)'s, so each
+        // product that overwrites them comes after the one that reads them (the pipe runs
+        // a CTA's MMAs in issue order), and only dK(t) and dP^T(t+1) lie between one dS^T
+        // and the next.
         for (int t = 0; t < n && ok; ++t) {
             const uint32_t i = i0 + t;
             const bool more = t + 1 < n;
-            // the next S^T as soon as this tile's S^T is out of TMEM
-            if (!mbar_wait_w(b.s_free, sf & 1u, wc)) { ok = false; break; }
-            ++sf;
-            if (more) {
-                if (!ring_wait_w(b.a_full, i + 1, C::kSlotsA, wc)) { ok = false; break; }
-                tc_fence_after();
-                issue_kk<D>(tmem, sK, sA + ((i + 1) % C::kSlotsA) * C::kTileBytes);
-                mma_commit_e(b.s_full);
-            }
-            if (!mbar_wait_w(&b.ds_full[0], pf & 1u, wc)) { ok = false; break; }
+            if (!mbar_wait_w(b.pt_full, pf & 1u, wc)) { ok = false; break; }
             ++pf;
             if (t == 0 && !mbar_wait_w(b.acc_free, (kit & 1u) ^ 1u, wc)) { ok = false; break; }
             tc_fence_after();
             const uint32_t sq = sA + (i % C::kSlotsA) * C::kTileBytes;
             const uint32_t sdo = sB + (i % C::kSlotsB) * C::kTileBytes;
-            issue_tm<D>(tmem + kAccCol, tmem + kTile, 64, sdo, t > 0);           // dV += P^T dO
+            issue_tm<D>(tmem + kAccCol, tmem, 64, sdo, t > 0);  // dV += P^T dO
             mma_commit_e(&b.b_empty[i % C::kSlotsB]);
-            issue_tm<D>(tmem + kAccCol + D, tmem + kTile + 32, 64, sq, t > 0);   // dK += dS^T Q
+            if (more) {  // S^T(t+1) over P^T(t), which dV(t) has read
+                if (!ring_wait_w(b.a_full, i + 1, C::kSlotsA, wc)) { ok = false; break; }
+                tc_fence_after();
+                issue_kk<D>(tmem, sK, sA + ((i + 1) % C::kSlotsA) * C::kTileBytes);
+                mma_commit_e(b.s_full);
+            }
+            if (!mbar_wait_w(&b.ds_full[0], dsf & 1u, wc)) { ok = false; break; }
+            ++dsf;
+            tc_fence_after();
+            issue_tm<D>(tmem + kAccCol + D, tmem + kTile, 64, sq, t > 0);  // dK += dS^T Q
             mma_commit_e(&b.a_empty[i % C::kSlotsA]);
-            if (more) {
-                // dP^T(t+1) overwrites the P^T, dS^T columns the two products above read
+            if (more) {  // dP^T(t+1) over dS^T(t), which dK(t) has read
                 if (!ring_wait_w(b.b_full, i + 1, C::kSlotsB, wc)) { ok = false; break; }
                 tc_fence_after();
                 issue_kk<D>(tmem + kTile, sV, sB + ((i + 1) % C::kSlotsB) * C::kTileBytes);
@@ -680,48 +707,69 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
         int hk, kp;
         kv_item(p, item, hk, kp);
         const int kpos = kp + row;
+        // Each thread holds one of the warpgroup's 64 lse and 64 D values of a query tile
+        // (its 64 columns), fetched one step ahead so that the load's L2 latency hides
+        // behind a whole step instead of sitting on the chain to the next dS.
+        const float* ld_src = (row < 64 ? p.lse : p.delta) + h * 64 + (row & 63);
+        float mine_next = __ldg(ld_src + row_of(p, hk * R.g, R.S - kTile));
         for_each_query_tile(R, hk, kp, [&](int hq, int t0) -> bool {
-            const int qrow = row_of(p, hq, t0) + h * 64;  // my first query column's row in lse, delta
-            // each thread fetches one of the warpgroup's 64 lse and 64 D values now, so the
-            // load's latency hides behind the wait for S^T
-            const float mine = __ldg((row < 64 ? p.lse : p.delta) + qrow + (row & 63));
+            const float mine = mine_next;
+            int nhq, nt0;
+            if (next_query_tile(R, hk, kp, hq, t0, nhq, nt0)) mine_next = __ldg(ld_src + row_of(p, nhq, nt0));
             if (!group_wait(b.s_full, sf & 1u, h, wq, wc)) { ok = false; return false; }
             ++sf;
-            sld[row] = mine;  // every thread of the group is past its reads of the last tile
+            // staged as -lse log2(e) (the exponent's offset) and -D (the dS offset)
+            sld[row] = (row < 64) ? -mine * kLog2e : -mine;  // every thread is past its reads of the last tile
             group_sync(h);
             tc_fence_after();
             float x[64];
-            tmem_take64(s_tm, x, b.s_free);
+            tmem_ld64(s_tm, x);
             const int lo = kpos - (t0 + h * 64);  // my query columns [lo, 64) see my key
-            const bool mask = R.causal && lo > 0;
             const float4* l4 = reinterpret_cast<const float4*>(sld);
+            // only tiles on the diagonal mask; branch on the warp, not per element
+            if (__any_sync(0xffffffffu, R.causal && lo > 0)) {
+                const int lm = R.causal ? lo : 0;
 #pragma unroll
-            for (int i4 = 0; i4 < 16; ++i4) {
-                const float4 lv = l4[i4];
-                float p0, p1, p2, p3;
-                ffma2(p0, p1, x[4 * i4], x[4 * i4 + 1], kLog2e, kLog2e, -lv.x * kLog2e, -lv.y * kLog2e);
-                ffma2(p2, p3, x[4 * i4 + 2], x[4 * i4 + 3], kLog2e, kLog2e, -lv.z * kLog2e, -lv.w * kLog2e);
-                p0 = ex2(p0);
-                p1 = ex2(p1);
-                p2 = ex2(p2);
-                p3 = ex2(p3);
-                if (mask) {
+                for (int i4 = 0; i4 < 16; ++i4) {
+                    const float4 lv = l4[i4];
+                    float p0, p1, p2, p3;
+                    ffma2(p0, p1, x[4 * i4], x[4 * i4 + 1], kLog2e, kLog2e, lv.x, lv.y);
+                    ffma2(p2, p3, x[4 * i4 + 2], x[4 * i4 + 3], kLog2e, kLog2e, lv.z, lv.w);
                     const int i = 4 * i4;
-                    p0 = (i < lo) ? 0.f : p0;
-                    p1 = (i + 1 < lo) ? 0.f : p1;
-                    p2 = (i + 2 < lo) ? 0.f : p2;
-                    p3 = (i + 3 < lo) ? 0.f : p3;
+                    x[i] = (i < lm) ? 0.f : ex2(p0);
+                    x[i + 1] = (i + 1 < lm) ? 0.f : ex2(p1);
+                    x[i + 2] = (i + 2 < lm) ? 0.f : ex2(p2);
+                    x[i + 3] = (i + 3 < lm) ? 0.f : ex2(p3);
                 }
-                x[4 * i4] = p0;
-                x[4 * i4 + 1] = p1;
-                x[4 * i4 + 2] = p2;
-                x[4 * i4 + 3] = p3;
+            } else {
+#pragma unroll
+                for (int i4 = 0; i4 < 16; ++i4) {
+                    const float4 lv = l4[i4];
+                    float p0, p1, p2, p3;
+                    ffma2(p0, p1, x[4 * i4], x[4 * i4 + 1], kLog2e, kLog2e, lv.x, lv.y);
+                    ffma2(p2, p3, x[4 * i4 + 2], x[4 * i4 + 3], kLog2e, kLog2e, lv.z, lv.w);
+                    x[4 * i4] = ex2(p0);
+                    x[4 * i4 + 1] = ex2(p1);
+                    x[4 * i4 + 2] = ex2(p2);
+                    x[4 * i4 + 3] = ex2(p3);
+                }
+            }
+            {
+                // P^T (bf16) over the first 32 of my own S^T columns, whose values are in
+                // registers: dV(t) can start while dS^T is still being formed
+                uint32_t pp[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) pp[k] = pack_bf16x2(x[2 * k], x[2 * k + 1]);
+                tmem_st32(s_tm, pp);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(b.pt_full);
             }
             if (!group_wait(b.dp_full, dpf & 1u, h, wq, wc)) { ok = false; return false; }
             ++dpf;
             tc_fence_after();
             const float4* d4 = reinterpret_cast<const float4*>(sld + 64);
-            uint32_t pp[32], pd[32];
+            uint32_t pd[32];
             // dP^T in two 32-column chunks, each packed as soon as it is used, so that P, dP^T
             // and the packed words are never all live at once
 #pragma unroll
@@ -731,18 +779,18 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
                 tmem_wait_ld();
 #pragma unroll
                 for (int i4 = 0; i4 < 8; ++i4) {
-                    const float4 dv = d4[8 * c + i4];
+                    const float4 nd = d4[8 * c + i4];  // -D of four query columns
                     const int i = 32 * c + 4 * i4, k = 16 * c + 2 * i4;
-                    pp[k] = pack_bf16x2(x[i], x[i + 1]);
-                    pp[k + 1] = pack_bf16x2(x[i + 2], x[i + 3]);
-                    pd[k] = pack_bf16x2(x[i] * (__uint_as_float(r[4 * i4]) - dv.x),
-                                        x[i + 1] * (__uint_as_float(r[4 * i4 + 1]) - dv.y));
-                    pd[k + 1] = pack_bf16x2(x[i + 2] * (__uint_as_float(r[4 * i4 + 2]) - dv.z),
-                                            x[i + 3] * (__uint_as_float(r[4 * i4 + 3]) - dv.w));
+                    float a0, a1, a2, a3;
+                    fadd2(a0, a1, __uint_as_float(r[4 * i4]), __uint_as_float(r[4 * i4 + 1]), nd.x, nd.y);
+                    fadd2(a2, a3, __uint_as_float(r[4 * i4 + 2]), __uint_as_float(r[4 * i4 + 3]), nd.z, nd.w);
+                    fmul2(a0, a1, a0, a1, x[i], x[i + 1]);
+                    fmul2(a2, a3, a2, a3, x[i + 2], x[i + 3]);
+                    pd[k] = pack_bf16x2(a0, a1);
+                    pd[k + 1] = pack_bf16x2(a2, a3);
                 }
             }
-            tmem_st32(dp_tm, pp);       // P^T over the first 32 of my own dP^T columns
-            tmem_st32(dp_tm + 32, pd);  // dS^T over the other 32
+            tmem_st32(dp_tm, pd);  // dS^T over the first 32 of my own dP^T columns
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&b.ds_full[0]);
