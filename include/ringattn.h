@@ -42,6 +42,12 @@
  *    CUDA runtime call or launch failed.  Device-side waits are bounded; one that
  *    runs out records RA_ERR_TIMEOUT, read with ringattn_sync_status.  No exception
  *    crosses the ABI and there is no CPU fallback.
+ *  - Check build: the same sources compiled with -DRA_CHECK give libringattn_check.so,
+ *    the same ABI with an index check at every place a kernel derives a memory index
+ *    from the chunk and work-item arithmetic (TMA row coordinates, output rows, document
+ *    starts, source slabs and rows).  A failed check records RA_ERR_BOUNDS (read with
+ *    ringattn_sync_status) and the access is skipped, read as zero, or moved to row 0;
+ *    nothing traps.  The normal library never records RA_ERR_BOUNDS.
  *  - The library allocates no device memory per call; scratch it needs is passed in,
  *    except for ringattn_fwd_docmask_noalloc, which uses a static device array.
  *  - The first call of any entry point on a device performs the library's one-time
@@ -71,7 +77,8 @@ typedef enum {
     RA_ERR_UNSUPPORTED = -2,
     RA_ERR_ARCH = -3,
     RA_ERR_CUDA = -4,
-    RA_ERR_TIMEOUT = -5
+    RA_ERR_TIMEOUT = -5,
+    RA_ERR_BOUNDS = -6
 } ra_status;
 
 /*
@@ -342,8 +349,9 @@ int ringattn_rank_work(int S, int c, int causal, int layout, int tile, long long
 
 /*
  * ringattn_sync_status -- synchronise `stream`, then return RA_ERR_TIMEOUT if a
- * bounded device wait of any earlier call on the current device ran out (the record
- * is cleared), RA_ERR_CUDA if the synchronisation failed, else RA_OK.
+ * bounded device wait of any earlier call on the current device ran out, or (check
+ * build only) RA_ERR_BOUNDS if an index check failed; the record is cleared.  Returns
+ * RA_ERR_CUDA if the synchronisation failed, else RA_OK.
  */
 int ringattn_sync_status(ra_stream_t stream);
 
@@ -356,9 +364,11 @@ int ringattn_sync_status(ra_stream_t stream);
 int ringattn_selftest_timeout(long long timeout_ns, ra_stream_t stream);
 
 /*
- * ringattn_last_timeout -- host only.  Where the last timeout that ringattn_sync_status
- * reported happened: info[0] = shared-memory address of the barrier whose wait ran out,
- * info[1] = CTA index, info[2] = thread index within the CTA (all 0 if none yet).
+ * ringattn_last_timeout -- host only.  Where the last device error that
+ * ringattn_sync_status reported happened: info[0] = shared-memory address of the barrier
+ * whose wait ran out (RA_ERR_TIMEOUT) or the number of the index check that failed
+ * (RA_ERR_BOUNDS), info[1] = CTA index, info[2] = thread index within the CTA (all 0 if
+ * none yet).
  * info must hold 3 ints.  A diagnostic for reports; the values are not stable across
  * library versions.
  */

@@ -1,9 +1,13 @@
-"""Compile libringattn.so in-tree for sm_103a (nvcc, translation units in parallel).
+"""Compile libringattn.so and its check build in-tree for sm_103a (nvcc, every
+translation unit of both in parallel).
 
     python -m online_softmax_attention_zigzag_gb300.build [-v]
 
-Objects go to ``_build/`` at the repository root; the library lands next to this
-file, where the Python binding loads it.
+Objects go to ``_build/release`` and ``_build/check`` at the repository root; the
+libraries land next to this file, where the Python binding loads them:
+libringattn.so, and libringattn_check.so (-DRA_CHECK: the kernels check the memory
+indices they derive and record RA_ERR_BOUNDS instead of going out of bounds; the binding
+loads it when RINGATTN_CHECK=1).
 """
 from __future__ import annotations
 
@@ -19,6 +23,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libringattn.so")
+LIB_CHECK = os.path.join(PKG, "libringattn_check.so")  # -DRA_CHECK: index checks in the kernels
 SOURCES = ["api.cu", "attn_bf16.cu", "attn_f32.cu", "permute_merge.cu", "ulysses.cu", "attn_bwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -37,16 +42,28 @@ def _run(cmd):
     return r.returncode, r.stdout
 
 
-def build(verbose: bool = False) -> str:
-    nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
-    extra = ["-Xptxas", "-v"] if verbose else []
+def _objects(nvcc, variant, extra):
+    """(source, command, object) for every translation unit of one library variant."""
     jobs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD, variant, src.replace(".cu", ".o"))
         jobs.append((src, [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj], obj))
-    with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
-        results = list(ex.map(lambda j: (j[0], *_run(j[1])), jobs))
+    return jobs
+
+
+def build(verbose: bool = False) -> str:
+    """Compile libringattn.so and the check build libringattn_check.so (-DRA_CHECK: index
+    checks that record RA_ERR_BOUNDS), all translation units of both in parallel."""
+    nvcc = _nvcc()
+    extra = ["-Xptxas", "-v"] if verbose else []
+    variants = {"release": (LIB, []), "check": (LIB_CHECK, ["-DRA_CHECK"])}
+    jobs = {}
+    for name, (_, defs) in variants.items():
+        os.makedirs(os.path.join(BUILD, name), exist_ok=True)
+        jobs[name] = _objects(nvcc, name, [*defs, *extra])
+    flat = [j for js in jobs.values() for j in js]
+    with ThreadPoolExecutor(max_workers=len(flat)) as ex:
+        results = list(ex.map(lambda j: (j[0], *_run(j[1])), flat))
     failed = False
     for src, rc, out in results:
         if rc != 0 or verbose:
@@ -54,12 +71,13 @@ def build(verbose: bool = False) -> str:
         failed |= rc != 0
     if failed:
         raise RuntimeError("nvcc failed")
-    tmp = LIB + ".tmp"
-    rc, out = _run([nvcc, *ARCH, "-shared", "-o", tmp, *[j[2] for j in jobs]])
-    if rc != 0:
-        sys.stdout.write(out)
-        raise RuntimeError("link failed")
-    os.replace(tmp, LIB)
+    for name, (lib, _) in variants.items():
+        tmp = lib + ".tmp"
+        rc, out = _run([nvcc, *ARCH, "-shared", "-o", tmp, *[j[2] for j in jobs[name]]])
+        if rc != 0:
+            sys.stdout.write(out)
+            raise RuntimeError("link failed")
+        os.replace(tmp, lib)
     return LIB
 
 

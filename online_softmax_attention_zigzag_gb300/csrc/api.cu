@@ -261,6 +261,7 @@ int fwd_f32(const float* q, const float* k, const float* v, float* out, float* l
     ra::AttnF32Params p;
     p.ring = R;
     p.kv_block = kv_block;
+    p.err = dev->err;
     p.q = q;
     p.k = k;
     p.v = v;
@@ -507,7 +508,8 @@ int ringattn_relayout(const void* src, void* dst, int S, int H, int row_bytes, i
     DeviceInfo* dev = nullptr;
     int st = device_info(&dev);
     if (st != RA_OK) return st;
-    return ra::launch_relayout(src, dst, S, H, row_bytes, c, layout, to_heads, reinterpret_cast<cudaStream_t>(stream));
+    return ra::launch_relayout(src, dst, S, H, row_bytes, c, layout, to_heads, dev->err,
+                               reinterpret_cast<cudaStream_t>(stream));
 }
 
 int ringattn_ulysses_fwd(const void* q_seq, const void* k_seq, const void* v_seq, float* out_seq, float* lse_seq,
@@ -541,15 +543,15 @@ int ringattn_ulysses_fwd(const void* q_seq, const void* k_seq, const void* v_seq
     float* oh = reinterpret_cast<float*>(ws + off[3]);
     float* lh = reinterpret_cast<float*>(ws + off[4]);
     // all-to-all: sequence shards -> head shards
-    if (ra::launch_relayout(q_seq, qh, S, Hq, 2 * d, c, layout, 1, s) != 0 ||
-        ra::launch_relayout(k_seq, kh, S, Hkv, 2 * d, c, layout, 1, s) != 0 ||
-        ra::launch_relayout(v_seq, vh, S, Hkv, 2 * d, c, layout, 1, s) != 0)
+    if (ra::launch_relayout(q_seq, qh, S, Hq, 2 * d, c, layout, 1, dev->err, s) != 0 ||
+        ra::launch_relayout(k_seq, kh, S, Hkv, 2 * d, c, layout, 1, dev->err, s) != 0 ||
+        ra::launch_relayout(v_seq, vh, S, Hkv, 2 * d, c, layout, 1, dev->err, s) != 0)
         return RA_ERR_CUDA;
     // local attention of every rank's heads over the whole sequence, one launch for all ranks
     if ((st = fwd_bf16(qh, kh, vh, oh, lh, S, Hq, Hkv, d, 1, causal, 0, S, 1, -1, 0, -1, s)) != RA_OK) return st;
     // all-to-all back: head shards -> sequence shards
-    if (ra::launch_relayout(oh, out_seq, S, Hq, 4 * d, c, layout, 0, s) != 0 ||
-        ra::launch_relayout(lh, lse_seq, S, Hq, 4, c, layout, 0, s) != 0)
+    if (ra::launch_relayout(oh, out_seq, S, Hq, 4 * d, c, layout, 0, dev->err, s) != 0 ||
+        ra::launch_relayout(lh, lse_seq, S, Hq, 4, c, layout, 0, dev->err, s) != 0)
         return RA_ERR_CUDA;
     return RA_OK;
 }
@@ -674,7 +676,8 @@ int ringattn_permute(const void* src, void* dst, int S, int H, int row_bytes, in
     DeviceInfo* dev = nullptr;
     int st = device_info(&dev);
     if (st != RA_OK) return st;
-    return ra::launch_permute(src, dst, S, H, row_bytes, c, layout, inverse, reinterpret_cast<cudaStream_t>(stream));
+    return ra::launch_permute(src, dst, S, H, row_bytes, c, layout, inverse, dev->err,
+                              reinterpret_cast<cudaStream_t>(stream));
 }
 
 int ringattn_rank_work(int S, int c, int causal, int layout, int tile, long long* units, long long* pairs,
@@ -732,7 +735,8 @@ int ringattn_sync_status(ra_stream_t stream) {
         }
         const int zero[4] = {0, 0, 0, 0};
         if (cudaMemcpy(dev->err, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return RA_ERR_CUDA;
-        return RA_ERR_TIMEOUT;
+        // a bounded wait that ran out, or (check build) an index check that failed
+        return rec[0] == RA_ERR_BOUNDS ? RA_ERR_BOUNDS : RA_ERR_TIMEOUT;
     }
     return RA_OK;
 }
@@ -763,6 +767,7 @@ const char* ringattn_strerror(int status) {
         case RA_ERR_ARCH: return "current device is not compute capability 10.3 (sm_103)";
         case RA_ERR_CUDA: return "CUDA runtime error";
         case RA_ERR_TIMEOUT: return "a bounded device wait ran out";
+        case RA_ERR_BOUNDS: return "a device index check failed (check build)";
         default: return "unknown status";
     }
 }

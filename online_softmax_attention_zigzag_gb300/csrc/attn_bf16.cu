@@ -168,7 +168,10 @@ __device__ __forceinline__ void decode_item(const AttnBf16Params& p, int item, I
     it.pmax = max(it.pos[0], it.pos[1]) + kTile - 1;
     // document mask: no key before the start of the document of the item's first row is
     // visible to any of its rows (starts do not decrease along the sequence)
-    it.klo = DOC ? (__ldg(p.doc_start + min(it.pos[0], it.pos[1])) / kTile) * kTile : 0;
+    const int p0 = min(it.pos[0], it.pos[1]);
+    it.klo = (DOC && RA_CHECKED(p0 >= 0 && p0 < R.S, p.err, kSiteFwdDocStart))
+                 ? (__ldg(p.doc_start + p0) / kTile) * kTile
+                 : 0;
 }
 
 // Row of natural key position pos of KV head hk in k / v (rank-major unless p.natural).
@@ -265,6 +268,9 @@ __device__ void load_role(const AttnBf16Params& p, const CUtensorMap* tq, const 
         return true;
     };
     auto load_tile = [&](uint32_t s, int off, const CUtensorMap* map, int row) {
+        if (!RA_CHECKED(row >= 0 && static_cast<long long>(row) + kTile <= static_cast<long long>(p.ring.Hkv) * p.ring.S,
+                        p.err, kSiteFwdKvRow))
+            row = 0;
         for (int bx = 0; bx < C::kBoxes; ++bx)
             tma_load_2d_hint(sKV + s * C::kStageBytes + off + bx * C::kBoxBytes, map, &b.kv_full[s], bx * 64, row,
                              keep);
@@ -284,7 +290,10 @@ __device__ void load_role(const AttnBf16Params& p, const CUtensorMap* tq, const 
             if (!mbar_wait(&b.q_empty[x], (qit[x] & 1u) ^ 1u, wc, 32)) { ok = false; break; }
             ++qit[x];
             mbar_arrive_expect_tx(&b.q_full[x], C::kTileBytes);
-            const int qrow = x ? it.qrow[1] : it.qrow[0];
+            int qrow = x ? it.qrow[1] : it.qrow[0];
+            if (!RA_CHECKED(qrow >= 0 && static_cast<long long>(qrow) + kTile <= static_cast<long long>(p.ring.Hq) * p.ring.S,
+                            p.err, kSiteFwdQRow))
+                qrow = 0;
 #pragma unroll
             for (int bx = 0; bx < C::kBoxes; ++bx)
                 tma_load_2d_hint(sQ + x * C::kTileBytes + bx * C::kBoxBytes, tq, &b.q_full[x], bx * 64, qrow, stream);
@@ -541,16 +550,22 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
         const int nj = count_kv_tiles<DOC>(p, it);
         const size_t grow = static_cast<size_t>((x ? it.qrow[1] : it.qrow[0]) + row);
         float* orow = p.out + grow * D;
+        const bool row_ok =
+            RA_CHECKED(grow < static_cast<size_t>(p.ring.Hq) * p.ring.S, p.err, kSiteFwdOutRow);
         if (nj == 0) {  // a message with no visible key for this tile
-            float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (row_ok) {
+                float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int i = 0; i < D / 4; ++i) reinterpret_cast<float4*>(orow)[i] = z;
-            p.lse[grow] = -INFINITY;
+                for (int i = 0; i < D / 4; ++i) reinterpret_cast<float4*>(orow)[i] = z;
+                p.lse[grow] = -INFINITY;
+            }
             continue;
         }
         const int tpos = x ? it.pos[1] : it.pos[0];
         const int qpos = tpos + row;
-        const int doc_lo = DOC ? __ldg(p.doc_start + qpos) : 0;  // first key of my document
+        // first key of my document
+        const int doc_lo =
+            (DOC && RA_CHECKED(qpos >= 0 && qpos < p.ring.S, p.err, kSiteFwdDocStart)) ? __ldg(p.doc_start + qpos) : 0;
         // l: sum of the exact p (for lse); lr: sum of p as rounded to bf16 for the P V
         // product, so that out = O / lr weighs every key consistently (a key that
         // dominates the row then comes out exactly, whatever its rounding)
@@ -692,6 +707,7 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
         mbar_arrive(&b.o_free[x]);
 #pragma unroll
         for (int i = 0; i < D; ++i) o[i] *= inv;
+        if (!row_ok) continue;
         if ((reinterpret_cast<uintptr_t>(p.out) & 31u) == 0u) {
 #pragma unroll
             for (int i = 0; i < D; i += 8) {

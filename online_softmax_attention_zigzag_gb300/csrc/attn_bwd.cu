@@ -88,6 +88,14 @@ __device__ __forceinline__ int row_of(const AttnBwdParams& p, int head, int pos)
     return head * R.S + s * R.n_r + (second ? R.m : 0) + (pos - k * R.m);
 }
 
+// A 128-row tile of a [heads * S, d] tensor starting at `row` (check build: a row outside the
+// tensor is recorded and replaced by row 0).
+__device__ __forceinline__ int checked_tile_row(int row, int heads, const Ring& R, int* err, int site) {
+    if (!RA_CHECKED(row >= 0 && static_cast<long long>(row) + kTile <= static_cast<long long>(heads) * R.S, err, site))
+        return 0;
+    return row;
+}
+
 __device__ __forceinline__ int rank_of(const Ring& R, int pos) {
     const int k = pos / R.m;
     return (R.layout == 1 && k >= R.c) ? 2 * R.c - 1 - k : k;
@@ -356,12 +364,12 @@ __device__ void dq_load(const AttnBwdParams& p, const CUtensorMap* tq, const CUt
         if (!mbar_wait(b.res_empty, (qit & 1u) ^ 1u, wc, 32)) { ok = false; break; }
         ++qit;
         mbar_arrive_expect_tx(b.res_full, 2 * C::kTileBytes);
-        const int qrow = row_of(p, hq, qp);
+        const int qrow = checked_tile_row(row_of(p, hq, qp), R.Hq, R, p.err, kSiteBwdQRow);
         load_tile<D>(smem, tq, b.res_full, qrow, stream);
         load_tile<D>(smem + C::kTileBytes, tdo, b.res_full, qrow, stream);
         const int hk = hq / R.g;
         for_each_key_tile(R, qp, [&](int t0) -> bool {
-            const int krow = row_of(p, hk, t0);
+            const int krow = checked_tile_row(row_of(p, hk, t0), R.Hkv, R, p.err, kSiteBwdKvRow);
             if (!ring_load<D>(smem + C::kAOff, b.a_full, b.a_empty, ka, C::kSlotsA, tk, krow, keep, wc) ||
                 !ring_load<D>(smem + C::kBOff, b.b_full, b.b_empty, vb, C::kSlotsB, tv, krow, keep, wc)) {
                 ok = false;
@@ -504,8 +512,9 @@ __device__ void dq_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
         int hq, qp;
         dq_item(p, item, hq, qp);
         const int grow = row_of(p, hq, qp) + row;
-        const float nl = -__ldg(p.lse + grow) * kLog2e;
-        const float dl = __ldg(p.delta + grow);
+        const bool row_ok = RA_CHECKED(grow >= 0 && grow < R.Hq * R.S, p.err, kSiteBwdLseRow);
+        const float nl = row_ok ? -__ldg(p.lse + grow) * kLog2e : 0.f;
+        const float dl = row_ok ? __ldg(p.delta + grow) : 0.f;
         const int qpos = qp + row;
         uint32_t jj = 0;  // tile within the item
         for_each_key_tile(R, qp, [&](int t0) -> bool {
@@ -562,7 +571,8 @@ __device__ void dq_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
         if (!warp_wait(b.acc_done, it & 1u, wc)) { ok = false; break; }
         ++it;
         tc_fence_after();
-        store_acc<D / 2>(acc_tm, p.dq + static_cast<size_t>(grow) * D + h * (D / 2));
+        if (RA_CHECKED(row_ok, p.err, kSiteBwdGradRow))
+            store_acc<D / 2>(acc_tm, p.dq + static_cast<size_t>(grow) * D + h * (D / 2));
         tc_fence_before();
         mbar_arrive(b.acc_free);
     }
@@ -588,11 +598,11 @@ __device__ void kv_load(const AttnBwdParams& p, const CUtensorMap* tq, const CUt
         if (!mbar_wait(b.res_empty, (kit & 1u) ^ 1u, wc, 32)) { ok = false; break; }
         ++kit;
         mbar_arrive_expect_tx(b.res_full, 2 * C::kTileBytes);
-        const int krow = row_of(p, hk, kp);
+        const int krow = checked_tile_row(row_of(p, hk, kp), R.Hkv, R, p.err, kSiteBwdKvRow);
         load_tile<D>(smem, tk, b.res_full, krow, stream);
         load_tile<D>(smem + C::kTileBytes, tv, b.res_full, krow, stream);
         for_each_query_tile(R, hk, kp, [&](int hq, int t0) -> bool {
-            const int qrow = row_of(p, hq, t0);
+            const int qrow = checked_tile_row(row_of(p, hq, t0), R.Hq, R, p.err, kSiteBwdQRow);
             if (!ring_load<D>(smem + C::kAOff, b.a_full, b.a_empty, qa, C::kSlotsA, tq, qrow, keep, wc) ||
                 !ring_load<D>(smem + C::kBOff, b.b_full, b.b_empty, ob, C::kSlotsB, tdo, qrow, keep, wc)) {
                 ok = false;
@@ -711,11 +721,18 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
         // (its 64 columns), fetched one step ahead so that the load's L2 latency hides
         // behind a whole step instead of sitting on the chain to the next dS.
         const float* ld_src = (row < 64 ? p.lse : p.delta) + h * 64 + (row & 63);
-        float mine_next = __ldg(ld_src + row_of(p, hk * R.g, R.S - kTile));
+        auto fetch = [&](int hq, int t0) -> float {
+            const int r0 = row_of(p, hq, t0);  // first row of the query tile
+            return RA_CHECKED(r0 >= 0 && static_cast<long long>(r0) + kTile <= static_cast<long long>(R.Hq) * R.S, p.err,
+                              kSiteBwdLseRow)
+                       ? __ldg(ld_src + r0)
+                       : 0.f;
+        };
+        float mine_next = fetch(hk * R.g, R.S - kTile);
         for_each_query_tile(R, hk, kp, [&](int hq, int t0) -> bool {
             const float mine = mine_next;
             int nhq, nt0;
-            if (next_query_tile(R, hk, kp, hq, t0, nhq, nt0)) mine_next = __ldg(ld_src + row_of(p, nhq, nt0));
+            if (next_query_tile(R, hk, kp, hq, t0, nhq, nt0)) mine_next = fetch(nhq, nt0);
             if (!group_wait(b.s_full, sf & 1u, h, wq, wc)) { ok = false; return false; }
             ++sf;
             // staged as -lse log2(e) (the exponent's offset) and -D (the dS offset)
@@ -801,8 +818,10 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
         ++it;
         tc_fence_after();
         const size_t grow = static_cast<size_t>(row_of(p, hk, kp) + row);
-        store_acc<D / 2>(dv_tm, p.dv + grow * D + h * (D / 2));
-        store_acc<D / 2>(dk_tm, p.dk + grow * D + h * (D / 2));
+        if (RA_CHECKED(grow < static_cast<size_t>(R.Hkv) * R.S, p.err, kSiteBwdGradRow)) {
+            store_acc<D / 2>(dv_tm, p.dv + grow * D + h * (D / 2));
+            store_acc<D / 2>(dk_tm, p.dk + grow * D + h * (D / 2));
+        }
         tc_fence_before();
         mbar_arrive(b.acc_free);
     }

@@ -42,10 +42,11 @@ __global__ void __launch_bounds__(kRows) attn_f32_kernel(const AttnF32Params p) 
     }
     const size_t qrow = static_cast<size_t>(h) * R.S + static_cast<size_t>(r) * R.n_r + (active ? local : 0);
 
+    const bool row_ok = !active || RA_CHECKED(qrow < static_cast<size_t>(R.Hq) * R.S, p.err, kSiteF32Row);
     float q[DP], o[DP];
 #pragma unroll
     for (int t = 0; t < DP; ++t) {
-        q[t] = (active && t < d) ? p.q[qrow * d + t] : 0.f;
+        q[t] = (active && row_ok && t < d) ? p.q[qrow * d + t] : 0.f;
         o[t] = 0.f;
     }
     float run_max = -INFINITY, run_sum = 0.f;
@@ -66,7 +67,9 @@ __global__ void __launch_bounds__(kRows) attn_f32_kernel(const AttnF32Params p) 
                 __syncthreads();
                 for (int e = threadIdx.x; e < nk * DP; e += kRows) {
                     const int kr = e / DP, t = e % DP;
-                    sk[kr][t] = (t < d) ? p.k[(kv_base + k0 + kr) * d + t] : 0.f;
+                    const size_t kvr = kv_base + k0 + kr;
+                    const bool ok = RA_CHECKED(kvr < static_cast<size_t>(R.Hkv) * R.S, p.err, kSiteF32Row);
+                    sk[kr][t] = (t < d && ok) ? p.k[kvr * d + t] : 0.f;
                 }
                 __syncthreads();
                 for (int kr = 0; kr < nk; ++kr) {
@@ -94,9 +97,11 @@ __global__ void __launch_bounds__(kRows) attn_f32_kernel(const AttnF32Params p) 
                 __syncthreads();
                 for (int e = threadIdx.x; e < nk * DP; e += kRows) {
                     const int kr = e / DP, t = e % DP;
-                    const size_t off = (kv_base + k0 + kr) * d + t;
-                    sk[kr][t] = (t < d) ? p.k[off] : 0.f;
-                    sv[kr][t] = (t < d) ? p.v[off] : 0.f;
+                    const size_t kvr = kv_base + k0 + kr;
+                    const bool ok = RA_CHECKED(kvr < static_cast<size_t>(R.Hkv) * R.S, p.err, kSiteF32Row);
+                    const size_t off = kvr * d + t;
+                    sk[kr][t] = (t < d && ok) ? p.k[off] : 0.f;
+                    sv[kr][t] = (t < d && ok) ? p.v[off] : 0.f;
                 }
                 __syncthreads();
                 if (!visible) continue;
@@ -117,7 +122,7 @@ __global__ void __launch_bounds__(kRows) attn_f32_kernel(const AttnF32Params p) 
             run_max = new_max;
         }
     }
-    if (!active) return;
+    if (!active || !row_ok) return;
     const bool seen = run_sum > 0.f;
     const float inv = seen ? 1.f / run_sum : 0.f;
     for (int t = 0; t < d; ++t) p.out[qrow * d + t] = o[t] * inv;

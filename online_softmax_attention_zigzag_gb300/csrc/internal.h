@@ -7,6 +7,37 @@
 
 namespace ra {
 
+// ------------------------------------------------------------------ check build
+// Index checks of the check build (compiled with -DRA_CHECK, libringattn_check.so): at every
+// site where a kernel derives a memory index from the ring's chunk and work-item arithmetic
+// (TMA row coordinates, output rows, document starts, source slabs), the index is checked
+// against the tensor it addresses.  A failed check records RA_ERR_BOUNDS and the site
+// number in the device error word (read with ringattn_sync_status / ringattn_last_timeout)
+// and the access is skipped (a store), read as zero (a load) or moved to row 0 (a TMA load,
+// so the pipeline's byte counts still complete); nothing traps.  In the normal build
+// RA_CHECKED(cond, err, site) is `true` and the condition is not evaluated.
+constexpr int kErrBounds = -6;  // RA_ERR_BOUNDS
+enum CheckSite : int {
+    kSiteFwdQRow = 1, kSiteFwdKvRow = 2, kSiteFwdOutRow = 3, kSiteFwdDocStart = 4,
+    kSiteBwdQRow = 11, kSiteBwdKvRow = 12, kSiteBwdLseRow = 13, kSiteBwdGradRow = 14,
+    kSitePermuteSlab = 21, kSiteRelayoutSrc = 31, kSiteF32Row = 41
+};
+#if defined(__CUDACC__) && defined(RA_CHECK)
+__device__ __forceinline__ bool ra_check(bool ok, int* err, int site) {
+    if (!ok && err) {
+        atomicCAS(err, 0, kErrBounds);
+        if (atomicCAS(err + 1, 0, 1) == 0) {
+            err[2] = site;
+            err[3] = static_cast<int>((blockIdx.x << 10) | threadIdx.x);
+        }
+    }
+    return ok;
+}
+#define RA_CHECKED(cond, err, site) ::ra::ra_check((cond), (err), (site))
+#else
+#define RA_CHECKED(cond, err, site) true
+#endif
+
 // Ring geometry, fixed per call.
 //   n_r  rows per rank (S / c);  m  rows per chunk (n_r, or n_r / 2 for zigzag);
 //   nslot chunks per rank (1 or 2).  A rank's local row x lies in chunk slot x / m;
@@ -67,6 +98,7 @@ struct AttnBwdParams {
 struct AttnF32Params {
     Ring ring;
     int kv_block;
+    int* err;  // device error word (check build)
     const float* q;
     const float* k;
     const float* v;
@@ -78,7 +110,7 @@ int launch_attn_bf16(const AttnBf16Params& p, const CUtensorMap& tq, const CUten
                      const CUtensorMap& tv, int grid, cudaStream_t stream);
 int launch_attn_f32(const AttnF32Params& p, cudaStream_t stream);
 int launch_permute(const void* src, void* dst, int S, int H, int row_bytes, int c, int layout, int inverse,
-                   cudaStream_t stream);
+                   int* err, cudaStream_t stream);
 int launch_merge(float* o_run, float* lse_run, const float* o_part, const float* lse_part, long long rows,
                  int d, cudaStream_t stream);
 int launch_selftest_timeout(int* err, unsigned long long timeout_ns, cudaStream_t stream);
@@ -87,7 +119,7 @@ int launch_doc_start(const int* doc_id, int* doc_start, int S, cudaStream_t stre
 // head-sharded [H, S, row] (natural tokens); relayout_fits checks the index ranges.
 bool relayout_fits(long long S, int H, int row_bytes, int c, int layout);
 int launch_relayout(const void* src, void* dst, int S, int H, int row_bytes, int c, int layout, int to_heads,
-                    cudaStream_t stream);
+                    int* err, cudaStream_t stream);
 
 int launch_attn_bwd(const AttnBwdParams& p, const float* out, const void* dout, const CUtensorMap& tq,
                     const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo, int sms,

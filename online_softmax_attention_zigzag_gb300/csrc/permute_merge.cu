@@ -20,7 +20,7 @@ namespace {
 template <typename V>
 __global__ void __launch_bounds__(256) permute_kernel(const V* __restrict__ src, V* __restrict__ dst,
                                                       long long slab_vecs, int nchunks, int c, int layout,
-                                                      int inverse, long long nslabs) {
+                                                      int inverse, long long nslabs, int* err) {
     constexpr int kUnroll = 4;
     const long long slab = static_cast<long long>(blockIdx.z) * gridDim.y + blockIdx.y;
     if (slab >= nslabs) return;
@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(256) permute_kernel(const V* __restrict__ src,
     } else {
         sslab = dslab;
     }
+    if (!RA_CHECKED(sslab >= 0 && sslab < nchunks, err, kSitePermuteSlab)) return;
     const V* sp = src + (h * nchunks + sslab) * slab_vecs;
     V* dp = dst + slab * slab_vecs;
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -60,7 +61,7 @@ __global__ void __launch_bounds__(256) permute_kernel(const V* __restrict__ src,
 
 template <typename V>
 int launch_permute_v(const void* src, void* dst, long long slab_bytes, int H, int nchunks, int c, int layout,
-                     int inverse, cudaStream_t stream) {
+                     int inverse, int* err, cudaStream_t stream) {
     const long long slab_vecs = slab_bytes / static_cast<long long>(sizeof(V));
     const long long nslabs = static_cast<long long>(H) * nchunks;
     if (slab_vecs == 0 || nslabs == 0) return 0;
@@ -78,7 +79,7 @@ int launch_permute_v(const void* src, void* dst, long long slab_bytes, int H, in
     if (gz > 65535) return -2;
     dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(gy), static_cast<unsigned>(gz));
     permute_kernel<V><<<grid, 256, 0, stream>>>(static_cast<const V*>(src), static_cast<V*>(dst), slab_vecs, nchunks,
-                                               c, layout, inverse, nslabs);
+                                               c, layout, inverse, nslabs, err);
     return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
@@ -202,16 +203,16 @@ __global__ void selftest_timeout_kernel(int* err, unsigned long long timeout_ns)
 }  // namespace
 
 int launch_permute(const void* src, void* dst, int S, int H, int row_bytes, int c, int layout, int inverse,
-                   cudaStream_t stream) {
+                   int* err, cudaStream_t stream) {
     const int nchunks = c * (layout == 1 ? 2 : 1);
     const long long slab = static_cast<long long>(S / nchunks) * row_bytes;
     const uintptr_t align = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst) |
                             static_cast<uintptr_t>(slab);
-    if ((align & 15) == 0) return launch_permute_v<uint4>(src, dst, slab, H, nchunks, c, layout, inverse, stream);
-    if ((align & 7) == 0) return launch_permute_v<uint2>(src, dst, slab, H, nchunks, c, layout, inverse, stream);
-    if ((align & 3) == 0) return launch_permute_v<uint32_t>(src, dst, slab, H, nchunks, c, layout, inverse, stream);
-    if ((align & 1) == 0) return launch_permute_v<uint16_t>(src, dst, slab, H, nchunks, c, layout, inverse, stream);
-    return launch_permute_v<uint8_t>(src, dst, slab, H, nchunks, c, layout, inverse, stream);
+    if ((align & 15) == 0) return launch_permute_v<uint4>(src, dst, slab, H, nchunks, c, layout, inverse, err, stream);
+    if ((align & 7) == 0) return launch_permute_v<uint2>(src, dst, slab, H, nchunks, c, layout, inverse, err, stream);
+    if ((align & 3) == 0) return launch_permute_v<uint32_t>(src, dst, slab, H, nchunks, c, layout, inverse, err, stream);
+    if ((align & 1) == 0) return launch_permute_v<uint16_t>(src, dst, slab, H, nchunks, c, layout, inverse, err, stream);
+    return launch_permute_v<uint8_t>(src, dst, slab, H, nchunks, c, layout, inverse, err, stream);
 }
 
 int launch_merge(float* o_run, float* lse_run, const float* o_part, const float* lse_part, long long rows, int d,

@@ -31,6 +31,8 @@ struct RelayoutArgs {
     unsigned slab_vecs;   // vectors per destination slab
     FastDiv div_rowv;     // by rowv
     FastDiv div_hrow;     // by H * rowv
+    long long total_vecs; // vectors in the source tensor (check build)
+    int* err;             // device error word (check build)
 };
 
 // Rank-major token index of the first token of natural chunk k.
@@ -84,8 +86,10 @@ __global__ void __launch_bounds__(256) relayout_kernel(const V* __restrict__ src
                     const unsigned v = rem - hh * a.rowv;
                     s = (static_cast<long long>(hh) * a.S + src_tok + row) * a.rowv + v;
                 }
-                vals[u] = src[s];
-                dsto[u] = dst_base + i;
+                if (RA_CHECKED(s >= 0 && s < a.total_vecs, a.err, kSiteRelayoutSrc)) {
+                    vals[u] = src[s];
+                    dsto[u] = dst_base + i;
+                }
             }
         }
 #pragma unroll
@@ -123,7 +127,7 @@ bool relayout_fits(long long S, int H, int row_bytes, int c, int layout) {
 }
 
 int launch_relayout(const void* src, void* dst, int S, int H, int row_bytes, int c, int layout, int to_heads,
-                    cudaStream_t stream) {
+                    int* err, cudaStream_t stream) {
     const bool vec16 = row_bytes % 16 == 0 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0 &&
                        (reinterpret_cast<uintptr_t>(dst) & 15u) == 0;
     RelayoutArgs a;
@@ -141,6 +145,8 @@ int launch_relayout(const void* src, void* dst, int S, int H, int row_bytes, int
                                                  : static_cast<long long>(a.m) * H * a.rowv);
     a.div_rowv = make_fastdiv(static_cast<unsigned>(a.rowv));
     a.div_hrow = make_fastdiv(static_cast<unsigned>(H * a.rowv));
+    a.total_vecs = static_cast<long long>(S) * H * a.rowv;
+    a.err = err;
     if (a.slab_vecs == 0) return 0;
     return vec16 ? launch_relayout_v<uint4>(src, dst, a, stream) : launch_relayout_v<uint32_t>(src, dst, a, stream);
 }

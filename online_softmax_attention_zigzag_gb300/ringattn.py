@@ -16,7 +16,10 @@ import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libringattn.so")
+# RINGATTN_CHECK=1 loads the check build (index checks in the kernels, RA_ERR_BOUNDS);
+# same ABI, same results
+LIB_PATH = os.path.join(_PKG, "libringattn_check.so" if os.environ.get("RINGATTN_CHECK") == "1"
+                        else "libringattn.so")
 
 RA_OK = 0
 RA_ERR_INVALID_ARG = -1
@@ -24,6 +27,7 @@ RA_ERR_UNSUPPORTED = -2
 RA_ERR_ARCH = -3
 RA_ERR_CUDA = -4
 RA_ERR_TIMEOUT = -5
+RA_ERR_BOUNDS = -6
 
 EXPORTS = (
     "ringattn_fwd", "ringattn_fwd_natural", "ringattn_fwd_f32", "ringattn_fwd_hop",

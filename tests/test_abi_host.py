@@ -38,8 +38,19 @@ def test_library_exports_every_declared_symbol(ra):
     assert set(ra.EXPORTS) == declared
 
 
+def test_check_build_exports_the_same_symbols(ra):
+    """libringattn_check.so (compiled with -DRA_CHECK) is the same ABI."""
+    path = os.path.join(os.path.dirname(ra.LIB_PATH), "libringattn_check.so")
+    assert os.path.exists(path), "build() makes the check build too"
+    L = ctypes.CDLL(path)
+    for name in _declared():
+        assert hasattr(L, name), name
+    L.ringattn_strerror.restype = ctypes.c_char_p
+    assert b"index check" in L.ringattn_strerror(-6)
+
+
 def test_strerror(ra):
-    for code in (0, -1, -2, -3, -4, -5):
+    for code in (0, -1, -2, -3, -4, -5, -6):
         assert ra.strerror(code) not in ("", "unknown status")
     assert ra.strerror(12345) == "unknown status"
 
