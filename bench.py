@@ -222,6 +222,24 @@ def max_over_ranks(values, dist, device):
     return t.tolist()
 
 
+# Dense bf16 tensor work per SM per clock: one 128x128x16 tcgen05.mma (2*128*128*16 FLOP)
+# every 64 cycles, measured on this GPU with a single-SM stream of MMAs.
+TENSOR_FLOP_PER_CLK_PER_SM = 8192
+
+
+def clock_ceiling(achieved_tflops, clk, device):
+    """The kernel's fraction of the tensor ceiling at the SM clock seen during the timed
+    region (SMs x 8192 FLOP/clk x median SM MHz), beside the cuBLAS-burst fraction."""
+    mhz = clk.get("sm_mhz") if clk else None
+    if not mhz:
+        return {"clock_ceiling": None, "frac_of_clock_ceiling": None}
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    ceil_tf = sms * TENSOR_FLOP_PER_CLK_PER_SM * mhz * 1e6 / 1e12
+    return {"clock_ceiling": ceil_tf, "frac_of_clock_ceiling": achieved_tflops / ceil_tf,
+            "clock_ceiling_how": f"{sms} SMs x {TENSOR_FLOP_PER_CLK_PER_SM} FLOP/clk x {mhz:.0f} MHz (median SM clock "
+                                 "in the timed region)"}
+
+
 def whole_job_value(flop_per_step: float, world: int, ms_per_step: float) -> float:
     """TFLOP/s of all replicas together: every rank runs one step of the workload."""
     return world * flop_per_step / (ms_per_step * 1e-3) / 1e12
@@ -625,7 +643,8 @@ def main():
                          "kernel": "attn_bf16_kernel<%d, false>" % w.d, "kernel_ms": attn_ms,
                          "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
                          "frac_of_sustained": (achieved / bf16_sust) if bf16_sust else None,
-                         "nominal_peak": NOMINAL_BF16_TFLOPS, "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS},
+                         "nominal_peak": NOMINAL_BF16_TFLOPS, "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS,
+                         **clock_ceiling(achieved, clk, dev)},
             "natural_step": {"ms_per_step": nat_ms, "value": flop / (nat_ms * 1e-3) / 1e12, "unit": UNIT,
                              "what": "ringattn_fwd_natural: chunk map in TMA addressing, no permutation passes"},
             "also_measured": extra,
