@@ -18,7 +18,6 @@ of that threshold, so the inputs here are built to:
 
 A small random part on the other features keeps the rows distinct; V is N(0, 1).
 """
-import numpy as np
 import pytest
 import torch
 
