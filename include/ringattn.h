@@ -178,9 +178,11 @@ int ringattn_fwd_docmask_noalloc(const void* q, const void* k, const void* v, fl
  * computes, and copies out and lse back, with the copies overlapped with the attention.
  * The computation is that of ringattn_fwd_natural (same sources, same result); the KV
  * heads are split into G groups (G divides Hkv, at most 16, each group at least four
- * waves of work items), and while group g computes on `stream`, the inputs of later
- * groups travel host->device and the results of earlier groups device->host, on two
- * streams the library creates once per device and keeps until exit.
+ * waves of work items), and while group g computes, the inputs of later groups travel
+ * host->device and the results of earlier groups device->host.  The launches alternate
+ * between `stream` and a compute stream of the library's, so that one group's CTAs start
+ * on the SMs the previous group's last CTAs leave; the library creates its streams (one
+ * per copy direction and that compute stream) once per device and keeps them until exit.
  * q_h, k_h, v_h: HOST [Hq|Hkv, S, d] bf16, natural order.  out_h: HOST [Hq, S, d] fp32,
  *     lse_h: HOST [Hq, S] fp32, natural order.  Page-locked memory (cudaHostAlloc or
  *     cudaHostRegister) is needed for the copies to run asynchronously and overlap;

@@ -273,14 +273,17 @@ int fwd_f32(const float* q, const float* k, const float* v, float* out, float* l
 // ------------------------------------------------------------------ host-buffer path
 // ringattn_fwd_host runs the natural-order kernel once per group of KV heads, so that the
 // copies of one group overlap the attention of another: H2D of group g+1 and D2H of group
-// g-1 run on two internal streams (one per copy direction) while group g computes on the
-// caller's stream.  Streams and events are created once per device and kept until exit.
+// g-1 run on two internal streams (one per copy direction) while group g computes.  The
+// launches alternate between the caller's stream and a third internal stream, so that a
+// launch's CTAs take the SMs its predecessor's last CTAs leave (each launch ends with a
+// tail of long work items; the launches are independent: different heads, their own
+// work-item counters).  Streams and events are created once per device and kept until exit.
 constexpr int kMaxGroups = 16;
 constexpr int kMaxLaunches = kMaxGroups + 4;  // the first and last group may run as three launches
 
 struct HostPipe {
     bool ready = false;
-    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaStream_t h2d = nullptr, d2h = nullptr, comp = nullptr;
     cudaEvent_t start = nullptr, done = nullptr;
     cudaEvent_t in[kMaxLaunches] = {}, out[kMaxLaunches] = {};
     std::mutex mu;  // one call enqueues at a time per device
@@ -298,6 +301,7 @@ int host_pipe(HostPipe** out) {
         const unsigned ef = cudaEventDisableTiming;
         if (cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) != cudaSuccess ||
             cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&hp.comp, cudaStreamNonBlocking) != cudaSuccess ||
             cudaEventCreateWithFlags(&hp.start, ef) != cudaSuccess ||
             cudaEventCreateWithFlags(&hp.done, ef) != cudaSuccess)
             return RA_ERR_CUDA;
@@ -383,8 +387,10 @@ int fwd_host(const void* q_h, const void* k_h, const void* v_h, float* out_h, fl
     const size_t qh_b = 2ull * S * d, oh_b = 4ull * S * d, lh_b = 4ull * S;  // one query head's rows
     const size_t kv_b = 2ull * hkv_g * S * d;
     std::lock_guard<std::mutex> lock(hp->mu);
-    // the copies start only after the work already queued on `stream`
-    if (cudaEventRecord(hp->start, stream) != cudaSuccess || cudaStreamWaitEvent(hp->h2d, hp->start, 0) != cudaSuccess)
+    // the copies and the second compute stream start only after the work already queued on
+    // `stream`
+    if (cudaEventRecord(hp->start, stream) != cudaSuccess || cudaStreamWaitEvent(hp->h2d, hp->start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->comp, hp->start, 0) != cudaSuccess)
         return RA_ERR_CUDA;
     for (int li = 0; li < nl; ++li) {
         const int gi = L[li].g;
@@ -405,11 +411,12 @@ int fwd_host(const void* q_h, const void* k_h, const void* v_h, float* out_h, fl
         const size_t h0 = static_cast<size_t>(gi) * hq_g + L[li].h0;
         float* od = reinterpret_cast<float*>(base + off[3] + h0 * oh_b);
         float* ld = reinterpret_cast<float*>(base + off[4] + h0 * lh_b);
-        if (cudaStreamWaitEvent(stream, hp->in[li], 0) != cudaSuccess) return RA_ERR_CUDA;
+        cudaStream_t ks = (li % 2 == 0) ? stream : hp->comp;  // launches alternate between two streams
+        if (cudaStreamWaitEvent(ks, hp->in[li], 0) != cudaSuccess) return RA_ERR_CUDA;
         st = fwd_bf16(base + off[0] + h0 * qh_b, base + off[1] + gi * kv_b, base + off[2] + gi * kv_b, od, ld, S,
-                      L[li].hn, hkv_g, d, c, causal, layout, kv_block, 1, -1, 0, -1, stream);
+                      L[li].hn, hkv_g, d, c, causal, layout, kv_block, 1, -1, 0, -1, ks);
         if (st != RA_OK) return st;
-        if (cudaEventRecord(hp->out[li], stream) != cudaSuccess || cudaStreamWaitEvent(hp->d2h, hp->out[li], 0) != cudaSuccess ||
+        if (cudaEventRecord(hp->out[li], ks) != cudaSuccess || cudaStreamWaitEvent(hp->d2h, hp->out[li], 0) != cudaSuccess ||
             cudaMemcpyAsync(reinterpret_cast<char*>(out_h) + h0 * oh_b, od, L[li].hn * oh_b, cudaMemcpyDeviceToHost,
                             hp->d2h) != cudaSuccess ||
             cudaMemcpyAsync(reinterpret_cast<char*>(lse_h) + h0 * lh_b, ld, L[li].hn * lh_b, cudaMemcpyDeviceToHost,
