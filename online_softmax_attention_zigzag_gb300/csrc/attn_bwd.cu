@@ -73,9 +73,7 @@ struct BwdCfg {
     static constexpr int kBarOff = kBOff + kSlotsB * kTileBytes;
     static constexpr int kNumBars = 40;
     static constexpr int kRingOff = kBarOff + kNumBars * 8 + 16;  // item ids, loader -> other roles
-    // dk/dv: lse and D of the current query tile, per compute warpgroup (64 + 64 floats)
-    static constexpr int kLdOff = kRingOff + 16;
-    static constexpr int kSmem = kLdOff + 2 * 128 * 4 + 1024;  // + slack to align the base
+    static constexpr int kSmem = kRingOff + 16 + 1024;  // + slack to align the base
 };
 
 // Rank-major (or natural) row of natural position pos of head `head`.
@@ -692,13 +690,8 @@ __device__ void kv_mma(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uin
     }
 }
 
-// Named barrier over one compute warpgroup, no predicate.
-__device__ __forceinline__ void group_sync(int h) {
-    asm volatile("bar.sync %0, 128;" ::"r"(3 + h) : "memory");
-}
-
 template <int D>
-__device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem, float* sld, volatile int* ring, const WaitCtl& wc) {
+__device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem, volatile int* ring, const WaitCtl& wc) {
     const Ring& R = p.ring;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int h = warp / 4, wq = warp % 4;
@@ -717,58 +710,51 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
         int hk, kp;
         kv_item(p, item, hk, kp);
         const int kpos = kp + row;
-        // Each thread holds one of the warpgroup's 64 lse and 64 D values of a query tile
-        // (its 64 columns), fetched one step ahead so that the load's L2 latency hides
-        // behind a whole step instead of sitting on the chain to the next dS.
-        const float* ld_src = (row < 64 ? p.lse : p.delta) + h * 64 + (row & 63);
-        auto fetch = [&](int hq, int t0) -> float {
+        // Lane l of every warp holds -lse log2(e) and -D of query columns 2l and 2l+1 of its
+        // warpgroup's 64, fetched one step ahead (the loads' L2 latency hides behind a
+        // step); the loops take a column's value from its lane with a shuffle.  (Staged in
+        // shared memory instead, the values were read while the tensor core's operand
+        // reads held shared memory busy, which doubled the exponential loop.)
+        auto fetch = [&](int hq, int t0) -> float4 {
             const int r0 = row_of(p, hq, t0);  // first row of the query tile
-            return RA_CHECKED(r0 >= 0 && static_cast<long long>(r0) + kTile <= static_cast<long long>(R.Hq) * R.S, p.err,
-                              kSiteBwdLseRow)
-                       ? __ldg(ld_src + r0)
-                       : 0.f;
+            if (!RA_CHECKED(r0 >= 0 && static_cast<long long>(r0) + kTile <= static_cast<long long>(R.Hq) * R.S, p.err,
+                            kSiteBwdLseRow))
+                return make_float4(0.f, 0.f, 0.f, 0.f);
+            const int c = r0 + h * 64 + 2 * lane;
+            const float2 a = __ldg(reinterpret_cast<const float2*>(p.lse + c));
+            const float2 dd = __ldg(reinterpret_cast<const float2*>(p.delta + c));
+            return make_float4(-a.x * kLog2e, -a.y * kLog2e, -dd.x, -dd.y);
         };
-        float mine_next = fetch(hk * R.g, R.S - kTile);
+        float4 vals_next = fetch(hk * R.g, R.S - kTile);
         for_each_query_tile(R, hk, kp, [&](int hq, int t0) -> bool {
-            const float mine = mine_next;
+            const float4 vals = vals_next;
             int nhq, nt0;
-            if (next_query_tile(R, hk, kp, hq, t0, nhq, nt0)) mine_next = fetch(nhq, nt0);
+            if (next_query_tile(R, hk, kp, hq, t0, nhq, nt0)) vals_next = fetch(nhq, nt0);
             if (!group_wait(b.s_full, sf & 1u, h, wq, wc)) { ok = false; return false; }
             ++sf;
-            // staged as -lse log2(e) (the exponent's offset) and -D (the dS offset)
-            sld[row] = (row < 64) ? -mine * kLog2e : -mine;  // every thread is past its reads of the last tile
-            group_sync(h);
             tc_fence_after();
             float x[64];
             tmem_ld64(s_tm, x);
             const int lo = kpos - (t0 + h * 64);  // my query columns [lo, 64) see my key
-            const float4* l4 = reinterpret_cast<const float4*>(sld);
             // only tiles on the diagonal mask; branch on the warp, not per element
             if (__any_sync(0xffffffffu, R.causal && lo > 0)) {
                 const int lm = R.causal ? lo : 0;
 #pragma unroll
-                for (int i4 = 0; i4 < 16; ++i4) {
-                    const float4 lv = l4[i4];
-                    float p0, p1, p2, p3;
-                    ffma2(p0, p1, x[4 * i4], x[4 * i4 + 1], kLog2e, kLog2e, lv.x, lv.y);
-                    ffma2(p2, p3, x[4 * i4 + 2], x[4 * i4 + 3], kLog2e, kLog2e, lv.z, lv.w);
-                    const int i = 4 * i4;
-                    x[i] = (i < lm) ? 0.f : ex2(p0);
-                    x[i + 1] = (i + 1 < lm) ? 0.f : ex2(p1);
-                    x[i + 2] = (i + 2 < lm) ? 0.f : ex2(p2);
-                    x[i + 3] = (i + 3 < lm) ? 0.f : ex2(p3);
+                for (int k = 0; k < 32; ++k) {
+                    float p0, p1;
+                    ffma2(p0, p1, x[2 * k], x[2 * k + 1], kLog2e, kLog2e, __shfl_sync(0xffffffffu, vals.x, k),
+                          __shfl_sync(0xffffffffu, vals.y, k));
+                    x[2 * k] = (2 * k < lm) ? 0.f : ex2(p0);
+                    x[2 * k + 1] = (2 * k + 1 < lm) ? 0.f : ex2(p1);
                 }
             } else {
 #pragma unroll
-                for (int i4 = 0; i4 < 16; ++i4) {
-                    const float4 lv = l4[i4];
-                    float p0, p1, p2, p3;
-                    ffma2(p0, p1, x[4 * i4], x[4 * i4 + 1], kLog2e, kLog2e, lv.x, lv.y);
-                    ffma2(p2, p3, x[4 * i4 + 2], x[4 * i4 + 3], kLog2e, kLog2e, lv.z, lv.w);
-                    x[4 * i4] = ex2(p0);
-                    x[4 * i4 + 1] = ex2(p1);
-                    x[4 * i4 + 2] = ex2(p2);
-                    x[4 * i4 + 3] = ex2(p3);
+                for (int k = 0; k < 32; ++k) {
+                    float p0, p1;
+                    ffma2(p0, p1, x[2 * k], x[2 * k + 1], kLog2e, kLog2e, __shfl_sync(0xffffffffu, vals.x, k),
+                          __shfl_sync(0xffffffffu, vals.y, k));
+                    x[2 * k] = ex2(p0);
+                    x[2 * k + 1] = ex2(p1);
                 }
             }
             {
@@ -785,7 +771,6 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
             if (!group_wait(b.dp_full, dpf & 1u, h, wq, wc)) { ok = false; return false; }
             ++dpf;
             tc_fence_after();
-            const float4* d4 = reinterpret_cast<const float4*>(sld + 64);
             uint32_t pd[32];
             // dP^T in two 32-column chunks, each packed as soon as it is used, so that P, dP^T
             // and the packed words are never all live at once
@@ -795,16 +780,13 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
                 tmem_ld32(dp_tm + 32 * c, r);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i4 = 0; i4 < 8; ++i4) {
-                    const float4 nd = d4[8 * c + i4];  // -D of four query columns
-                    const int i = 32 * c + 4 * i4, k = 16 * c + 2 * i4;
-                    float a0, a1, a2, a3;
-                    fadd2(a0, a1, __uint_as_float(r[4 * i4]), __uint_as_float(r[4 * i4 + 1]), nd.x, nd.y);
-                    fadd2(a2, a3, __uint_as_float(r[4 * i4 + 2]), __uint_as_float(r[4 * i4 + 3]), nd.z, nd.w);
-                    fmul2(a0, a1, a0, a1, x[i], x[i + 1]);
-                    fmul2(a2, a3, a2, a3, x[i + 2], x[i + 3]);
+                for (int k2 = 0; k2 < 16; ++k2) {
+                    const int k = 16 * c + k2;  // query columns 2k, 2k+1: -D from lane k
+                    float a0, a1;
+                    fadd2(a0, a1, __uint_as_float(r[2 * k2]), __uint_as_float(r[2 * k2 + 1]),
+                          __shfl_sync(0xffffffffu, vals.z, k), __shfl_sync(0xffffffffu, vals.w, k));
+                    fmul2(a0, a1, a0, a1, x[2 * k], x[2 * k + 1]);
                     pd[k] = pack_bf16x2(a0, a1);
-                    pd[k + 1] = pack_bf16x2(a2, a3);
                 }
             }
             tmem_st32(dp_tm, pd);  // dS^T over the first 32 of my own dP^T columns
@@ -864,7 +846,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* ring = reinterpret_cast<volatile int*>(smem + C::kRingOff);
     if (warp < 8) {
         if constexpr (DQ) dq_compute<D>(p, b, tmem, ring, wc);
-        else kv_compute<D>(p, b, tmem, reinterpret_cast<float*>(smem + C::kLdOff) + (warp / 4) * 128, ring, wc);
+        else kv_compute<D>(p, b, tmem, ring, wc);
     } else if (warp == kMmaWarp) {  // the whole warp: see mma_ss_e
         if constexpr (DQ) dq_mma<D>(p, smem, b, tmem, ring, wc);
         else kv_mma<D>(p, smem, b, tmem, ring, wc);
