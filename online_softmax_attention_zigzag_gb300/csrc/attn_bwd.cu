@@ -715,21 +715,25 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
         // step); the loops take a column's value from its lane with a shuffle.  (Staged in
         // shared memory instead, the values were read while the tensor core's operand
         // reads held shared memory busy, which doubled the exponential loop.)
-        auto fetch = [&](int hq, int t0) -> float4 {
+        // (raw values travel a step; they are scaled where they are used, so that no
+        // instruction waits for the loads until then)
+        auto fetch = [&](int hq, int t0, float2& a, float2& dd) {
             const int r0 = row_of(p, hq, t0);  // first row of the query tile
             if (!RA_CHECKED(r0 >= 0 && static_cast<long long>(r0) + kTile <= static_cast<long long>(R.Hq) * R.S, p.err,
-                            kSiteBwdLseRow))
-                return make_float4(0.f, 0.f, 0.f, 0.f);
+                            kSiteBwdLseRow)) {
+                a = dd = make_float2(0.f, 0.f);
+                return;
+            }
             const int c = r0 + h * 64 + 2 * lane;
-            const float2 a = __ldg(reinterpret_cast<const float2*>(p.lse + c));
-            const float2 dd = __ldg(reinterpret_cast<const float2*>(p.delta + c));
-            return make_float4(-a.x * kLog2e, -a.y * kLog2e, -dd.x, -dd.y);
+            a = __ldg(reinterpret_cast<const float2*>(p.lse + c));
+            dd = __ldg(reinterpret_cast<const float2*>(p.delta + c));
         };
-        float4 vals_next = fetch(hk * R.g, R.S - kTile);
+        float2 lse_next, d_next;
+        fetch(hk * R.g, R.S - kTile, lse_next, d_next);
         for_each_query_tile(R, hk, kp, [&](int hq, int t0) -> bool {
-            const float4 vals = vals_next;
+            const float4 vals = make_float4(-lse_next.x * kLog2e, -lse_next.y * kLog2e, -d_next.x, -d_next.y);
             int nhq, nt0;
-            if (next_query_tile(R, hk, kp, hq, t0, nhq, nt0)) vals_next = fetch(nhq, nt0);
+            if (next_query_tile(R, hk, kp, hq, t0, nhq, nt0)) fetch(nhq, nt0, lse_next, d_next);
             if (!group_wait(b.s_full, sf & 1u, h, wq, wc)) { ok = false; return false; }
             ++sf;
             tc_fence_after();
