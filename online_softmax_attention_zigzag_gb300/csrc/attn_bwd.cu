@@ -716,9 +716,15 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
         // shared memory instead, the values were read while the tensor core's operand
         // reads held shared memory busy, which doubled the exponential loop.)
         // (raw values travel a step; they are scaled where they are used, so that no
-        // instruction waits for the loads until then)
+        // instruction waits for the loads until then).  The chunk map of a position is
+        // worked out once for the g heads that share it.
+        int map_t0 = -1, map_row = 0;
         auto fetch = [&](int hq, int t0, float2& a, float2& dd) {
-            const int r0 = row_of(p, hq, t0);  // first row of the query tile
+            if (t0 != map_t0) {
+                map_t0 = t0;
+                map_row = row_of(p, 0, t0);
+            }
+            const int r0 = hq * R.S + map_row;  // first row of the query tile
             if (!RA_CHECKED(r0 >= 0 && static_cast<long long>(r0) + kTile <= static_cast<long long>(R.Hq) * R.S, p.err,
                             kSiteBwdLseRow)) {
                 a = dd = make_float2(0.f, 0.f);
@@ -731,11 +737,12 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
         float2 lse_next, d_next;
         fetch(hk * R.g, R.S - kTile, lse_next, d_next);
         for_each_query_tile(R, hk, kp, [&](int hq, int t0) -> bool {
-            const float4 vals = make_float4(-lse_next.x * kLog2e, -lse_next.y * kLog2e, -d_next.x, -d_next.y);
+            const float2 lse_cur = lse_next, d_cur = d_next;
             int nhq, nt0;
             if (next_query_tile(R, hk, kp, hq, t0, nhq, nt0)) fetch(nhq, nt0, lse_next, d_next);
             if (!group_wait(b.s_full, sf & 1u, h, wq, wc)) { ok = false; return false; }
             ++sf;
+            const float4 vals = make_float4(-lse_cur.x * kLog2e, -lse_cur.y * kLog2e, -d_cur.x, -d_cur.y);
             tc_fence_after();
             float x[64];
             tmem_ld64(s_tm, x);
