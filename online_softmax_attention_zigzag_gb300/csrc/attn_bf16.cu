@@ -486,10 +486,21 @@ __device__ void mma_role(const AttnBf16Params& p, int x, uint8_t* sQ, uint8_t* s
             if (!wait_stage(s, base)) { ok = false; break; }
             // Under the document mask items are short, and P of the tile's first 64 keys
             // goes into O while the softmax finishes the rest; in the ring, all of P at once.
-            if (!mbar_wait_w(DOC ? &b.p_half[x] : &b.p_full[x], pit & 1u, wc)) { ok = false; break; }
-            if (j == 0 && !mbar_wait_w(&b.o_free[x], (qit & 1u) ^ 1u, wc)) { ok = false; break; }
+            // Each check reads shared memory, which the tensor core's operand reads keep busy
+            // (~130 cycles even when already satisfied), so the one expected to be satisfied
+            // comes first and the last arrival leads straight to the issue: on the ring the
+            // other unit's batch is usually queued before this unit's P is written; under the
+            // document mask (short items) it is usually the other way round.
             const uint32_t mine = seq + nx * (j + 1) + x;
-            if (!__all_sync(0xffffffffu, wait_turn(turn, mine, wc))) { ok = false; break; }
+            if constexpr (DOC) {
+                if (!mbar_wait_w(&b.p_half[x], pit & 1u, wc)) { ok = false; break; }
+                if (j == 0 && !mbar_wait_w(&b.o_free[x], (qit & 1u) ^ 1u, wc)) { ok = false; break; }
+                if (!__all_sync(0xffffffffu, wait_turn(turn, mine, wc))) { ok = false; break; }
+            } else {
+                if (!__all_sync(0xffffffffu, wait_turn(turn, mine, wc))) { ok = false; break; }
+                if (j == 0 && !mbar_wait_w(&b.o_free[x], (qit & 1u) ^ 1u, wc)) { ok = false; break; }
+                if (!mbar_wait_w(&b.p_full[x], pit & 1u, wc)) { ok = false; break; }
+            }
             tc_fence_after();
             if constexpr (DOC) {
                 issue_pv_part<D, 0, kTile / 32>(tmem, x, base, j > 0);

@@ -417,17 +417,24 @@ __device__ void dq_mma(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uin
         mma_commit_e(&b.b_empty[i0 % C::kSlotsB]);  // V(0) is done once dP(0) is
         for (int j = 0; j + 1 < nj && ok; ++j) {
             const uint32_t i = i0 + j;
-            // the next S as soon as this tile's S is out of TMEM, likewise dP
-            if (!mbar_wait_w(b.s_free, sf & 1u, wc)) { ok = false; break; }
+            // the next S as soon as this tile's S is out of TMEM and K(j+1) has landed,
+            // likewise dP with V(j+1); each pair is checked at once (both are usually complete
+            // already, and each check is a shared-memory read behind the tensor core's)
+            const uint32_t na = i + 1;
+            if (!mbar_wait2_w(b.s_free, sf & 1u, &b.a_full[na % C::kSlotsA], (na / C::kSlotsA) & 1u, wc)) {
+                ok = false;
+                break;
+            }
             ++sf;
-            if (!ring_wait_w(b.a_full, i + 1, C::kSlotsA, wc)) { ok = false; break; }
             tc_fence_after();
             issue_kk<D>(tmem, sQ, sA + ((i + 1) % C::kSlotsA) * C::kTileBytes);
             mma_commit_e(b.s_full);
             mma_commit_e(&b.a_empty[(i + 1) % C::kSlotsA]);
-            if (!mbar_wait_w(b.dp_free, dpf & 1u, wc)) { ok = false; break; }
+            if (!mbar_wait2_w(b.dp_free, dpf & 1u, &b.b_full[na % C::kSlotsB], (na / C::kSlotsB) & 1u, wc)) {
+                ok = false;
+                break;
+            }
             ++dpf;
-            if (!ring_wait_w(b.b_full, i + 1, C::kSlotsB, wc)) { ok = false; break; }
             tc_fence_after();
             issue_kk<D>(tmem + kTile, sdO, sB + ((i + 1) % C::kSlotsB) * C::kTileBytes);
             mma_commit_e(b.dp_full);

@@ -89,6 +89,39 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     }
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for two barrier phases at once: both are polled with non-blocking reads issued back
+// to back, so that when both have already completed the check costs one shared-memory round
+// trip instead of two; false on abort/timeout.  Every lane of the warp takes part.
+__device__ __forceinline__ bool mbar_wait2_w(uint64_t* a, uint32_t pa, uint64_t* b, uint32_t pb, const WaitCtl& w) {
+    bool da = false, db = false;
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        const bool ra = da || mbar_test_wait(a, pa);
+        const bool rb = db || mbar_test_wait(b, pb);
+        da = ra;
+        db = rb;
+        if (__all_sync(0xffffffffu, ra && rb)) return true;
+        if (i == 0) t0 = globaltimer_ns();
+        if ((i & 63u) == 63u) {
+            if (*w.abort_flag) return false;
+            if (globaltimer_ns() - t0 > w.timeout_ns) {
+                raise_abort(w, da ? b : a);
+                return false;
+            }
+        }
+    }
+}
+
 // Bounded wait that ignores the abort flag (used to drain in-flight work on abort).
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
     const uint64_t t0 = globaltimer_ns();
