@@ -65,6 +65,8 @@ CASES = [
     (8, 2, 2048, 128, 4, 1, 1, 128 ** -0.5),   # the 4-rank zigzag GQA shape
     (4, 1, 512, 128, 1, 0, 1, 128 ** -0.5),    # one rank (no ring), one KV head for all queries
     (2, 2, 256, 64, 1, 1, 1, 0.125),           # smallest zigzag: one 128-row tile per chunk
+    (8, 1, 1024, 64, 2, 1, 0, 0.125),          # g = 8 (the headline's group size), d = 64, non-causal
+    (8, 2, 1024, 128, 4, 0, 1, 128 ** -0.5),   # contiguous chunks over 4 ranks, g = 4
 ]
 
 
