@@ -5,10 +5,15 @@ and lse as the oracle computes them (float64 rounded to fp32), so that the compa
 isolates the backward.
 
 Tolerance, derived from the arithmetic: the kernel rounds P (for dV) and dS (for dQ, dK)
-to bf16, relative error at most 2^-9 each, and sums every product in fp32.  An entry
-g = sum_n a_n b_n whose factors a_n carry relative error 2^-9 is off by at most
-2^-9 * A with A = sum_n |a_n| |b_n| (oracle.backward.grad_abs_sums).  The test allows
-2^-8 * A, a factor two for fp32 summation, ex2.approx and the fp32 lse.
+to bf16, which keeps 8 significant bits (relative error at most 2^-8), and sums every
+product in fp32.  An entry g = sum_n a_n b_n whose factors a_n carry relative error 2^-8
+is off by at most 2^-8 * A with A = sum_n |a_n| |b_n| (oracle.backward.grad_abs_sums);
+fp32 summation, ex2.approx and the fp32 lse add terms some 10^4 times smaller in
+practice.  The test allows 2^-8 * A plus 1e-6 of the largest A of the tensor (entries
+whose terms nearly cancel, such as dq of a causal row that sees one key, have A ~ 0 and
+only the fp32 error), so it checks each entry at the worst case of the rounding itself:
+the largest error over the cases below is 0.93 of 2^-8 * A (d = 64 with unscaled scores,
+rows dominated by one key, where one term's rounding is the whole error).
 """
 import numpy as np
 import pytest
