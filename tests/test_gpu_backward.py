@@ -12,8 +12,9 @@ fp32 summation, ex2.approx and the fp32 lse add terms some 10^4 times smaller in
 practice.  The test allows 2^-8 * A plus 1e-6 of the largest A of the tensor (entries
 whose terms nearly cancel, such as dq of a causal row that sees one key, have A ~ 0 and
 only the fp32 error), so it checks each entry at the worst case of the rounding itself:
-apart from such entries, the largest error over the cases below is 0.93 of 2^-8 * A (d = 64 with unscaled scores,
-rows dominated by one key, where one term's rounding is the whole error).
+apart from such entries, the largest error over the cases below is 0.93 of 2^-8 * A
+(d = 64 with unscaled scores, rows dominated by one key, where one term's rounding is the
+whole error).
 """
 import numpy as np
 import pytest
