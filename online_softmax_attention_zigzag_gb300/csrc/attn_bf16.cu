@@ -640,13 +640,15 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
             const float nmu = (m == -INFINITY) ? 0.f : -m;
             float se[4] = {0.f, 0.f, 0.f, 0.f};
             float sr[4] = {0.f, 0.f, 0.f, 0.f};
+            // P goes to TMEM in four stores of 16 columns (32 keys each): a 16-word packing
+            // buffer keeps the softmax within its registers, where two 32-word ones spilled
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t pk[32];
+            for (int qq = 0; qq < 4; ++qq) {
+                uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
+                for (int i = 0; i < 16; ++i) {
                     float t0, t1;
-                    ffma2(t0, t1, s[hh * 64 + 2 * i], s[hh * 64 + 2 * i + 1], kLog2e, kLog2e, nmu, nmu);
+                    ffma2(t0, t1, s[qq * 32 + 2 * i], s[qq * 32 + 2 * i + 1], kLog2e, kLog2e, nmu, nmu);
                     const float a = ex2(t0), c2 = ex2(t1);
                     const int q2 = 2 * (i & 1);
                     fadd2(se[q2], se[q2 + 1], se[q2], se[q2 + 1], a, c2);
@@ -654,8 +656,8 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
                     add_bf16x2_f32(sr[q2], sr[q2 + 1], pk[i]);
                 }
                 // every score is in registers: P may overwrite S's upper half
-                tmem_st32(p_tmem + hh * 32, pk);
-                if (DOC && hh == 0) {  // hand the first 64 keys' P (and a rescaled O) over at once
+                tmem_st16(p_tmem + qq * 16, pk);
+                if (DOC && qq == 1) {  // hand the first 64 keys' P (and a rescaled O) over at once
                     // O is stable here: the commit that signalled this S also covered the
                     // previous P V, and this tile's P V waits for this arrival.
                     if (__any_sync(0xffffffffu, need)) {
