@@ -547,8 +547,11 @@ def main():
 
     # end to end through the C-ABI call on host buffers (ringattn_fwd_host): H2D of Q/K/V
     # from pinned memory, the attention, D2H of out and lse, every step inside the timed
-    # region; the library overlaps the copies with the attention by KV-head groups
-    e2e_steps = max(1, min(args.steps, 10))
+    # region; the library overlaps the copies with the attention by KV-head groups.  Each call
+    # is timed on its own and the median is the figure: the host link stalls now and then for
+    # tens of milliseconds whatever runs over it, so the mean (reported beside it) mostly
+    # measures how many stalls fell into the window.
+    e2e_steps = max(1, min(args.steps, 20))
     ws = torch.empty(ra.host_workspace_bytes(S, w.bhq, w.bhkv, w.d), dtype=torch.uint8, device=dev)
     for _ in range(3):   # the first call creates the copy streams; all touch every host page
         ra.fwd_host(q_h, k_h, v_h, out_h, lse_h, ws, **kw)
@@ -559,8 +562,9 @@ def main():
         ra.fwd_host(q_h, k_h, v_h, out_h, lse_h, ws, **kw)
         e2e_ev[i + 1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e2e_ev[0].elapsed_time(e2e_ev[-1]) / e2e_steps
+    e2e_mean_ms = e2e_ev[0].elapsed_time(e2e_ev[-1]) / e2e_steps
     e2e_each = [e2e_ev[i].elapsed_time(e2e_ev[i + 1]) for i in range(e2e_steps)]
+    e2e_ms = float(np.median(e2e_each))
     del ws
     if ra.sync_status() != ra.RA_OK:
         raise SystemExit("device wait timed out in the end-to-end region")
@@ -658,8 +662,9 @@ def main():
             },
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms, "steps": e2e_steps,
-                    "ms_per_step_min": min(e2e_each), "ms_per_step_median": float(np.median(e2e_each)),
+                    "ms_per_step": e2e_ms, "steps": e2e_steps, "statistic": "median of the calls' times",
+                    "ms_per_step_mean": e2e_mean_ms, "ms_per_step_min": min(e2e_each),
+                    "ms_per_step_max": max(e2e_each),
                     "call": "ringattn_fwd_host (natural order; copies overlapped with attention by KV-head groups)"},
             "context": {"overlap_condition_tokens_per_block": {
                 "pages_H100_989TFLOPs_over_450GBs_NVLink": 2198,

@@ -587,12 +587,13 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
             ++sit;
             tc_fence_after();
             float s[kTile];
+            float pm0, pm1, pm2, pm3;  // the largest score of each 32-column load
             {
                 uint32_t r0[32], r1[32], r2[32], r3[32];
-                tmem_ld32(s_tmem + 0, r0);
-                tmem_ld32(s_tmem + 32, r1);
-                tmem_ld32(s_tmem + 64, r2);
-                tmem_ld32(s_tmem + 96, r3);
+                tmem_ld32_max(s_tmem + 0, r0, pm0);
+                tmem_ld32_max(s_tmem + 32, r1, pm1);
+                tmem_ld32_max(s_tmem + 64, r2, pm2);
+                tmem_ld32_max(s_tmem + 96, r3, pm3);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
@@ -602,20 +603,24 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
                     s[96 + i] = __uint_as_float(r3[i]);
                 }
             }
+            bool masked = false;
             if constexpr (DOC) {
                 // my keys [lo, hi] are visible: my document's start up to my own position
                 const int hi = qpos - kpos, lo = doc_lo - kpos;
                 if (lo > 0 || hi < kTile - 1) {
+                    masked = true;
 #pragma unroll
                     for (int i = 0; i < kTile; ++i) s[i] = (i > hi || i < lo) ? -INFINITY : s[i];
                 }
             } else if (causal && kpos + kTile - 1 > tpos) {  // the tile may cross the diagonal
+                masked = true;
                 const int lim = qpos - kpos;                  // my keys [0, lim] are visible
 #pragma unroll
                 for (int i = 0; i < kTile; ++i) s[i] = (i > lim) ? -INFINITY : s[i];
             }
-            float mx;
-            {
+            // row max: from the loads themselves unless some score of the warp was masked
+            float mx = fmaxf(fmaxf(pm0, pm1), fmaxf(pm2, pm3));
+            if (__any_sync(0xffffffffu, masked)) {
                 float c[8];
 #pragma unroll
                 for (int a = 0; a < 8; ++a) c[a] = fmaxf(s[2 * a], s[2 * a + 1]);
