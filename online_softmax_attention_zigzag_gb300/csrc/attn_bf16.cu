@@ -33,8 +33,10 @@
 //     each unit's batch whole while one issuer's waits and commits overlap the other's
 //     batch;
 //   * warps 0-7 are two softmax warpgroups, one per unit; thread t owns row t of its
-//     unit and all 128 key columns of every score tile.  They read S from TMEM, mask,
-//     update the running max and sums with exp2, write P (bf16) back to TMEM, rescale O
+//     unit and all 128 key columns of every score tile.  They read S from TMEM (with
+//     loads that also return each thread's largest score, the row max of a tile no mask
+//     touches), mask, update the running max and sums with exp2, write P (bf16) back to
+//     TMEM, rescale O
 //     in TMEM when the running max rose by more than 2^8, and at the end write
 //     out = O / (sum of the bf16 P) and lse = m + ln(sum of the exact p).
 //   One unit's softmax overlaps the other unit's MMAs.
