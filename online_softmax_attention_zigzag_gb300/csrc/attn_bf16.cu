@@ -53,7 +53,9 @@ namespace ra {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kThreads = 352;  // 2 softmax warpgroups + two MMA warps + TMA warp
+constexpr int kThreads = 352;
+constexpr int kPBar = 1;              // named barriers kPBar + x: unit x's P hand-off on the ring
+constexpr int kPBarThreads = 4 * 32 + 32;  // its softmax warpgroup and its issuer warp
 constexpr int kMmaWarp = 8, kLoadWarp = 10;  // warp 8 + x issues the MMAs of unit x
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kItemTakers = 10;  // work-item takers: 2 MMA issuers + 8 softmax warps
@@ -501,7 +503,12 @@ __device__ void mma_role(const AttnBf16Params& p, int x, uint8_t* sQ, uint8_t* s
             } else {
                 if (!__all_sync(0xffffffffu, wait_turn(turn, mine, wc))) { ok = false; break; }
                 if (j == 0 && !mbar_wait_w(&b.o_free[x], (qit & 1u) ^ 1u, wc)) { ok = false; break; }
-                if (!mbar_wait_w(&b.p_full[x], pit & 1u, wc)) { ok = false; break; }
+                // P on the unit's named barrier: the hardware releases the issuer as the last
+                // softmax warp arrives, sooner than an mbarrier's wake (1-3% on the ring).  It
+                // cannot time out, so it is entered only while no role has given up, and the
+                // softmax role arrives once more on every way out after an abort (see there).
+                if (__any_sync(0xffffffffu, *wc.abort_flag != 0)) { ok = false; break; }
+                named_bar_sync(kPBar + x, kPBarThreads);
             }
             tc_fence_after();
             if constexpr (DOC) {
@@ -552,9 +559,23 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
     const bool causal = p.ring.causal != 0;
     uint32_t sit = 0, iit = 0;
     bool ok = true;
+    // On the ring the issuer waits for P on a hardware named barrier, which cannot time out.
+    // Every way out of this role on an abort therefore arrives on it once more: the issuer
+    // checks the abort flag before each wait, so it can be waiting at most for the tile
+    // these warps were about to handle, and that arrival lets it through.
+    auto p_abort_arrive = [&]() {
+        if constexpr (!DOC) {
+            __threadfence_block();  // the abort flag is seen by the issuer after this arrival
+            named_bar_arrive(kPBar + x, kPBarThreads);
+        }
+    };
     for (uint32_t k = 0; ok; ++k) {
         const int item = take_item(b.item_full, b.item_empty, ring, k, lane == 0, wc);
-        if (item == -2) { ok = false; break; }
+        if (__any_sync(0xffffffffu, item == -2)) {  // warp-uniform: bar.arrive takes the whole warp
+            p_abort_arrive();
+            ok = false;
+            break;
+        }
         if (item < 0) break;
         Item it;
         decode_item<DOC>(p, item, it);
@@ -585,7 +606,11 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
         float m = -INFINITY, l = 0.f, lr = 0.f;
         int j = 0;
         for_each_kv_tile<DOC>(p, it, [&](int, int kpos) -> bool {
-            if (!__all_sync(0xffffffffu, mbar_wait(&b.s_full[x], sit & 1u, wc))) { ok = false; return false; }
+            if (!__all_sync(0xffffffffu, mbar_wait(&b.s_full[x], sit & 1u, wc))) {
+                p_abort_arrive();
+                ok = false;
+                return false;
+            }
             ++sit;
             tc_fence_after();
             float s[kTile];
@@ -709,13 +734,21 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&b.p_full[x]);
+            if constexpr (DOC) {
+                mbar_arrive(&b.p_full[x]);
+            } else {
+                named_bar_arrive(kPBar + x, kPBarThreads);
+            }
             ++j;
             return true;
         });
         if (!ok) break;
         // epilogue: out = O / lr, lse = m + log2(l), both in natural-log units
-        if (!__all_sync(0xffffffffu, mbar_wait(&b.o_done[x], iit & 1u, wc))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(&b.o_done[x], iit & 1u, wc))) {
+            p_abort_arrive();
+            ok = false;
+            break;
+        }
         ++iit;
         tc_fence_after();
         const float inv = (lr > 0.f) ? 1.f / lr : 0.f;

@@ -143,6 +143,15 @@ __device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool ok) {
     return r != 0;
 }
 
+// Hardware named barrier `id` over `nthreads` threads: arrive without waiting / arrive and
+// wait for the rest.
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Wait on an mbarrier phase with every lane of the warp; the verdict is the warp's.
 __device__ __forceinline__ bool mbar_wait_w(uint64_t* bar, uint32_t parity, const WaitCtl& wc) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
