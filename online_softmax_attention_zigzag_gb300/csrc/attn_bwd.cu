@@ -176,6 +176,9 @@ __device__ __forceinline__ int count_query_tiles(const Ring& R, int hk, int kp) 
 
 // Named barrier over one compute warpgroup (128 threads); returns the AND of `ok`.
 __device__ __forceinline__ bool group_bar_and(int h, bool ok) { return named_bar_and(1 + h, 128, ok); }
+// dK/dV kernel: P^T and dS^T handed to the MMA warp on named barriers 3 and 4 (the eight
+// compute warps arrive, the MMA warp syncs)
+constexpr int kPtBar = 3, kDsBar = 4, kHandThreads = 8 * 32 + 32;
 
 // D[tmem] = A B^T with A (128 x D) and B (128 x D) both K-major in shared memory (128-byte
 // swizzle, 64-column boxes): the 128 x 128 tile products S, dP, S^T, dP^T.
@@ -659,7 +662,8 @@ __device__ void kv_mma(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uin
         for (int t = 0; t < n && ok; ++t) {
             const uint32_t i = i0 + t;
             const bool more = t + 1 < n;
-            if (!mbar_wait_w(b.pt_full, pf & 1u, wc)) { ok = false; break; }
+            if (__any_sync(0xffffffffu, *wc.abort_flag != 0)) { ok = false; break; }
+            named_bar_sync(kPtBar, kHandThreads);
             ++pf;
             if (t == 0 && !mbar_wait_w(b.acc_free, (kit & 1u) ^ 1u, wc)) { ok = false; break; }
             tc_fence_after();
@@ -673,7 +677,8 @@ __device__ void kv_mma(const AttnBwdParams& p, uint8_t* smem, const Bars& b, uin
                 issue_kk<D>(tmem, sK, sA + ((i + 1) % C::kSlotsA) * C::kTileBytes);
                 mma_commit_e(b.s_full);
             }
-            if (!mbar_wait_w(&b.ds_full[0], dsf & 1u, wc)) { ok = false; break; }
+            if (__any_sync(0xffffffffu, *wc.abort_flag != 0)) { ok = false; break; }
+            named_bar_sync(kDsBar, kHandThreads);
             ++dsf;
             tc_fence_after();
             issue_tm<D>(tmem + kAccCol + D, tmem + kTile, 64, sq, t > 0);  // dK += dS^T Q
@@ -710,9 +715,21 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
     const uint32_t dk_tm = tmem + lane_off + kAccCol + D + h * (D / 2);
     uint32_t sf = 0, dpf = 0, it = 0;
     bool ok = true;
+    // The MMA warp waits for P^T and dS^T on named barriers, which cannot time out; it
+    // checks the abort flag before each, and every way out of this role after an abort
+    // arrives once more on both, so that it is never left waiting.
+    auto abort_arrive = [&]() {
+        __threadfence_block();
+        named_bar_arrive(kPtBar, kHandThreads);
+        named_bar_arrive(kDsBar, kHandThreads);
+    };
     for (uint32_t n_it = 0; ok; ++n_it) {
         const int item = take_item(b.item_full, b.item_empty, ring, n_it, lane == 0, wc);
-        if (item == -2) { ok = false; break; }
+        if (__any_sync(0xffffffffu, item == -2)) {
+            abort_arrive();
+            ok = false;
+            break;
+        }
         if (item < 0) break;
         int hk, kp;
         kv_item(p, item, hk, kp);
@@ -747,7 +764,11 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
             const float2 lse_cur = lse_next, d_cur = d_next;
             int nhq, nt0;
             if (next_query_tile(R, hk, kp, hq, t0, nhq, nt0)) fetch(nhq, nt0, lse_next, d_next);
-            if (!group_wait(b.s_full, sf & 1u, h, wq, wc)) { ok = false; return false; }
+            if (!group_wait(b.s_full, sf & 1u, h, wq, wc)) {
+                abort_arrive();
+                ok = false;
+                return false;
+            }
             ++sf;
             const float4 vals = make_float4(-lse_cur.x * kLog2e, -lse_cur.y * kLog2e, -d_cur.x, -d_cur.y);
             tc_fence_after();
@@ -784,9 +805,13 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
                 tmem_st32(s_tm, pp);
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(b.pt_full);
+                named_bar_arrive(kPtBar, kHandThreads);
             }
-            if (!group_wait(b.dp_full, dpf & 1u, h, wq, wc)) { ok = false; return false; }
+            if (!group_wait(b.dp_full, dpf & 1u, h, wq, wc)) {
+                abort_arrive();
+                ok = false;
+                return false;
+            }
             ++dpf;
             tc_fence_after();
             uint32_t pd[32];
@@ -810,11 +835,15 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
             tmem_st32(dp_tm, pd);  // dS^T over the first 32 of my own dP^T columns
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&b.ds_full[0]);
+            named_bar_arrive(kDsBar, kHandThreads);
             return true;
         });
         if (!ok) break;
-        if (!group_wait(b.acc_done, it & 1u, h, wq, wc)) { ok = false; break; }
+        if (!group_wait(b.acc_done, it & 1u, h, wq, wc)) {
+            abort_arrive();
+            ok = false;
+            break;
+        }
         ++it;
         tc_fence_after();
         const size_t grow = static_cast<size_t>(row_of(p, hk, kp) + row);
