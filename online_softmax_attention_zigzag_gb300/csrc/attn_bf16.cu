@@ -505,8 +505,8 @@ __device__ void mma_role(const AttnBf16Params& p, int x, uint8_t* sQ, uint8_t* s
                 if (j == 0 && !mbar_wait_w(&b.o_free[x], (qit & 1u) ^ 1u, wc)) { ok = false; break; }
                 // P on the unit's named barrier: the hardware releases the issuer as the last
                 // softmax warp arrives, sooner than an mbarrier's wake (1-3% on the ring).  It
-                // cannot time out, so it is entered only while no role has given up, and the
-                // softmax role arrives once more on every way out after an abort (see there).
+                // cannot time out: it is entered only while no role has given up, after S(j) was
+                // queued, and the softmax arrives for every tile whose S it sees (see there).
                 if (__any_sync(0xffffffffu, *wc.abort_flag != 0)) { ok = false; break; }
                 named_bar_sync(kPBar + x, kPBarThreads);
             }
@@ -560,19 +560,17 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
     uint32_t sit = 0, iit = 0;
     bool ok = true;
     // On the ring the issuer waits for P on a hardware named barrier, which cannot time out.
-    // Every way out of this role on an abort therefore arrives on it once more: the issuer
-    // checks the abort flag before each wait, so it can be waiting at most for the tile
-    // these warps were about to handle, and that arrival lets it through.
-    auto p_abort_arrive = [&]() {
-        if constexpr (!DOC) {
-            __threadfence_block();  // the abort flag is seen by the issuer after this arrival
-            named_bar_arrive(kPBar + x, kPBarThreads);
-        }
+    // These warps arrive on it for every tile whose S the issuer queued (that S completes),
+    // and the issuer queues S(j+1) only after taking P(j), so no phase gets a second
+    // arrival; their waits ignore the abort flag and give up only on their own time limit,
+    // which S the issuer queued cannot reach, so the issuer is never left without P.
+    constexpr bool kFlagAware = DOC;
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, kFlagAware ? mbar_wait(bar, parity, wc) : mbar_wait_noabort(bar, parity, wc));
     };
     for (uint32_t k = 0; ok; ++k) {
-        const int item = take_item(b.item_full, b.item_empty, ring, k, lane == 0, wc);
-        if (__any_sync(0xffffffffu, item == -2)) {  // warp-uniform: bar.arrive takes the whole warp
-            p_abort_arrive();
+        const int item = take_item(b.item_full, b.item_empty, ring, k, lane == 0, wc, kFlagAware);
+        if (__any_sync(0xffffffffu, item == -2)) {
             ok = false;
             break;
         }
@@ -606,8 +604,7 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
         float m = -INFINITY, l = 0.f, lr = 0.f;
         int j = 0;
         for_each_kv_tile<DOC>(p, it, [&](int, int kpos) -> bool {
-            if (!__all_sync(0xffffffffu, mbar_wait(&b.s_full[x], sit & 1u, wc))) {
-                p_abort_arrive();
+            if (!wait(&b.s_full[x], sit & 1u)) {
                 ok = false;
                 return false;
             }
@@ -744,8 +741,7 @@ __device__ void softmax_role(const AttnBf16Params& p, int x, const Bars& b, uint
         });
         if (!ok) break;
         // epilogue: out = O / lr, lse = m + log2(l), both in natural-log units
-        if (!__all_sync(0xffffffffu, mbar_wait(&b.o_done[x], iit & 1u, wc))) {
-            p_abort_arrive();
+        if (!wait(&b.o_done[x], iit & 1u)) {
             ok = false;
             break;
         }

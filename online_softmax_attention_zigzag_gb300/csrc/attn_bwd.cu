@@ -301,9 +301,11 @@ __device__ __forceinline__ void init_bars(const Bars& b, uint32_t a_releases) {
 }
 
 // Wait (one poller warp per warpgroup, the rest in the group's named barrier).
-__device__ __forceinline__ bool group_wait(uint64_t* bar, uint32_t parity, int h, int wq, const WaitCtl& wc) {
+__device__ __forceinline__ bool group_wait(uint64_t* bar, uint32_t parity, int h, int wq, const WaitCtl& wc,
+                                           bool honour_abort = true) {
     bool ok = true;
-    if (wq == 0) ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
+    if (wq == 0)
+        ok = __all_sync(0xffffffffu, honour_abort ? mbar_wait(bar, parity, wc) : mbar_wait_noabort(bar, parity, wc));
     return group_bar_and(h, ok);
 }
 
@@ -715,21 +717,15 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
     const uint32_t dk_tm = tmem + lane_off + kAccCol + D + h * (D / 2);
     uint32_t sf = 0, dpf = 0, it = 0;
     bool ok = true;
-    // The MMA warp waits for P^T and dS^T on named barriers, which cannot time out; it
-    // checks the abort flag before each, and every way out of this role after an abort
-    // arrives once more on both, so that it is never left waiting.
-    auto abort_arrive = [&]() {
-        __threadfence_block();
-        named_bar_arrive(kPtBar, kHandThreads);
-        named_bar_arrive(kDsBar, kHandThreads);
-    };
+    // The MMA warp waits for P^T and dS^T on named barriers, which cannot time out.  These
+    // warps arrive for every tile whose S^T (for P^T) and dP^T (for dS^T) the MMA warp queued
+    // (those complete), and it queues S^T(t+1) only after taking P^T(t) and dP^T(t+1) only
+    // after taking dS^T(t), so no phase gets a second arrival; their waits ignore the abort
+    // flag and give up only on their own time limit, which products the MMA warp queued
+    // cannot reach, so it is never left without an arrival.
     for (uint32_t n_it = 0; ok; ++n_it) {
-        const int item = take_item(b.item_full, b.item_empty, ring, n_it, lane == 0, wc);
-        if (__any_sync(0xffffffffu, item == -2)) {
-            abort_arrive();
-            ok = false;
-            break;
-        }
+        const int item = take_item(b.item_full, b.item_empty, ring, n_it, lane == 0, wc, false);
+        if (item == -2) { ok = false; break; }
         if (item < 0) break;
         int hk, kp;
         kv_item(p, item, hk, kp);
@@ -764,11 +760,7 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
             const float2 lse_cur = lse_next, d_cur = d_next;
             int nhq, nt0;
             if (next_query_tile(R, hk, kp, hq, t0, nhq, nt0)) fetch(nhq, nt0, lse_next, d_next);
-            if (!group_wait(b.s_full, sf & 1u, h, wq, wc)) {
-                abort_arrive();
-                ok = false;
-                return false;
-            }
+            if (!group_wait(b.s_full, sf & 1u, h, wq, wc, false)) { ok = false; return false; }
             ++sf;
             const float4 vals = make_float4(-lse_cur.x * kLog2e, -lse_cur.y * kLog2e, -d_cur.x, -d_cur.y);
             tc_fence_after();
@@ -807,11 +799,7 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
                 tc_fence_before();
                 named_bar_arrive(kPtBar, kHandThreads);
             }
-            if (!group_wait(b.dp_full, dpf & 1u, h, wq, wc)) {
-                abort_arrive();
-                ok = false;
-                return false;
-            }
+            if (!group_wait(b.dp_full, dpf & 1u, h, wq, wc, false)) { ok = false; return false; }
             ++dpf;
             tc_fence_after();
             uint32_t pd[32];
@@ -839,11 +827,7 @@ __device__ void kv_compute(const AttnBwdParams& p, const Bars& b, uint32_t tmem,
             return true;
         });
         if (!ok) break;
-        if (!group_wait(b.acc_done, it & 1u, h, wq, wc)) {
-            abort_arrive();
-            ok = false;
-            break;
-        }
+        if (!group_wait(b.acc_done, it & 1u, h, wq, wc, false)) { ok = false; break; }
         ++it;
         tc_fence_after();
         const size_t grow = static_cast<size_t>(row_of(p, hk, kp) + row);

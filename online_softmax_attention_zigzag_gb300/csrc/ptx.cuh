@@ -89,6 +89,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     }
 }
 
+// As mbar_wait, but gives up only when its own time limit runs out, not when another role
+// has raised the abort flag (it still raises the flag itself).  For the roles that feed a
+// named barrier: they keep arriving for every tile whose gating MMA was issued, so that a
+// waiter on that barrier is never left without its arrival.
+__device__ __forceinline__ bool mbar_wait_noabort(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0u && globaltimer_ns() - t0 > w.timeout_ns) {
+            raise_abort(w, bar);
+            return false;
+        }
+    }
+}
+
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -181,9 +197,10 @@ __device__ __forceinline__ int publish_item(unsigned int* counter, int n_items, 
 // Every taker takes every entry, in order; one arrival per taker (`leader`: one lane of
 // a warp, or a lone issuing thread) frees the slot.
 __device__ __forceinline__ int take_item(uint64_t* full, uint64_t* empty, const volatile int* ring, uint32_t k,
-                                         bool leader, const WaitCtl& wc) {
+                                         bool leader, const WaitCtl& wc, bool honour_abort = true) {
     const uint32_t slot = k % kItemRing;
-    if (!mbar_wait(&full[slot], (k / kItemRing) & 1u, wc)) return -2;
+    const uint32_t par = (k / kItemRing) & 1u;
+    if (!(honour_abort ? mbar_wait(&full[slot], par, wc) : mbar_wait_noabort(&full[slot], par, wc))) return -2;
     const int item = ring[slot];
     __syncwarp(__activemask());
     if (leader) mbar_arrive(&empty[slot]);
