@@ -81,3 +81,25 @@ def test_whole_job_value_counts_every_replica():
     one = bench.whole_job_value(1e12, 1, 1000.0)
     assert abs(one - 1.0) < 1e-12
     assert abs(bench.whole_job_value(1e12, 4, 1000.0) - 4.0) < 1e-12
+
+
+def test_code_fingerprint_ignores_comments_only(tmp_path, monkeypatch):
+    """The traffic record is keyed by a fingerprint of the attention kernel's code: editing a
+    comment keeps it, editing code changes it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src = open(bench.ATTN_SRC, encoding="utf-8").read()
+    base = tmp_path / "a.cu"
+    base.write_text(src, encoding="utf-8")
+    monkeypatch.setattr(bench, "ATTN_SRC", str(base))
+    h0 = bench.src_hash()
+    commented = tmp_path / "b.cu"
+    commented.write_text("// a new comment line\n" + src.replace("namespace ra {", "namespace ra {  /* note */", 1),
+                         encoding="utf-8")
+    monkeypatch.setattr(bench, "ATTN_SRC", str(commented))
+    assert bench.src_hash() == h0
+    changed = tmp_path / "c.cu"
+    changed.write_text(src.replace("constexpr int kThreads = 352;", "constexpr int kThreads = 384;", 1),
+                       encoding="utf-8")
+    monkeypatch.setattr(bench, "ATTN_SRC", str(changed))
+    assert bench.src_hash() != h0
