@@ -36,7 +36,7 @@
 //     unit and all 128 key columns of every score tile.  They read S from TMEM (with
 //     loads that also return each thread's largest score, the row max of a tile no mask
 //     touches), mask, update the running max and sums with exp2, write P (bf16) back to
-//     TMEM, rescale O
+//     TMEM (and hand it to the issuer: on a named barrier on the ring), rescale O
 //     in TMEM when the running max rose by more than 2^8, and at the end write
 //     out = O / (sum of the bf16 P) and lse = m + ln(sum of the exact p).
 //   One unit's softmax overlaps the other unit's MMAs.
@@ -87,7 +87,8 @@ struct Bars {
     uint64_t* q_full;    // [2] loader -> mma (TMA bytes)
     uint64_t* q_empty;   // [2] mma -> loader (last S MMA of an item done)
     uint64_t* s_full;    // [2] mma -> softmax
-    uint64_t* p_full;    // [2] softmax (128 threads) -> mma: all of P written
+    uint64_t* p_full;    // [2] softmax (128 threads) -> mma: all of P written (document mask; the
+                         //     ring hands P over on named barrier kPBar + x instead)
     uint64_t* p_half;    // [2] softmax (128 threads) -> mma: P of keys [0, 64) written (and O rescaled)
     uint64_t* o_done;    // [2] mma -> softmax (last PV of an item done)
     uint64_t* o_free;    // [2] softmax (128 threads) -> mma (O read out)

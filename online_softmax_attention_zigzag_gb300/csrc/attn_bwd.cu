@@ -259,8 +259,9 @@ struct Bars {
     uint64_t *res_full, *res_empty;  // resident tiles landed / item's MMAs done with them
     uint64_t *s_full, *dp_full;      // S (S^T) / dP (dP^T) in TMEM
     uint64_t *s_free, *dp_free;      // 256 compute threads copied S / dP out of TMEM
-    uint64_t *ds_full;               // [2] dq: dS buffer written; dk/dv: [0] dS^T written
-    uint64_t *pt_full;               // dk/dv: P^T written (the same barrier as ds_full[1])
+    uint64_t *ds_full;               // [2] dq: dS buffer written (the dk/dv kernel hands dS^T
+                                     //     and P^T over on named barriers kDsBar and kPtBar)
+    uint64_t *pt_full;               // the same barrier as ds_full[1]; unused by the dk/dv kernel
     uint64_t *acc_done, *acc_free, *drain, *drain2;
     uint64_t *ds_free;  // [2] dQ kernel: the dQ product that read dS buffer b is done
     uint64_t *a_full, *a_empty, *b_full, *b_empty;
