@@ -334,9 +334,6 @@ __device__ __forceinline__ bool ring_load(uint8_t* ring, uint64_t* full, uint64_
     return true;
 }
 
-__device__ __forceinline__ bool ring_wait(uint64_t* full, uint32_t i, int n, const WaitCtl& wc) {
-    return mbar_wait(&full[i % n], (i / n) & 1u, wc);
-}
 __device__ __forceinline__ bool ring_wait_w(uint64_t* full, uint32_t i, int n, const WaitCtl& wc) {
     return mbar_wait_w(&full[i % n], (i / n) & 1u, wc);
 }
