@@ -118,6 +118,11 @@ def _stream(stream) -> int:
 def _dev(t: torch.Tensor, name: str, dtype=None):
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        # the library launches on the current device; another device's pointer would reach
+        # its kernels as a foreign address
+        raise ValueError(f"{name} is on {t.device}, but the current device is "
+                         f"cuda:{torch.cuda.current_device()}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:

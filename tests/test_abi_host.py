@@ -191,3 +191,24 @@ def test_rank_work_zigzag_balanced_contiguous_skewed(ra):
     assert len(set(u)) == 1 and u[0] == 17 and len(set(p)) == 1 and len(set(t)) == 1
     u, p, t = ra.rank_work(32768, 8, 1, 0, 128)
     assert list(u) == list(range(1, 9))
+
+
+def test_binding_rejects_a_tensor_on_another_device(ra, monkeypatch):
+    """The binding passes raw device pointers to kernels launched on the current device, so a
+    tensor on another device is refused before any call (stand-in tensors: no GPU here)."""
+    from unittest import mock
+    import torch
+
+    def fake(index):
+        t = mock.MagicMock(spec=torch.Tensor)
+        t.is_cuda = True
+        t.device = torch.device("cuda", index)
+        t.dtype = torch.float32
+        t.is_contiguous.return_value = True
+        t.data_ptr.return_value = 4096
+        return t
+
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    assert ra._dev(fake(0), "x", torch.float32).value == 4096
+    with pytest.raises(ValueError, match="current device is cuda:0"):
+        ra._dev(fake(1), "x", torch.float32)
