@@ -162,12 +162,14 @@ class ClockSampler:
 CPU_UNIT_ROWS = 4096  # query rows per timed unit of the CPU oracle (one full_attention_rows call)
 
 
-def cpu_oracle_units(w, qkv, budget_s: float, first_unit: int = 0, min_units: int = 1):
+def cpu_oracle_units(w, qkv, budget_s: float, first_unit: int = 0, min_units: int = 1, check=None):
     """Time the float64 oracle on units of CPU_UNIT_ROWS seeded random query rows of
     workload ``w`` (unit i draws its rows with seed 7000 + i), until ``budget_s`` seconds
     of oracle time and at least ``min_units`` units are spent.  Returns a list of
     (flop, seconds) per unit.  Input generation is not timed.  The GPU arm's cpu_baseline
-    and the reference arm both time these units, so they report the same quantity."""
+    and the reference arm both time these units, so they report the same quantity.
+    ``check(heads, positions, out, lse)``, if given, receives each unit's oracle rows
+    after its timing."""
     from oracle.attention import full_attention_rows
     q, k, v = qkv
     res, spent, i = [], 0.0, first_unit
@@ -177,12 +179,55 @@ def cpu_oracle_units(w, qkv, budget_s: float, first_unit: int = 0, min_units: in
         keys = (ps + 1) if w.causal else np.full_like(ps, w.seq)
         flop = float(np.sum(4.0 * w.d * keys))
         t0 = time.perf_counter()
-        full_attention_rows(q, k, v, hs, ps, bool(w.causal))
+        o, l = full_attention_rows(q, k, v, hs, ps, bool(w.causal))
         dt = time.perf_counter() - t0
         res.append((flop, dt))
         spent += dt
         i += 1
+        if check is not None:
+            check(hs, ps, o, l)
     return res
+
+
+# bf16 tolerances on the output and the natural-log lse (max abs error)
+TOL_OUT, TOL_LSE = 2e-2, 1e-3
+
+
+class RowParity:
+    """Max abs error of a natural-order GPU result held in host memory (out [BH, S, d],
+    lse [BH, S]) against the oracle rows that the cpu_baseline leg computes anyway.  A
+    failure inside the comparison is recorded, never raised, so that it cannot cost the
+    bench its line."""
+
+    def __init__(self, out_h: torch.Tensor, lse_h: torch.Tensor, source: str):
+        self.out_h, self.lse_h, self.source = out_h, lse_h, source
+        self.rows, self.nonfinite = 0, 0
+        self.err_out, self.err_lse = 0.0, 0.0
+        self.error = None
+
+    def __call__(self, hs, ps, o, l):
+        try:
+            h = torch.from_numpy(np.asarray(hs, dtype=np.int64))
+            pos = torch.from_numpy(np.asarray(ps, dtype=np.int64))
+            go = self.out_h[h, pos].to(torch.float64).numpy()
+            gl = self.lse_h[h, pos].to(torch.float64).numpy()
+            finite = np.isfinite(go).all(axis=1) & np.isfinite(gl)
+            self.nonfinite += int(np.count_nonzero(~finite))
+            if finite.any():
+                self.err_out = max(self.err_out, float(np.max(np.abs(go[finite] - o[finite]))))
+                self.err_lse = max(self.err_lse, float(np.max(np.abs(gl[finite] - l[finite]))))
+            self.rows += len(h)
+        except Exception as e:  # recorded in the line instead
+            self.error = f"{type(e).__name__}: {e}"
+
+    def summary(self) -> dict:
+        ok = (self.error is None and self.rows > 0 and self.nonfinite == 0
+              and self.err_out <= TOL_OUT and self.err_lse <= TOL_LSE)
+        return {"output_of": self.source, "rows": self.rows,
+                "sample": "the cpu_baseline leg's seeded random query rows",
+                "max_abs_err_out": self.err_out, "max_abs_err_lse": self.err_lse,
+                "nonfinite_rows": self.nonfinite, "tolerance": {"out": TOL_OUT, "lse": TOL_LSE},
+                "within_tolerance": ok, "error": self.error}
 
 
 def cpu_threads() -> int:
@@ -631,8 +676,12 @@ def main():
         extra.append({"mode": "per-rank launches", "per_rank": per_rank(ra, [CAUSAL_MHA_S4K], dev, stream)})
 
     cpu = None
+    parity = None
     if rank == 0 and not args.no_cpu_baseline:
-        units = cpu_oracle_units(w, (q_h, k_h, v_h), args.cpu_seconds)
+        # the last end-to-end call left its natural-order result in out_h, lse_h
+        check = RowParity(out_h, lse_h, "ringattn_fwd_host (the last end-to-end call)")
+        units = cpu_oracle_units(w, (q_h, k_h, v_h), args.cpu_seconds, check=check)
+        parity = check.summary()
         secs = sum(t for _, t in units)
         cpu = {"value": sum(f for f, _ in units) / secs / 1e12, "unit": UNIT, "cores": cpu_threads(),
                "kind": "oracle",
@@ -668,6 +717,7 @@ def main():
                               "kernel_ms": perm_ms, "bytes": perm_bytes},
             },
             "cpu_baseline": cpu,
+            "parity": parity,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "steps": e2e_steps, "statistic": "median of the calls' times",
                     "ms_per_step_mean": e2e_mean_ms, "ms_per_step_min": min(e2e_each),

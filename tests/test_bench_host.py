@@ -103,3 +103,51 @@ def test_code_fingerprint_ignores_comments_only(tmp_path, monkeypatch):
                        encoding="utf-8")
     monkeypatch.setattr(bench, "ATTN_SRC", str(changed))
     assert bench.src_hash() != h0
+
+
+def _row_parity_case():
+    """A small causal GQA case whose 'device result' is the oracle's own, in host float32."""
+    from types import SimpleNamespace
+    from oracle.attention import full_attention
+    g = torch.Generator().manual_seed(41)
+    q = torch.randn((4, 48, 16), generator=g).to(torch.bfloat16)
+    k = torch.randn((2, 48, 16), generator=g).to(torch.bfloat16)
+    v = torch.randn((2, 48, 16), generator=g).to(torch.bfloat16)
+    o, l = full_attention(*(x.double().numpy() for x in (q, k, v)), True)
+    w = SimpleNamespace(bhq=4, seq=48, causal=1, d=16)
+    return w, (q, k, v), torch.from_numpy(o).float(), torch.from_numpy(l).float()
+
+
+def test_bench_row_parity_reports_the_sampled_rows():
+    """The bench line's `parity` entry: the cpu_baseline leg's oracle rows against a result in
+    host memory -- exact agreement passes, a planted error or a NaN row fails, and a failure
+    inside the comparison is recorded instead of raised."""
+    sys.path.insert(0, ROOT)
+    import bench
+    w, qkv, out_h, lse_h = _row_parity_case()
+
+    check = bench.RowParity(out_h, lse_h, "host copy")
+    units = bench.cpu_oracle_units(w, qkv, 0.0, min_units=2, check=check)
+    s = check.summary()
+    assert len(units) == 2 and s["rows"] == 2 * 4 * 48   # each unit samples every row here
+    assert s["within_tolerance"] and s["error"] is None and s["nonfinite_rows"] == 0
+    assert s["max_abs_err_out"] < 1e-6 and s["max_abs_err_lse"] < 1e-5
+
+    bad = out_h.clone()
+    bad[3, 47, 5] += 0.05
+    check = bench.RowParity(bad, lse_h, "host copy")
+    bench.cpu_oracle_units(w, qkv, 0.0, check=check)
+    s = check.summary()
+    assert not s["within_tolerance"] and abs(s["max_abs_err_out"] - 0.05) < 1e-3
+
+    nan = lse_h.clone()
+    nan[1, 0] = float("nan")
+    check = bench.RowParity(out_h, nan, "host copy")
+    bench.cpu_oracle_units(w, qkv, 0.0, check=check)
+    s = check.summary()
+    assert s["nonfinite_rows"] == 1 and not s["within_tolerance"]
+
+    check = bench.RowParity(out_h[:, :8], lse_h, "host copy")   # too short: indexing fails
+    bench.cpu_oracle_units(w, qkv, 0.0, check=check)
+    s = check.summary()
+    assert s["error"] is not None and not s["within_tolerance"]
