@@ -1,4 +1,5 @@
-"""The per-rank ring computation, restated step by step in float64 (oracle side).
+"""The per-rank ring computation, restated step by step in float64 (oracle side; test
+infrastructure only).
 
 Follows "Ring Attention and Ulysses shard a sequence two different ways..."
 (section "Ring Attention: point-to-point rotation, and an online softmax that
