@@ -44,7 +44,9 @@ UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-ATTN_SRC = os.path.join(ROOT, "online_softmax_attention_zigzag_gb300", "csrc", "attn_bf16.cu")
+# the attention kernel's source and the headers it includes (its device code lives in all three)
+KERNEL_SRCS = tuple(os.path.join(ROOT, "online_softmax_attention_zigzag_gb300", "csrc", f)
+                    for f in ("attn_bf16.cu", "ptx.cuh", "internal.h"))
 
 
 def parse():
@@ -80,15 +82,22 @@ def peaks():
     return FALLBACK_BF16_TFLOPS, None, FALLBACK_HBM_GBS, "fallback"
 
 
-def src_hash() -> str:
-    """Fingerprint of the attention kernel's code: SHA-256 of its source with the comments
-    and blank lines taken out, so that a comment edit keeps a recorded traffic figure."""
-    with open(ATTN_SRC, encoding="utf-8") as f:
-        text = f.read()
+def _code_only(text: str) -> str:
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     lines = (re.sub(r"//.*", "", ln).rstrip() for ln in text.splitlines())
-    code = "\n".join(ln for ln in lines if ln.strip())
-    return hashlib.sha256(code.encode()).hexdigest()[:16]
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
+def src_hash() -> str:
+    """Fingerprint of the attention kernel's code: SHA-256 of its source file and the
+    headers it includes, each with the comments and blank lines taken out, so that a
+    comment edit keeps a recorded traffic figure and any code edit drops it."""
+    h = hashlib.sha256()
+    for path in KERNEL_SRCS:
+        with open(path, encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
+        h.update(b"\0")
+    return h.hexdigest()[:16]
 
 
 def traffic_for(workload: str):
@@ -99,7 +108,7 @@ def traffic_for(workload: str):
     with open(TRAFFIC_FILE) as f:
         j = json.load(f)
     e = j.get(workload)
-    if not e or e.get("attn_bf16_code_sha256_16") != src_hash():
+    if not e or e.get("attn_kernel_code_sha256_16") != src_hash():
         return None
     return e.get("dram_bytes_per_launch")
 

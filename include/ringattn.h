@@ -42,10 +42,10 @@
  *    CUDA runtime call or launch failed.  Device-side waits are bounded; one that
  *    runs out records RA_ERR_TIMEOUT, read with ringattn_sync_status.  The limit is
  *    the environment variable RINGATTN_WAIT_TIMEOUT_MS, read once per process (default
- *    2000, clamped to 1 .. 600000); the waits of the warps that feed a hardware named
- *    barrier (forward P hand-off, backward P^T and dS^T hand-offs) take at least 10 s
- *    whatever it says, since the waiting side of such a barrier cannot give up.  No
- *    exception crosses the ABI and there is no CPU fallback.
+ *    2000, clamped to 1000 .. 600000).  It is never below 1 s because the warps that
+ *    feed a hardware named barrier (forward P hand-off, backward P^T and dS^T hand-offs)
+ *    stop arriving only when it runs out, and the waiting side of such a barrier cannot
+ *    give up.  No exception crosses the ABI and there is no CPU fallback.
  *  - Check build: the same sources compiled with -DRA_CHECK give libringattn_check.so,
  *    the same ABI with an index check at every place a kernel derives a memory index
  *    from the chunk and work-item arithmetic (TMA row coordinates, output rows, document

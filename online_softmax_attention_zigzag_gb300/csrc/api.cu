@@ -130,11 +130,14 @@ int encode_bf16_map(CUtensorMap* map, const void* base, long long rows, int d, i
     return r == CUDA_SUCCESS ? RA_OK : RA_ERR_CUDA;
 }
 
+// The attention kernels' wait limit.  Never below 1 s: the warps that feed a hardware
+// named barrier (whose waiter cannot give up) stop arriving only when their own limit runs
+// out, so that limit must stay far above the time a queued MMA takes to complete.
 unsigned long long wait_timeout_ns() {
     static unsigned long long ns = [] {
         const char* e = std::getenv("RINGATTN_WAIT_TIMEOUT_MS");
         long long ms = e ? std::atoll(e) : 2000;
-        if (ms < 1) ms = 1;
+        if (ms < 1000) ms = 1000;
         if (ms > 600000) ms = 600000;
         return static_cast<unsigned long long>(ms) * 1000000ull;
     }();

@@ -92,17 +92,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
 // As mbar_wait, but gives up only when its own time limit runs out, not when another role
 // has raised the abort flag (it still raises the flag itself).  For the roles that feed a
 // named barrier: they keep arriving for every tile whose gating MMA was issued, so that a
-// waiter on that barrier is never left without its arrival.  Their limit is never below
-// 10 s, whatever limit the caller set, so that a queued MMA always completes within it, even
-// while the GPU runs other contexts for a while.
-constexpr uint64_t kFeederMinTimeoutNs = 10000000000ull;
+// waiter on that barrier is never left without its arrival.  The host never sets a limit
+// below 1 s, far above the time a queued MMA takes to complete.
 __device__ __forceinline__ bool mbar_wait_noabort(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    const uint64_t limit = w.timeout_ns > kFeederMinTimeoutNs ? w.timeout_ns : kFeederMinTimeoutNs;
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0u && globaltimer_ns() - t0 > limit) {
+        if ((i & 63u) == 0u && globaltimer_ns() - t0 > w.timeout_ns) {
             raise_abort(w, bar);
             return false;
         }

@@ -84,25 +84,33 @@ def test_whole_job_value_counts_every_replica():
 
 
 def test_code_fingerprint_ignores_comments_only(tmp_path, monkeypatch):
-    """The traffic record is keyed by a fingerprint of the attention kernel's code: editing a
-    comment keeps it, editing code changes it."""
+    """The traffic record is keyed by a fingerprint of the attention kernel's code (its source
+    and the headers it includes): editing a comment keeps it, editing code in any of the files
+    changes it."""
     sys.path.insert(0, ROOT)
     import bench
-    src = open(bench.ATTN_SRC, encoding="utf-8").read()
-    base = tmp_path / "a.cu"
-    base.write_text(src, encoding="utf-8")
-    monkeypatch.setattr(bench, "ATTN_SRC", str(base))
-    h0 = bench.src_hash()
-    commented = tmp_path / "b.cu"
-    commented.write_text("// a new comment line\n" + src.replace("namespace ra {", "namespace ra {  /* note */", 1),
-                         encoding="utf-8")
-    monkeypatch.setattr(bench, "ATTN_SRC", str(commented))
-    assert bench.src_hash() == h0
-    changed = tmp_path / "c.cu"
-    changed.write_text(src.replace("constexpr int kThreads = 352;", "constexpr int kThreads = 384;", 1),
-                       encoding="utf-8")
-    monkeypatch.setattr(bench, "ATTN_SRC", str(changed))
-    assert bench.src_hash() != h0
+    srcs = [open(p, encoding="utf-8").read() for p in bench.KERNEL_SRCS]
+
+    def fingerprint(texts, tag):
+        paths = []
+        for i, t in enumerate(texts):
+            q = tmp_path / f"{tag}_{i}"
+            q.write_text(t, encoding="utf-8")
+            paths.append(str(q))
+        monkeypatch.setattr(bench, "KERNEL_SRCS", tuple(paths))
+        return bench.src_hash()
+
+    h0 = fingerprint(srcs, "base")
+    assert h0 == fingerprint(srcs, "again")
+    commented = ["// a new comment line\n" + srcs[0].replace("namespace ra {", "namespace ra {  /* note */", 1)]
+    commented += [srcs[1] + "\n// trailing note\n", srcs[2]]
+    assert fingerprint(commented, "commented") == h0
+    changed = [srcs[0].replace("constexpr int kThreads = 352;", "constexpr int kThreads = 384;", 1)] + srcs[1:]
+    assert changed[0] != srcs[0] and fingerprint(changed, "kernel") != h0
+    marker = "__device__ __forceinline__ bool mbar_wait_noabort("
+    assert marker in srcs[1]
+    header = [srcs[0], srcs[1].replace(marker, "__device__ __noinline__ bool mbar_wait_noabort(", 1), srcs[2]]
+    assert fingerprint(header, "header") != h0
 
 
 def _row_parity_case():
